@@ -1,0 +1,269 @@
+"""Python binding of libblockmoe.so, the fused block-scaled MoE layer for GB300 (sm_103a).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Functions carry the C ABI's names (include/blockmoe.h); the
+`BlockScaledMoE` class wraps a handle for torch tensors (torch provides device
+memory and streams).  Importing the package does not need a GPU; loading the
+library raises if it has not been built, and there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "lib", "libblockmoe.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "blockmoe.h")
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _header_constants() -> dict:
+    out = {}
+    with open(HEADER) as f:
+        for m in re.finditer(r"#define\s+(MOE_\w+)\s+\(?(-?(?:0x)?[0-9a-fA-F]+)u?\)?", f.read()):
+            out[m.group(1)] = int(m.group(2), 0)
+    return out
+
+
+C = _header_constants()
+globals().update(C)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+def load(path: Optional[str] = None):
+    """Load libblockmoe.so (built in-tree by `__graft_entry__.build()`)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError(f"libblockmoe.so is not built ({p}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(p)
+        vp, i32, f64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_size_t
+        lib.moe_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32]
+        lib.moe_create.restype = i32
+        lib.moe_bind_weights.argtypes = [vp, vp, vp, vp, vp]
+        lib.moe_bind_weights.restype = i32
+        lib.moe_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp]
+        lib.moe_forward.restype = i32
+        lib.moe_destroy.argtypes = [vp]
+        lib.moe_destroy.restype = None
+        lib.moe_set_option.argtypes = [vp, i32, f64]
+        lib.moe_set_option.restype = i32
+        lib.moe_get_option.argtypes = [vp, i32, ctypes.POINTER(f64)]
+        lib.moe_get_option.restype = i32
+        lib.moe_workspace_bytes.argtypes = [vp]
+        lib.moe_workspace_bytes.restype = sz
+        lib.moe_set_workspace.argtypes = [vp, vp, sz]
+        lib.moe_set_workspace.restype = i32
+        lib.moe_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+        lib.moe_read_status.restype = i32
+        lib.moe_last_error.argtypes = [vp]
+        lib.moe_last_error.restype = ctypes.c_char_p
+        lib.moe_dispatch_scheme.argtypes = [vp]
+        lib.moe_dispatch_scheme.restype = i32
+        lib.moe_debug_copy.argtypes = [vp, i32, vp, ctypes.POINTER(sz), vp]
+        lib.moe_debug_copy.restype = i32
+        _lib = lib
+        return lib
+
+
+def exported_symbols_from_header() -> list:
+    """Names of the functions include/blockmoe.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return re.findall(r"^\s*(?:int|void|size_t|const char\*)\s+(moe_\w+)\s*\(", text, flags=re.M)
+
+
+# ---------------------------------------------------------------- C ABI names
+
+def _check(h, rc: int):
+    if rc != 0:
+        msg = load().moe_last_error(h)
+        raise MoeError(rc, msg.decode() if msg else "")
+
+
+def moe_create(H: int, I: int, E: int, topk: int, capacity: int):
+    lib = load()
+    h = ctypes.c_void_p()
+    rc = lib.moe_create(ctypes.byref(h), H, I, E, topk, capacity)
+    _check(None, rc)
+    return h
+
+
+def moe_bind_weights(h, w13_fp4: int, w13_sf: int, w2_fp4: int, w2_sf: int):
+    _check(h, load().moe_bind_weights(h, w13_fp4, w13_sf, w2_fp4, w2_sf))
+
+
+def moe_forward(h, x: int, topk_ids: int, topk_weights: int, num_valid_rows: Optional[int], out: int, T: int,
+                stream: int = 0):
+    _check(h, load().moe_forward(h, x, topk_ids, topk_weights, num_valid_rows, out, T, stream))
+
+
+def moe_destroy(h):
+    load().moe_destroy(h)
+
+
+def moe_set_option(h, key: int, value: float):
+    _check(h, load().moe_set_option(h, key, float(value)))
+
+
+def moe_get_option(h, key: int) -> float:
+    v = ctypes.c_double()
+    _check(h, load().moe_get_option(h, key, ctypes.byref(v)))
+    return v.value
+
+
+def moe_workspace_bytes(h) -> int:
+    return load().moe_workspace_bytes(h)
+
+
+def moe_set_workspace(h, ptr: int, nbytes: int):
+    _check(h, load().moe_set_workspace(h, ptr, nbytes))
+
+
+def moe_read_status(h, stream: int = 0) -> int:
+    v = ctypes.c_uint32()
+    _check(h, load().moe_read_status(h, ctypes.byref(v), stream))
+    return v.value
+
+
+def moe_last_error(h=None) -> str:
+    m = load().moe_last_error(h)
+    return m.decode() if m else ""
+
+
+def moe_dispatch_scheme(h) -> int:
+    return load().moe_dispatch_scheme(h)
+
+
+def moe_debug_copy(h, which: int, stream: int = 0) -> bytes:
+    lib = load()
+    n = ctypes.c_size_t(0)
+    _check(h, lib.moe_debug_copy(h, which, None, ctypes.byref(n), stream))
+    buf = ctypes.create_string_buffer(max(n.value, 1))
+    _check(h, lib.moe_debug_copy(h, which, buf, ctypes.byref(n), stream))
+    return buf.raw[: n.value]
+
+
+# ---------------------------------------------------------------- torch wrapper
+
+class BlockScaledMoE:
+    """One layer instance: torch tensors in, torch tensors out (CUDA, contiguous)."""
+
+    def __init__(self, H: int, I: int, E: int, topk: int, capacity: int, *, dispatch: Optional[str] = None,
+                 swiglu_limit: float = 0.0, route_tile: int = 0, debug: bool = False,
+                 fixed_slot_max: Optional[int] = None, workspace=None):
+        self.H, self.I, self.E, self.topk, self.capacity = H, I, E, topk, capacity
+        self.h = moe_create(H, I, E, topk, capacity)
+        try:
+            if fixed_slot_max is not None:
+                moe_set_option(self.h, MOE_OPT_FIXED_SLOT_MAX, fixed_slot_max)
+            if dispatch is not None:
+                moe_set_option(self.h, MOE_OPT_DISPATCH,
+                               {"auto": MOE_DISPATCH_AUTO, "fixed": MOE_DISPATCH_FIXED,
+                                "compact": MOE_DISPATCH_COMPACT}[dispatch])
+            if route_tile:
+                moe_set_option(self.h, MOE_OPT_ROUTE_TILE, route_tile)
+            if debug:
+                moe_set_option(self.h, MOE_OPT_DEBUG_CAPTURE, 1)
+            moe_set_option(self.h, MOE_OPT_SWIGLU_LIMIT, swiglu_limit)
+            if workspace is not None:
+                moe_set_workspace(self.h, workspace.data_ptr(), workspace.numel() * workspace.element_size())
+        except Exception:
+            moe_destroy(self.h)
+            self.h = None
+            raise
+        self._weights = None
+
+    def close(self):
+        if getattr(self, "h", None) is not None:
+            moe_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def scheme(self) -> str:
+        return "fixed" if moe_dispatch_scheme(self.h) == MOE_DISPATCH_FIXED else "compact"
+
+    @property
+    def workspace_bytes(self) -> int:
+        return moe_workspace_bytes(self.h)
+
+    def _dev(self, t, name, shape, dtypes):
+        import torch
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (strided views are refused, not copied)")
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+        if t.dtype not in dtypes:
+            raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+        return t.data_ptr()
+
+    def bind_weights(self, w13, w13_sf, w2, w2_sf):
+        import torch
+        E, H, I = self.E, self.H, self.I
+        fp4 = (torch.uint8,) + ((torch.float4_e2m1fn_x2,) if hasattr(torch, "float4_e2m1fn_x2") else ())
+        sf = (torch.uint8,) + ((torch.float8_e8m0fnu,) if hasattr(torch, "float8_e8m0fnu") else ())
+        ptrs = (self._dev(w13, "w13", (E, 2 * I, H // 2), fp4), self._dev(w13_sf, "w13_sf", (E, 2 * I, H // 32), sf),
+                self._dev(w2, "w2", (E, H, I // 2), fp4), self._dev(w2_sf, "w2_sf", (E, H, I // 32), sf))
+        moe_bind_weights(self.h, *ptrs)
+        self._weights = (w13, w13_sf, w2, w2_sf)  # keep caller tensors alive while bound
+
+    def forward(self, x, topk_ids, topk_weights, num_valid_rows=None, out=None, stream=None):
+        import torch
+        T = x.shape[0]
+        xp = self._dev(x, "x", (T, self.H), (torch.bfloat16,))
+        ip = self._dev(topk_ids, "topk_ids", (T, self.topk), (torch.int32,))
+        wp = self._dev(topk_weights, "topk_weights", (T, self.topk), (torch.float32,))
+        nvr = None
+        if num_valid_rows is not None:
+            if not (isinstance(num_valid_rows, torch.Tensor) and num_valid_rows.is_cuda
+                    and num_valid_rows.dtype == torch.int32 and num_valid_rows.numel() >= 1):
+                raise ValueError("num_valid_rows must be a CUDA int32 tensor (its first element is read)")
+            nvr = num_valid_rows.data_ptr()
+        if out is None:
+            out = torch.empty((T, self.H), dtype=torch.bfloat16, device=x.device)
+        op = self._dev(out, "out", (T, self.H), (torch.bfloat16,))
+        s = (stream if stream is not None else torch.cuda.current_stream(x.device)).cuda_stream
+        moe_forward(self.h, xp, ip, wp, nvr, op, T, s)
+        return out
+
+    __call__ = forward
+
+    def read_status(self, stream=None) -> int:
+        import torch
+        s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        return moe_read_status(self.h, s)
+
+    def debug_array(self, which: str):
+        import numpy as np
+        import torch
+        ids = {"counts": (MOE_DBG_COUNTS, np.int32), "offsets": (MOE_DBG_OFFSETS, np.int32),
+               "perm": (MOE_DBG_PERM, np.int32), "route_row": (MOE_DBG_ROUTE_ROW, np.int32),
+               "route_slot": (MOE_DBG_ROUTE_SLOT, np.int32), "occ": (MOE_DBG_OCC, np.uint32),
+               "xq": (MOE_DBG_XQ, np.uint8), "xs": (MOE_DBG_XS, np.uint8), "yrow": (MOE_DBG_YROW, np.int32),
+               "hq": (MOE_DBG_HQ, np.uint8), "g": (MOE_DBG_G, np.float32), "y": (MOE_DBG_Y, np.uint16),
+               "tiles": (MOE_DBG_TILES, np.int32)}
+        code, dt = ids[which]
+        raw = moe_debug_copy(self.h, code, torch.cuda.current_stream().cuda_stream)
+        return np.frombuffer(raw, dtype=dt).copy()

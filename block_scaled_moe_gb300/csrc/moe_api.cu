@@ -1,0 +1,509 @@
+// moe_api.cu -- the C ABI of include/blockmoe.h: handle state, argument and
+// weight validation, workspace carving, TMA descriptors and the launch order
+// of one forward (dispatch -> quant/scatter -> GEMM1 -> GEMM2 -> combine),
+// all on the caller's stream with no host synchronisation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "blockmoe.h"
+#include "moe_internal.h"
+
+using bmoe::Geometry;
+using bmoe::Workspace;
+
+struct moe_ctx {
+    int device = -1;
+    int num_sms = 0;
+    Geometry geo{};
+    int opt_dispatch = MOE_DISPATCH_AUTO;
+    double swiglu_limit = 0.0;
+    int fixed_slot_max = 255;
+    int debug = 0;
+    int route_tile = 0;
+    bool forwarded = false;
+    void* ws_mem = nullptr;
+    size_t ws_bytes = 0;
+    bool ws_owned = false;
+    Workspace ws{};
+    bool bound = false;
+    const uint8_t* w13 = nullptr;
+    const uint8_t* w13s = nullptr;
+    const uint8_t* w2 = nullptr;
+    const uint8_t* w2s = nullptr;
+    CUtensorMap tm_w13{}, tm_w2{}, tm_aq{}, tm_hq{};
+    int last_T = 0;
+    std::string err;
+};
+
+namespace {
+
+thread_local std::string g_create_err;
+
+int fail(moe_ctx* h, int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    if (h)
+        h->err = buf;
+    else
+        g_create_err = buf;
+    return code;
+}
+
+int cuda_fail(moe_ctx* h, cudaError_t e, const char* what) {
+    return fail(h, MOE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2D K-major tile map: inner dim = K elements, outer = rows; box 128 x box_rows, 128B swizzle.
+int make_map(moe_ctx* h, CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t K, uint64_t rows,
+             uint64_t row_bytes, uint32_t box_rows, CUtensorMapL2promotion l2) {
+    auto fn = encode_fn();
+    if (!fn) return fail(h, MOE_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {K, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(h, MOE_ECUDA, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu tensor", (int)r,
+                    (unsigned long long)rows, (unsigned long long)K);
+    return MOE_OK;
+}
+
+void compute_geometry(moe_ctx* h, Geometry* g) {
+    *g = h->geo;
+    const bool fixed = h->opt_dispatch == MOE_DISPATCH_FIXED ||
+                       (h->opt_dispatch == MOE_DISPATCH_AUTO && g->cap <= h->fixed_slot_max);
+    g->scheme = fixed ? 1 : 2;
+    g->mtpr = g->cap;
+    g->words = (g->cap + 31) / 32;
+    int NT = h->route_tile;
+    if (NT == 0) NT = ((long long)g->cap * g->K <= 8LL * g->E) ? 32 : 128;
+    g->NT = NT;
+    const long long slots = (long long)g->cap * g->K;
+    if (fixed) {
+        g->rows_cap = (long long)g->E * g->mtpr;
+        g->tiles_cap = (long long)g->E * ((g->mtpr + NT - 1) / NT);
+    } else {
+        g->rows_cap = slots;
+        g->tiles_cap = slots / NT + g->E;
+    }
+    // the row-tile TMA box is NT rows high: keep the packed tensors at least that tall
+    g->rows_cap = (g->rows_cap + NT - 1) / NT * NT;
+    if (g->tiles_cap < 1) g->tiles_cap = 1;
+    g->nchunks_cap = (int)((slots + bmoe::kChunk - 1) / bmoe::kChunk);
+    g->debug = h->debug != 0;
+}
+
+int setup_workspace_maps(moe_ctx* h) {
+    const Geometry& g = h->geo;
+    int rc = make_map(h, &h->tm_aq, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->ws.aq, g.H, g.rows_cap, g.H, g.NT,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+    if (rc) return rc;
+    return make_map(h, &h->tm_hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->ws.hq, g.I, g.rows_cap, g.I, g.NT,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+}
+
+void release_workspace(moe_ctx* h) {
+    if (h->ws_owned && h->ws_mem) cudaFree(h->ws_mem);
+    h->ws_mem = nullptr;
+    h->ws_bytes = 0;
+    h->ws_owned = false;
+    h->ws = Workspace{};
+}
+
+// Point the handle at `mem` (bytes) for the current geometry and clear the counters.
+int adopt_workspace(moe_ctx* h, void* mem, size_t bytes, bool owned) {
+    Workspace w{};
+    const size_t need = bmoe::workspace_layout(h->geo, static_cast<char*>(mem), &w);
+    if (bytes < need) return fail(h, MOE_ENOMEM, "workspace holds %zu bytes, %zu needed", bytes, need);
+    cudaError_t e = cudaMemset(w.ticket, 0, 4 * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(w.status, 0, 4 * sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(h, e, "clearing workspace counters");
+    release_workspace(h);
+    h->ws_mem = mem;
+    h->ws_bytes = bytes;
+    h->ws_owned = owned;
+    h->ws = w;
+    return setup_workspace_maps(h);
+}
+
+int allocate_own_workspace(moe_ctx* h) {
+    const size_t need = bmoe::workspace_layout(h->geo, nullptr, nullptr);
+    void* mem = nullptr;
+    cudaError_t e = cudaMalloc(&mem, need);
+    if (e != cudaSuccess) return fail(h, MOE_ENOMEM, "cudaMalloc(%zu) for the workspace: %s", need, cudaGetErrorString(e));
+    int rc = adopt_workspace(h, mem, need, true);
+    if (rc) cudaFree(mem);
+    return rc;
+}
+
+// Re-derive the geometry after an option change; reallocate an owned workspace.
+int regeometry(moe_ctx* h) {
+    Geometry g;
+    compute_geometry(h, &g);
+    h->geo = g;
+    if (h->ws_owned || !h->ws_mem) {
+        release_workspace(h);
+        return allocate_own_workspace(h);
+    }
+    const size_t need = bmoe::workspace_layout(g, nullptr, nullptr);
+    if (need > h->ws_bytes) {
+        h->ws_mem = nullptr;
+        h->ws = Workspace{};
+        return fail(h, MOE_ENOMEM, "caller workspace too small for the new options (%zu needed)", need);
+    }
+    return adopt_workspace(h, h->ws_mem, h->ws_bytes, false);
+}
+
+int check_device_ptr(moe_ctx* h, const void* p, const char* name, size_t align) {
+    if (!p) return fail(h, MOE_EINVAL, "%s is NULL", name);
+    if (reinterpret_cast<uintptr_t>(p) % align)
+        return fail(h, MOE_EINVAL, "%s is not %zu-byte aligned", name, align);
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, MOE_EINVAL, "%s is not a CUDA pointer (%s)", name, cudaGetErrorString(e));
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+        return fail(h, MOE_EINVAL, "%s is not device memory", name);
+    if (at.device != h->device) return fail(h, MOE_EINVAL, "%s lives on device %d, the handle on %d", name, at.device, h->device);
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_create(moe_handle* out, int H, int I, int E, int topk, int capacity) {
+    if (!out) return fail(nullptr, MOE_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (H <= 0 || I <= 0 || H % 128 || I % 128)
+        return fail(nullptr, MOE_ESHAPE, "H=%d and I=%d must be positive multiples of 128", H, I);
+    if (E < 1 || E > bmoe::kMaxExperts) return fail(nullptr, MOE_ESHAPE, "E=%d outside [1, %d]", E, bmoe::kMaxExperts);
+    if (topk < 1 || topk > bmoe::kMaxTopk) return fail(nullptr, MOE_ESHAPE, "topk=%d outside [1, %d]", topk, bmoe::kMaxTopk);
+    if (capacity < 1) return fail(nullptr, MOE_EINVAL, "capacity=%d must be >= 1", capacity);
+    if ((long long)capacity * topk > (1LL << 30)) return fail(nullptr, MOE_EINVAL, "capacity * topk too large");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(nullptr, MOE_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return fail(nullptr, MOE_ECUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+    if (!(prop.major == 10 && prop.minor == 3))
+        return fail(nullptr, MOE_EDEVICE, "device %d is sm_%d%d; this library is built for sm_103a (GB300)", dev,
+                    prop.major, prop.minor);
+    e = bmoe::gemm_set_attributes();
+    if (e != cudaSuccess) return fail(nullptr, MOE_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    moe_ctx* h = new (std::nothrow) moe_ctx();
+    if (!h) return fail(nullptr, MOE_ENOMEM, "host allocation failed");
+    h->device = dev;
+    h->num_sms = prop.multiProcessorCount;
+    h->geo.H = H;
+    h->geo.I = I;
+    h->geo.E = E;
+    h->geo.K = topk;
+    h->geo.cap = capacity;
+    Geometry g;
+    compute_geometry(h, &g);
+    h->geo = g;
+    int rc = allocate_own_workspace(h);
+    if (rc) {
+        g_create_err = h->err;
+        delete h;
+        return rc;
+    }
+    *out = h;
+    return MOE_OK;
+}
+
+void moe_destroy(moe_handle h) {
+    if (!h) return;
+    release_workspace(h);
+    delete h;
+}
+
+int moe_bind_weights(moe_handle h, const void* w13_fp4, const void* w13_sf, const void* w2_fp4, const void* w2_sf) {
+    if (!h) return MOE_EINVAL;
+    int rc;
+    if ((rc = check_device_ptr(h, w13_fp4, "w13_fp4", 32))) return rc;
+    if ((rc = check_device_ptr(h, w13_sf, "w13_sf", 16))) return rc;
+    if ((rc = check_device_ptr(h, w2_fp4, "w2_fp4", 32))) return rc;
+    if ((rc = check_device_ptr(h, w2_sf, "w2_sf", 16))) return rc;
+    const Geometry& g = h->geo;
+    CUtensorMap m13, m2;
+    if ((rc = make_map(h, &m13, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13_fp4, g.H, (uint64_t)g.E * 2 * g.I, g.H / 2,
+                       128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
+        return rc;
+    if ((rc = make_map(h, &m2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2_fp4, g.I, (uint64_t)g.E * g.H, g.I / 2, 128,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
+        return rc;
+    // everything validated: switch the binding
+    h->tm_w13 = m13;
+    h->tm_w2 = m2;
+    h->w13 = static_cast<const uint8_t*>(w13_fp4);
+    h->w13s = static_cast<const uint8_t*>(w13_sf);
+    h->w2 = static_cast<const uint8_t*>(w2_fp4);
+    h->w2s = static_cast<const uint8_t*>(w2_sf);
+    h->bound = true;
+    return MOE_OK;
+}
+
+int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const float* topk_weights,
+                const int32_t* num_valid_rows, void* out, int T, moe_stream_t stream) {
+    if (!h) return MOE_EINVAL;
+    const Geometry& g = h->geo;
+    if (T < 0) return fail(h, MOE_EINVAL, "T=%d is negative", T);
+    if (T > g.cap) return fail(h, MOE_ECAPACITY, "T=%d exceeds the capacity %d", T, g.cap);
+    if (!h->bound) return fail(h, MOE_ENOTBOUND, "no weights bound");
+    if (!h->ws_mem) return fail(h, MOE_ENOMEM, "no workspace");
+    if (T == 0) return MOE_OK;
+    if (!x || !topk_ids || !topk_weights || !out) return fail(h, MOE_EINVAL, "x, topk_ids, topk_weights and out must be non-NULL");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15)
+        return fail(h, MOE_EINVAL, "x and out must be 16-byte aligned");
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device)
+        return fail(h, MOE_EINVAL, "current device %d is not the handle's device %d", cur, h->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Workspace& ws = h->ws;
+    cudaError_t e;
+    if (g.scheme == 1) {
+        e = cudaMemsetAsync(ws.occ, 0, sizeof(uint32_t) * (size_t)g.E * g.words, s);
+        if (e != cudaSuccess) return cuda_fail(h, e, "clearing occupancy");
+        e = bmoe::launch_fixed_mark(g, ws, topk_ids, T, num_valid_rows, s);
+    } else {
+        e = bmoe::launch_compact_dispatch(g, ws, topk_ids, T, num_valid_rows, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(h, e, "dispatch launch");
+    e = bmoe::launch_quant_scatter(g, ws, static_cast<const uint16_t*>(x), topk_ids, T, num_valid_rows, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "quant launch");
+
+    bmoe::GemmArgs a{};
+    a.counts = ws.counts;
+    a.rowbase = ws.rowbase;
+    a.tile_base = ws.tile_base;
+    a.E = g.E;
+    a.swiglu_limit = static_cast<float>(h->swiglu_limit);
+    a.status = ws.status;
+    a.I = g.I;
+    a.H = g.H;
+    // GEMM1: W13 (gate/up pairs) x dispatched rows, K = H
+    a.w_sf = h->w13s;
+    a.w_rows = 2 * g.I;
+    a.ld_sf = g.H / 32;
+    a.up_off = g.I;
+    a.ktiles = g.H / 128;
+    a.mtiles = g.I / 128;
+    a.b_sf = ws.as;
+    a.hq = ws.hq;
+    a.hs = ws.hs;
+    a.g_dbg = g.debug ? ws.g : nullptr;
+    e = bmoe::launch_gemm1(a, &h->tm_w13, &h->tm_aq, g.NT, h->num_sms, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "GEMM1 launch");
+    // GEMM2: W2 x h rows, K = I
+    a.w_sf = h->w2s;
+    a.w_rows = g.H;
+    a.ld_sf = g.I / 32;
+    a.up_off = 0;
+    a.ktiles = g.I / 128;
+    a.mtiles = g.H / 128;
+    a.b_sf = ws.hs;
+    a.y = ws.y;
+    a.g_dbg = nullptr;
+    e = bmoe::launch_gemm2(a, &h->tm_w2, &h->tm_hq, g.NT, h->num_sms, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "GEMM2 launch");
+    e = bmoe::launch_combine(g, ws, topk_weights, T, num_valid_rows, static_cast<uint16_t*>(out), s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
+    h->forwarded = true;
+    h->last_T = T;
+    return MOE_OK;
+}
+
+int moe_set_option(moe_handle h, int key, double value) {
+    if (!h) return MOE_EINVAL;
+    switch (key) {
+        case MOE_OPT_SWIGLU_LIMIT:
+            if (!(value >= 0.0)) return fail(h, MOE_EINVAL, "swiglu limit must be >= 0");
+            h->swiglu_limit = value;
+            return MOE_OK;
+        case MOE_OPT_DISPATCH:
+        case MOE_OPT_FIXED_SLOT_MAX:
+        case MOE_OPT_DEBUG_CAPTURE:
+        case MOE_OPT_ROUTE_TILE: {
+            if (h->forwarded) return fail(h, MOE_ESTATE, "option %d changes the workspace layout; set it before the first forward", key);
+            const int v = static_cast<int>(value);
+            if (static_cast<double>(v) != value) return fail(h, MOE_EINVAL, "option %d takes an integer", key);
+            moe_ctx saved = *h;
+            if (key == MOE_OPT_DISPATCH) {
+                if (v < MOE_DISPATCH_AUTO || v > MOE_DISPATCH_COMPACT) return fail(h, MOE_EINVAL, "bad dispatch scheme %d", v);
+                if (v == MOE_DISPATCH_FIXED && h->geo.cap > 4096)
+                    return fail(h, MOE_EINVAL, "fixed-slot dispatch needs capacity <= 4096");
+                h->opt_dispatch = v;
+            } else if (key == MOE_OPT_FIXED_SLOT_MAX) {
+                if (v < 0) return fail(h, MOE_EINVAL, "fixed-slot max must be >= 0");
+                h->fixed_slot_max = v;
+            } else if (key == MOE_OPT_DEBUG_CAPTURE) {
+                h->debug = v ? 1 : 0;
+            } else {
+                if (v != 0 && v != 32 && v != 128) return fail(h, MOE_EINVAL, "route tile must be 0, 32 or 128");
+                h->route_tile = v;
+            }
+            Geometry g;
+            compute_geometry(h, &g);
+            if (memcmp(&g, &h->geo, sizeof(g)) == 0) return MOE_OK;
+            int rc = regeometry(h);
+            if (rc) {  // restore the previous options and workspace
+                std::string msg = h->err;
+                h->opt_dispatch = saved.opt_dispatch;
+                h->fixed_slot_max = saved.fixed_slot_max;
+                h->debug = saved.debug;
+                h->route_tile = saved.route_tile;
+                compute_geometry(h, &g);
+                h->geo = g;
+                if (!h->ws_mem) allocate_own_workspace(h);
+                h->err = msg;
+            }
+            return rc;
+        }
+        default:
+            return fail(h, MOE_EINVAL, "unknown option %d", key);
+    }
+}
+
+int moe_get_option(moe_handle h, int key, double* value) {
+    if (!h || !value) return MOE_EINVAL;
+    switch (key) {
+        case MOE_OPT_DISPATCH: *value = h->opt_dispatch; return MOE_OK;
+        case MOE_OPT_SWIGLU_LIMIT: *value = h->swiglu_limit; return MOE_OK;
+        case MOE_OPT_FIXED_SLOT_MAX: *value = h->fixed_slot_max; return MOE_OK;
+        case MOE_OPT_DEBUG_CAPTURE: *value = h->debug; return MOE_OK;
+        case MOE_OPT_ROUTE_TILE: *value = h->geo.NT; return MOE_OK;
+        default: return fail(h, MOE_EINVAL, "unknown option %d", key);
+    }
+}
+
+size_t moe_workspace_bytes(moe_handle h) {
+    if (!h) return 0;
+    return bmoe::workspace_layout(h->geo, nullptr, nullptr);
+}
+
+int moe_set_workspace(moe_handle h, void* dev_ptr, size_t bytes) {
+    if (!h) return MOE_EINVAL;
+    if (h->forwarded) return fail(h, MOE_ESTATE, "set the workspace before the first forward");
+    if (!dev_ptr || reinterpret_cast<uintptr_t>(dev_ptr) % 256) return fail(h, MOE_EINVAL, "workspace must be non-NULL and 256-byte aligned");
+    int rc = check_device_ptr(h, dev_ptr, "workspace", 256);
+    if (rc) return rc;
+    return adopt_workspace(h, dev_ptr, bytes, false);
+}
+
+int moe_read_status(moe_handle h, uint32_t* flags, moe_stream_t stream) {
+    if (!h || !flags) return MOE_EINVAL;
+    if (!h->ws_mem) return fail(h, MOE_ENOMEM, "no workspace");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, h->ws.status, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->ws.status, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "reading the status word");
+    *flags = v;
+    return MOE_OK;
+}
+
+const char* moe_last_error(moe_handle h) {
+    return h ? h->err.c_str() : g_create_err.c_str();
+}
+
+int moe_dispatch_scheme(moe_handle h) {
+    if (!h) return MOE_EINVAL;
+    return h->geo.scheme == 1 ? MOE_DISPATCH_FIXED : MOE_DISPATCH_COMPACT;
+}
+
+int moe_debug_copy(moe_handle h, int which, void* host_dst, size_t* bytes, moe_stream_t stream) {
+    if (!h || !bytes) return MOE_EINVAL;
+    const Geometry& g = h->geo;
+    const Workspace& w = h->ws;
+    const size_t slots = (size_t)h->last_T * g.K;
+    const void* src = nullptr;
+    size_t n = 0;
+    switch (which) {
+        case MOE_DBG_COUNTS: src = w.counts; n = sizeof(int32_t) * g.E; break;
+        case MOE_DBG_OFFSETS: src = w.rowbase; n = sizeof(int32_t) * (g.E + 1); break;
+        case MOE_DBG_PERM: src = w.perm; n = sizeof(int32_t) * slots; break;
+        case MOE_DBG_ROUTE_ROW: src = w.route_row; n = sizeof(int32_t) * slots; break;
+        case MOE_DBG_ROUTE_SLOT: src = w.route_slot; n = sizeof(int32_t) * slots; break;
+        case MOE_DBG_OCC: src = w.occ; n = sizeof(uint32_t) * (size_t)g.E * g.words; break;
+        case MOE_DBG_XQ: src = w.xq; n = (size_t)h->last_T * g.H; break;
+        case MOE_DBG_XS: src = w.xs; n = (size_t)h->last_T * (g.H / 32); break;
+        case MOE_DBG_YROW: src = w.yrow; n = sizeof(int32_t) * slots; break;
+        case MOE_DBG_HQ: src = w.hq; n = (size_t)g.rows_cap * g.I; break;
+        case MOE_DBG_G: src = w.g; n = (size_t)g.rows_cap * 2 * g.I * sizeof(float); break;
+        case MOE_DBG_Y: src = w.y; n = (size_t)g.rows_cap * g.H * 2; break;
+        case MOE_DBG_TILES: {
+            std::vector<int32_t> cnt(g.E), rb(g.E + 1), tb(g.E + 1);
+            cudaStream_t s = static_cast<cudaStream_t>(stream);
+            cudaError_t e = cudaStreamSynchronize(s);
+            if (e == cudaSuccess) e = cudaMemcpy(cnt.data(), w.counts, sizeof(int32_t) * g.E, cudaMemcpyDeviceToHost);
+            if (e == cudaSuccess) e = cudaMemcpy(rb.data(), w.rowbase, sizeof(int32_t) * (g.E + 1), cudaMemcpyDeviceToHost);
+            if (e == cudaSuccess) e = cudaMemcpy(tb.data(), w.tile_base, sizeof(int32_t) * (g.E + 1), cudaMemcpyDeviceToHost);
+            if (e != cudaSuccess) return cuda_fail(h, e, "debug copy");
+            std::vector<int32_t> v(1 + 3 * (size_t)tb[g.E]);
+            v[0] = tb[g.E];
+            for (int e2 = 0; e2 < g.E; ++e2)
+                for (int j = 0; j < tb[e2 + 1] - tb[e2]; ++j) {
+                    const size_t t = tb[e2] + j;
+                    v[1 + 3 * t] = e2;
+                    v[2 + 3 * t] = rb[e2] + j * g.NT;
+                    v[3 + 3 * t] = cnt[e2] - j * g.NT < g.NT ? cnt[e2] - j * g.NT : g.NT;
+                }
+            n = v.size() * sizeof(int32_t);
+            if (host_dst) {
+                if (*bytes < n) return fail(h, MOE_EINVAL, "destination holds %zu bytes, %zu needed", *bytes, n);
+                memcpy(host_dst, v.data(), n);
+            }
+            *bytes = n;
+            return MOE_OK;
+        }
+        default: return fail(h, MOE_EINVAL, "unknown debug region %d", which);
+    }
+    if (!src) return fail(h, MOE_ESTATE, "region %d needs MOE_OPT_DEBUG_CAPTURE", which);
+    if (!host_dst) {
+        *bytes = n;
+        return MOE_OK;
+    }
+    if (*bytes < n) return fail(h, MOE_EINVAL, "destination holds %zu bytes, %zu needed", *bytes, n);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && n) e = cudaMemcpy(host_dst, src, n, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(h, e, "debug copy");
+    *bytes = n;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,383 @@
+// moe_gemm.cu -- grouped block-scaled GEMMs of the MoE layer on the 5th-generation
+// tensor cores (tcgen05.mma kind::mxf8f6f4 with E8M0 block scales).
+//
+// Orientation ("swap-AB"): the expert weight tile is the M=128 operand A and the
+// expert's dispatched rows are the N operand B, so an expert with n routed rows
+// runs MMAs of N = roundup(n, 16) instead of padding rows to 128.  For decode,
+// where a few rows meet each expert, the layer is a stream over the active
+// experts' weights (ROCm/aiter PR #6881 Technical Details: the small-input path
+// is dominated by reading expert weights); for prefill the same kernel runs
+// route tiles of up to NT=128 rows.
+//
+//   GEMM1 unit = (route tile, pair m): gate rows [128m,128m+128) and up rows
+//     I+[128m,128m+128) of W13[e], K = H.  Epilogue: SwiGLU (optional clamp,
+//     ROCm/aiter PR #6154 "clamp-10 SwiGLU") and MXFP8 1x32 re-quantisation of
+//     h along I ("FP8 intermediate quantization", aiter #6154 Summary).
+//   GEMM2 unit = (route tile, tile m): rows [128m,128m+128) of W2[e], K = I.
+//     Epilogue: BF16 rows y (aiter #6881: GEMM2 rows go to the combine as BF16).
+//
+// Pipeline per CTA (persistent, one CTA per SM, units strided over the grid):
+//   warp 0     producer: TMA of the FP4 weight tile (16U4_ALIGN16B expands each
+//              16 codes to 16 bytes in shared memory, the layout kind::mxf8f6f4
+//              reads), TMA of the FP8 row tile, bulk copy of the rows' scale
+//              atom, and the weight scales gathered from their natural
+//              [rows, K/32] layout into a 128x4 scale atom by the warp's lanes.
+//   warp 1     MMA issuer: tcgen05.cp of the scale atoms into TMEM, 4 MMAs of
+//              K=32 per 128-wide K stage (scale byte k of each TMEM word).
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (lane = output feature,
+//              column = routed row), math, global stores.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace bmoe {
+
+namespace {
+
+template <bool G1, int NT>
+struct Cfg {
+    static constexpr int NA = G1 ? 2 : 1;                  // weight tiles per stage
+    static constexpr int A_BYTES = 128 * 128;              // one weight tile in smem (1 byte per code)
+    static constexpr int B_BYTES = NT * 128;               // row tile in smem
+    static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES + (NA + 1) * 512;
+    static constexpr int STAGES = (220 * 1024) / STAGE_BYTES > 12 ? 12 : (220 * 1024) / STAGE_BYTES;
+    static constexpr int ACC_COLS = G1 ? 2 * NT : NT;
+    static constexpr int NUM_ACC = (2 * ACC_COLS <= 256) ? 2 : 1;
+    static constexpr int SF_COL0 = 256;
+    static constexpr int SF_COLS = 4 * (NA + 1);           // TMEM columns of scales per stage
+    static constexpr int BAR_BYTES = (2 * STAGES + 2 * 2 + 1) * 8 + 16;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static_assert(SF_COL0 + STAGES * SF_COLS <= 512, "TMEM columns");
+    static_assert(NUM_ACC * ACC_COLS <= SF_COL0, "TMEM accumulators");
+    static_assert(SMEM <= 232448, "shared memory");
+};
+
+struct UnitInfo {
+    int e, m, g, row0, n;
+};
+
+// Unit u of the global list: experts ascending; inside an expert, weight tile m
+// major and route tile j minor, so CTAs running consecutive units share a
+// weight tile (L2 reuse when an expert has several route tiles).  `ecur` only
+// moves forward because every role walks its units in increasing order.
+__device__ __forceinline__ UnitInfo decode_unit(int u, int& ecur, const GemmArgs& a, int NT) {
+    const int q = u / a.mtiles;
+    while (__ldg(a.tile_base + ecur + 1) <= q) ++ecur;
+    const int tb = __ldg(a.tile_base + ecur);
+    const int nt = __ldg(a.tile_base + ecur + 1) - tb;
+    const int ul = u - tb * a.mtiles;
+    UnitInfo r;
+    r.e = ecur;
+    r.m = ul / nt;
+    const int j = ul - r.m * nt;
+    r.g = tb + j;
+    r.row0 = __ldg(a.rowbase + ecur) + j * NT;
+    r.n = min(NT, __ldg(a.counts + ecur) - j * NT);
+    return r;
+}
+
+template <bool G1, int NT>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b, const GemmArgs a) {
+    using C = Cfg<G1, NT>;
+    constexpr int STAGES = C::STAGES, NA = C::NA;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = sm;
+    uint8_t* sB = sA + STAGES * NA * C::A_BYTES;
+    uint8_t* sSFA = sB + STAGES * C::B_BYTES;
+    uint8_t* sSFB = sSFA + STAGES * NA * 512;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * 512);
+    uint64_t* empty = full + STAGES;
+    uint64_t* accf = empty + STAGES;
+    uint64_t* acce = accf + 2;
+    uint64_t* drain = acce + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = __ldg(a.tile_base + a.E);
+    const int n_units = ntiles * a.mtiles;
+    if (static_cast<int>(blockIdx.x) >= n_units) return;  // whole CTA
+    const int my_units = (n_units - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1;
+    const int KT = a.ktiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 32);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const uint64_t pol_w = policy_evict_first();
+        const uint64_t pol_b = policy_evict_last();
+        if (lane == 0) {
+            prefetch_tmap(&tm_w);
+            prefetch_tmap(&tm_b);
+        }
+        const long njobs = static_cast<long>(my_units) * KT;
+        constexpr int D = 4;  // weight-scale prefetch distance, in stages
+        uint32_t sfr[D][4 * NA];
+        int pf_ecur = 0, pf_ui = -1;
+        UnitInfo pfu{};
+        auto load_sf = [&](long J, uint32_t(&dst)[4 * NA]) {
+            if (J >= njobs) return;
+            const int ui = static_cast<int>(J / KT), kk = static_cast<int>(J % KT);
+            if (ui != pf_ui) {
+                pfu = decode_unit(blockIdx.x + ui * gridDim.x, pf_ecur, a, NT);
+                pf_ui = ui;
+            }
+            const uint8_t* base =
+                a.w_sf + (static_cast<size_t>(pfu.e) * a.w_rows + pfu.m * 128 + lane) * a.ld_sf + kk * 4;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[i] = __ldg(reinterpret_cast<const uint32_t*>(base + static_cast<size_t>(32 * i) * a.ld_sf));
+            if constexpr (G1) {
+                const uint8_t* b2 = base + static_cast<size_t>(a.up_off) * a.ld_sf;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[4 + i] = __ldg(reinterpret_cast<const uint32_t*>(b2 + static_cast<size_t>(32 * i) * a.ld_sf));
+            }
+        };
+#pragma unroll
+        for (int d = 0; d < D; ++d) load_sf(d, sfr[d]);
+        int stage = 0;
+        uint32_t phase = 0;
+        int ecur = 0, cu_ui = -1;
+        UnitInfo cu{};
+        bool ok = true;
+        long issued = 0;
+        for (long J0 = 0; J0 < njobs && ok; J0 += D) {
+#pragma unroll
+            for (int d = 0; d < D; ++d) {
+                const long J = J0 + d;
+                if (J < njobs && ok) {
+                    const int ui = static_cast<int>(J / KT), kk = static_cast<int>(J % KT);
+                    if (ui != cu_ui) {
+                        cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, a, NT);
+                        cu_ui = ui;
+                    }
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, kStTimeout, kWaitLimitNs)) {
+                        ok = false;
+                    } else {
+                        if (lane == 0) {
+                            mbar_expect_tx(&full[stage], NA * C::A_BYTES + C::B_BYTES + 512);
+                            const int wrow = cu.e * a.w_rows + cu.m * 128;
+                            tma_load_2d(sA + (stage * NA) * C::A_BYTES, &tm_w, &full[stage], kk * 128, wrow, pol_w);
+                            if constexpr (G1)
+                                tma_load_2d(sA + (stage * NA + 1) * C::A_BYTES, &tm_w, &full[stage], kk * 128,
+                                            wrow + a.up_off, pol_w);
+                            tma_load_2d(sB + stage * C::B_BYTES, &tm_b, &full[stage], kk * 128, cu.row0, pol_b);
+                            bulk_load(sSFB + stage * 512, a.b_sf + (static_cast<size_t>(cu.g) * KT + kk) * 512, 512,
+                                      &full[stage]);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(sSFA + stage * NA * 512) + lane;
+                        dst[0] = make_uint4(sfr[d][0], sfr[d][1], sfr[d][2], sfr[d][3]);
+                        if constexpr (G1) dst[32] = make_uint4(sfr[d][4], sfr[d][5], sfr[d][6], sfr[d][7]);
+                        fence_proxy_async_smem();
+                        mbar_arrive(&full[stage]);
+                        ++issued;
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    load_sf(J + D, sfr[d]);
+                }
+            }
+        }
+        // Drain: the loads of the last STAGES issued jobs land before the CTA exits
+        // (they are consumed already unless another role gave up).
+        {
+            volatile int never = 0;
+            int st = stage;
+            uint32_t ph = phase;
+            for (long i = 0; i < STAGES && i < issued; ++i) {
+                if (st == 0) {
+                    st = STAGES - 1;
+                    ph ^= 1u;
+                } else {
+                    --st;
+                }
+                (void)mbar_wait(&full[st], ph, &never, a.status, kStTimeout, kWaitLimitNs / 4);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        int stage = 0, acc = 0, ecur = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        bool ok = true;
+        for (int ui = 0; ui < my_units && ok; ++ui) {
+            const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, a, NT);
+            const int N = (cu.n + 15) & ~15;
+            const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * C::ACC_COLS);
+            if (!mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, a.status, kStTimeout, kWaitLimitNs)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kk = 0; kk < KT; ++kk) {
+                if (!mbar_wait(&full[stage], phase, abort_flag, a.status, kStTimeout, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sfc = tmem + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
+                    tc_cp_32x128b_x4(sfc, desc_sf_atom(smem_u32(sSFA + stage * NA * 512)));
+                    if constexpr (G1) tc_cp_32x128b_x4(sfc + 4, desc_sf_atom(smem_u32(sSFA + stage * NA * 512 + 512)));
+                    tc_cp_32x128b_x4(sfc + 4 * NA, desc_sf_atom(smem_u32(sSFB + stage * 512)));
+                    const uint64_t da0 = desc_kmajor_sw128(smem_u32(sA + (stage * NA) * C::A_BYTES));
+                    const uint64_t da1 = desc_kmajor_sw128(smem_u32(sA + (stage * NA + NA - 1) * C::A_BYTES));
+                    const uint64_t db = desc_kmajor_sw128(smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t idesc = idesc_mx(128, N, 5, 0, k, k);
+                        const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);
+                        const uint32_t accum = (kk | k) != 0 ? 1u : 0u;
+                        tc_mma_mx(d_tmem, da0 + koff, db + koff, idesc, sfc, sfc + 4 * NA, accum);
+                        if constexpr (G1) tc_mma_mx(d_tmem + NT, da1 + koff, db + koff, idesc, sfc + 4, sfc + 4 * NA, accum);
+                    }
+                    tc_commit(&empty[stage]);
+                }
+                __syncwarp();
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(&accf[acc]);
+            __syncwarp();
+            if (C::NUM_ACC == 2) {
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            } else {
+                acc_phase ^= 1u;
+            }
+        }
+        // Drain: all MMAs issued by this thread complete before TMEM is released.
+        if (lane == 0) tc_commit(drain);
+        __syncwarp();
+        {
+            volatile int never = 0;
+            (void)mbar_wait(drain, 0, &never, a.status, kStTimeout, kWaitLimitNs);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        int acc = 0, ecur = 0;
+        uint32_t acc_phase = 0;
+        const float L = a.swiglu_limit;
+        for (int ui = 0; ui < my_units; ++ui) {
+            const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, a, NT);
+            if (!mbar_wait(&accf[acc], acc_phase, abort_flag, a.status, kStTimeout, kWaitLimitNs)) break;
+            tc_fence_after();
+            const uint32_t tb = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * C::ACC_COLS);
+            const int feat = cu.m * 128 + 32 * q + lane;
+            for (int c0 = 0; c0 < cu.n; c0 += 16) {
+                uint32_t ra[16], rb[16];
+                tmem_ld16(tb + c0, ra);
+                if constexpr (G1) tmem_ld16(tb + NT + c0, rb);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c = c0 + i;
+                    if (c < cu.n) {
+                        const size_t prow = static_cast<size_t>(cu.row0 + c);
+                        if constexpr (G1) {
+                            float ga = __uint_as_float(ra[i]), ub = __uint_as_float(rb[i]);
+                            if (a.g_dbg) {
+                                a.g_dbg[prow * 2 * a.I + feat] = ga;
+                                a.g_dbg[prow * 2 * a.I + a.I + feat] = ub;
+                            }
+                            if (L > 0.f) {
+                                ga = fminf(ga, L);
+                                ub = fminf(fmaxf(ub, -L), L);
+                            }
+                            const float h = ga * (1.0f / (1.0f + expf(-ga))) * ub;
+                            const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
+                            int code = static_cast<int>(amax >> 23) - 8;
+                            code = code < 0 ? 0 : code;
+                            const float mul = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
+                            a.hq[prow * a.I + feat] = __nv_cvt_float_to_fp8(h * mul, __NV_SATFINITE, __NV_E4M3);
+                            if (lane == 0)
+                                a.hs[(static_cast<size_t>(cu.g) * (a.I >> 7) + cu.m) * 512 + 16 * (c & 31) +
+                                     4 * (c >> 5) + q] = static_cast<uint8_t>(code);
+                        } else {
+                            a.y[prow * a.H + feat] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(ra[i])));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&acce[acc]);
+            if (C::NUM_ACC == 2) {
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            } else {
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <bool G1, int NT>
+cudaError_t set_attr() {
+    return cudaFuncSetAttribute(k_gemm<G1, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<G1, NT>::SMEM);
+}
+
+template <bool G1, int NT>
+cudaError_t launch(const GemmArgs& a, const CUtensorMap* tw, const CUtensorMap* tb, int grid, cudaStream_t s) {
+    k_gemm<G1, NT><<<grid, 192, Cfg<G1, NT>::SMEM, s>>>(*tw, *tb, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t gemm_set_attributes() {
+    cudaError_t e;
+    if ((e = set_attr<true, 128>()) != cudaSuccess) return e;
+    if ((e = set_attr<true, 32>()) != cudaSuccess) return e;
+    if ((e = set_attr<false, 128>()) != cudaSuccess) return e;
+    return set_attr<false, 32>();
+}
+
+cudaError_t launch_gemm1(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_x, int NT, int grid,
+                         cudaStream_t s) {
+    return NT == 32 ? launch<true, 32>(a, tm_w, tm_x, grid, s) : launch<true, 128>(a, tm_w, tm_x, grid, s);
+}
+
+cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_h, int NT, int grid,
+                         cudaStream_t s) {
+    return NT == 32 ? launch<false, 32>(a, tm_w, tm_h, grid, s) : launch<false, 128>(a, tm_w, tm_h, grid, s);
+}
+
+}  // namespace bmoe

@@ -1,0 +1,95 @@
+// moe_internal.h -- workspace layout, kernel parameter blocks and launchers
+// shared by the host code (moe_api.cu) and the kernels (moe_kernels.cu,
+// moe_gemm.cu).  Not part of the public ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace bmoe {
+
+constexpr int kChunk = 512;            // flat slots per compact-dispatch chunk
+constexpr int kMaxTopk = 16;
+constexpr int kMaxExperts = 4096;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per device-side wait
+constexpr uint32_t kStBadId = 0x1u, kStTimeout = 0x2u, kStOverflow = 0x4u;
+
+// Device workspace, carved from one allocation.
+struct Workspace {
+    int32_t* counts;       // [E]   rows per expert (compact: routes, fixed: occupied slots)
+    int32_t* rowbase;      // [E+1] first packed row of each expert
+    int32_t* tile_base;    // [E+1] exclusive scan of route tiles per expert; [E] = total tiles
+    int32_t* perm;         // [cap*K] compact packed row -> flat slot
+    int32_t* route_row;    // [cap*K] compact flat slot -> packed row (-1 invalid)
+    int32_t* route_slot;   // [cap*K] fixed flat slot -> e*MTPR+t (-1 invalid)
+    int32_t* yrow;         // [cap*K] packed row of the GEMM2 output each slot combines (-1 invalid)
+    uint32_t* occ;         // [E*words] fixed-slot occupancy bits
+    int32_t* chunk_base;   // [nchunks*E] compact per-chunk counts, then per-chunk base rows
+    uint32_t* ticket;      // [4] self-resetting last-block counters
+    uint32_t* status;      // [1] MOE_ST_* bits
+    uint8_t* aq;           // [rows_cap][H] packed E4M3 codes of the dispatched rows
+    uint8_t* as;           // [tiles_cap][H/128][512] scale atoms of aq, per route tile
+    uint8_t* hq;           // [rows_cap][I] E4M3 codes of h
+    uint8_t* hs;           // [tiles_cap][I/128][512] scale atoms of hq
+    uint16_t* y;           // [rows_cap][H] bf16 GEMM2 outputs
+    uint8_t* xq;           // [cap][H] canonical codes (debug capture only)
+    uint8_t* xs;           // [cap][H/32] canonical scales (debug capture only)
+    float* g;              // [rows_cap][2I] raw GEMM1 outputs (debug capture only)
+};
+
+struct Geometry {
+    int H, I, E, K, cap;
+    int scheme;            // 1 fixed, 2 compact
+    int mtpr;              // fixed-slot capacity per expert (= cap)
+    int words;             // ceil(mtpr/32)
+    int NT;                // route tile width (MMA N upper bound)
+    long long rows_cap;    // packed rows
+    long long tiles_cap;   // route tiles
+    int nchunks_cap;
+    bool debug;
+};
+
+size_t workspace_layout(const Geometry& g, char* base, Workspace* ws);  // base may be null (size only)
+
+// ------------------------------------------------------------------ launchers (moe_kernels.cu)
+cudaError_t launch_fixed_mark(const Geometry& g, const Workspace& ws, const int32_t* ids, int T,
+                              const int32_t* nvr, cudaStream_t s);
+cudaError_t launch_compact_dispatch(const Geometry& g, const Workspace& ws, const int32_t* ids, int T,
+                                    const int32_t* nvr, cudaStream_t s);
+cudaError_t launch_quant_scatter(const Geometry& g, const Workspace& ws, const uint16_t* x, const int32_t* ids,
+                                 int T, const int32_t* nvr, cudaStream_t s);
+cudaError_t launch_combine(const Geometry& g, const Workspace& ws, const float* wts, int T,
+                           const int32_t* nvr, uint16_t* out, cudaStream_t s);
+
+// ------------------------------------------------------------------ GEMMs (moe_gemm.cu)
+struct GemmArgs {
+    // routing plan
+    const int32_t* counts;
+    const int32_t* rowbase;
+    const int32_t* tile_base;
+    int E;
+    // weights: codes through the tensor map, scales read directly
+    const uint8_t* w_sf;   // natural [E*rows_per_expert][K/32]
+    int w_rows;            // weight rows per expert (2I for GEMM1, H for GEMM2)
+    int ld_sf;             // K/32
+    int up_off;            // GEMM1: row offset of the up half (= I)
+    int ktiles;            // K/128
+    int mtiles;            // weight tiles (of 128 rows, or row pairs for GEMM1) per expert
+    // activations: codes through the tensor map, scale atoms
+    const uint8_t* b_sf;   // [tiles][ktiles][512]
+    // outputs
+    uint8_t* hq;  uint8_t* hs;  int I;      // GEMM1
+    float* g_dbg;                           // GEMM1 debug capture (may be null)
+    uint16_t* y;  int H;                    // GEMM2
+    float swiglu_limit;
+    uint32_t* status;
+};
+
+cudaError_t launch_gemm1(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_x, int NT, int grid,
+                         cudaStream_t s);
+cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_h, int NT, int grid,
+                         cudaStream_t s);
+cudaError_t gemm_set_attributes();
+
+}  // namespace bmoe

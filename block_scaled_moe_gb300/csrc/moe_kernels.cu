@@ -1,0 +1,452 @@
+// moe_kernels.cu -- the bandwidth-bound steps of the layer: dispatch (fixed-slot
+// and compact), MXFP8 quantisation of the input rows fused with the scatter
+// into per-expert packed rows, and the top-k weighted combine.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "moe_internal.h"
+
+namespace bmoe {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ int read_nvr(const int32_t* p, int T) {
+    int v = p ? __ldg(p) : T;
+    return v < 0 ? 0 : (v > T ? T : v);
+}
+
+// Exclusive scan of in[0..n) into out[0..n], out[n] = total.  Whole block.
+__device__ void block_exclusive_scan(const int* in, int* out, int n, int* warp_sums) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = (blockDim.x + 31) >> 5;
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int start = tid * per;
+    int local = 0;
+    for (int i = start; i < start + per && i < n; ++i) local += in[i];
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int v = lane < nwarps ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(kFull, v, o);
+            if (lane >= o) v += y;
+        }
+        warp_sums[lane] = v;
+    }
+    __syncthreads();
+    int run = (warp > 0 ? warp_sums[warp - 1] : 0) + x - local;
+    for (int i = start; i < start + per && i < n; ++i) {
+        out[i] = run;
+        run += in[i];
+    }
+    if (tid == 0) out[n] = warp_sums[nwarps - 1];
+    __syncthreads();
+}
+
+// True in exactly one block: the last one to arrive at `ticket`.
+__device__ bool last_block(uint32_t* ticket, bool* flag_smem) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned prev = atomicAdd(ticket, 1u);
+        *flag_smem = (prev == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (*flag_smem) __threadfence();
+    return *flag_smem;
+}
+
+struct DispatchArgs {
+    const int32_t* ids;
+    const int32_t* nvr;
+    int T, K, E, mtpr, words, NT, nchunks;
+    Workspace ws;
+};
+
+// ---------------------------------------------------------------- fixed-slot
+// vLLM PR #61262 "second fixed-slot MegaMoEV2 runtime": each token writes
+// straight into a per-expert slot (e, t) of capacity MTPR; no prepare kernel.
+// Occupancy bits are ORed atomically (order-independent, so deterministic);
+// the last block turns them into per-expert row counts and the route-tile plan.
+__global__ void __launch_bounds__(256) k_fixed_mark(DispatchArgs a) {
+    extern __shared__ int sm[];
+    __shared__ int warp_sums[32];
+    __shared__ bool is_last;
+    const int s = blockIdx.x * blockDim.x + threadIdx.x;
+    const int nvr = read_nvr(a.nvr, a.T);
+    if (s < a.T * a.K) {
+        const int t = s / a.K, e = a.ids[s];
+        if (t < nvr && e >= a.E) atomicOr(a.ws.status, kStBadId);
+        if (t < nvr && e >= 0 && e < a.E) {
+            atomicOr(&a.ws.occ[(size_t)e * a.words + (t >> 5)], 1u << (t & 31));
+            a.ws.route_slot[s] = e * a.mtpr + t;
+        } else {
+            a.ws.route_slot[s] = -1;
+        }
+    }
+    if (!last_block(&a.ws.ticket[0], &is_last)) return;
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+        int c = 0;
+        for (int w = 0; w < a.words; ++w) c += __popc(__ldcg(&a.ws.occ[(size_t)e * a.words + w]));
+        a.ws.counts[e] = c;
+        a.ws.rowbase[e] = e * a.mtpr;
+        sm[e] = (c + a.NT - 1) / a.NT;
+    }
+    if (threadIdx.x == 0) a.ws.rowbase[a.E] = a.E * a.mtpr;
+    __syncthreads();
+    block_exclusive_scan(sm, sm + a.E, a.E, warp_sums);
+    for (int e = threadIdx.x; e <= a.E; e += blockDim.x) a.ws.tile_base[e] = sm[a.E + e];
+    if (threadIdx.x == 0) a.ws.ticket[0] = 0;
+}
+
+// ---------------------------------------------------------------- compact
+// vLLM PR #61262: compact dispatch packs tokens before dispatch.  Canonical
+// order: experts ascending, flat slot id t*K+k ascending inside an expert.
+// Pass 1: per-chunk expert histograms; the last block scans them into
+// per-expert offsets, per-(chunk, expert) base rows and the route-tile plan.
+__global__ void __launch_bounds__(512) k_compact_count(DispatchArgs a) {
+    extern __shared__ int sm[];  // cnt[E], offs[E+1], ntile[E], tbase[E+1]
+    __shared__ int warp_sums[32];
+    __shared__ bool is_last;
+    int* cnt = sm;
+    const int E = a.E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    const int nvr = read_nvr(a.nvr, a.T);
+    const int s = blockIdx.x * kChunk + threadIdx.x;
+    if (threadIdx.x < kChunk && s < a.T * a.K) {
+        const int t = s / a.K, e = a.ids[s];
+        if (t < nvr && e >= E) atomicOr(a.ws.status, kStBadId);
+        if (t < nvr && e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) a.ws.chunk_base[(size_t)blockIdx.x * E + e] = cnt[e];
+    if (!last_block(&a.ws.ticket[1], &is_last)) return;
+    int* offs = sm + E;
+    int* ntile = offs + E + 1;
+    int* tbase = ntile + E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int c = 0; c < a.nchunks; ++c) {
+            int v = __ldcg(&a.ws.chunk_base[(size_t)c * E + e]);
+            a.ws.chunk_base[(size_t)c * E + e] = run;
+            run += v;
+        }
+        cnt[e] = run;
+        a.ws.counts[e] = run;
+        ntile[e] = (run + a.NT - 1) / a.NT;
+    }
+    __syncthreads();
+    block_exclusive_scan(cnt, offs, E, warp_sums);
+    block_exclusive_scan(ntile, tbase, E, warp_sums);
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        a.ws.rowbase[e] = offs[e];
+        a.ws.tile_base[e] = tbase[e];
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        for (int c = 0; c < a.nchunks; ++c) a.ws.chunk_base[(size_t)c * E + e] += offs[e];
+    if (threadIdx.x == 0) a.ws.ticket[1] = 0;
+}
+
+// Pass 2: stable ranks inside each chunk (one warp walks the chunk in order;
+// equal experts inside 32 slots are ranked by lane), giving route_row and perm.
+__global__ void __launch_bounds__(32) k_compact_rank(DispatchArgs a) {
+    extern __shared__ int run[];  // [E]
+    const int lane = threadIdx.x;
+    const int E = a.E;
+    for (int e = lane; e < E; e += 32) run[e] = a.ws.chunk_base[(size_t)blockIdx.x * E + e];
+    __syncwarp();
+    const int nvr = read_nvr(a.nvr, a.T);
+    const unsigned lt = (1u << lane) - 1u;
+    for (int it = 0; it < kChunk / 32; ++it) {
+        const int s = blockIdx.x * kChunk + it * 32 + lane;
+        const bool in = s < a.T * a.K;
+        const int e = in ? a.ids[s] : -1;
+        const bool valid = in && (s / a.K) < nvr && e >= 0 && e < E;
+        const int key = valid ? e : (0x40000000 | lane);
+        const unsigned peers = __match_any_sync(kFull, key);
+        if (valid) {
+            const int p = run[e] + __popc(peers & lt);
+            a.ws.route_row[s] = p;
+            a.ws.perm[p] = s;
+        } else if (in) {
+            a.ws.route_row[s] = -1;
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(peers) - 1) run[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------- quant + scatter
+// MXFP8 quantisation of each valid row (E4M3 codes, one E8M0 scale per 32
+// along H, OCP MX rule: code = max(exponent(amax) - 8, 0), element =
+// RNE_satfinite(x * 2^(127-code))), written once per valid slot into the
+// expert's packed rows; the scale goes into the route tile's 128x4 scale atom
+// (byte 16*(c%32) + 4*(c/32) + kblock%4 for row c of the tile).
+struct QuantArgs {
+    const uint16_t* x;
+    const int32_t* ids;
+    const int32_t* nvr;
+    int T, K, E, H, mtpr, words, NT, scheme;
+    Workspace ws;
+};
+
+__device__ __forceinline__ uint32_t pack_fp8x4(float a, float b, float c, float d) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+__global__ void __launch_bounds__(256) k_quant_scatter(QuantArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= a.T) return;
+    const int nvr = read_nvr(a.nvr, a.T);
+    const int K = a.K;
+    int p = -1, gt = 0, c = 0;
+    bool valid = false;
+    if (lane < K) {
+        const int e = a.ids[(size_t)t * K + lane];
+        if (t < nvr && e >= a.E) atomicOr(a.ws.status, kStBadId);
+        valid = t < nvr && e >= 0 && e < a.E;
+        if (valid) {
+            int i;
+            if (a.scheme == 1) {
+                const uint32_t* wb = a.ws.occ + (size_t)e * a.words;
+                i = 0;
+                for (int w = 0; w < (t >> 5); ++w) i += __popc(__ldg(wb + w));
+                i += __popc(__ldg(wb + (t >> 5)) & ((1u << (t & 31)) - 1u));
+                p = e * a.mtpr + i;
+            } else {
+                p = a.ws.route_row[(size_t)t * K + lane];
+                i = p - __ldg(a.ws.rowbase + e);
+            }
+            gt = __ldg(a.ws.tile_base + e) + i / a.NT;
+            c = i % a.NT;
+        }
+        a.ws.yrow[(size_t)t * K + lane] = valid ? p : -1;
+    }
+    if (t >= nvr) return;
+    const unsigned vmask = __ballot_sync(kFull, valid);
+    int pk[kMaxTopk], gk[kMaxTopk], ck[kMaxTopk];
+#pragma unroll
+    for (int k = 0; k < kMaxTopk; ++k) {
+        pk[k] = __shfl_sync(kFull, p, k);
+        gk[k] = __shfl_sync(kFull, gt, k);
+        ck[k] = __shfl_sync(kFull, c, k);
+    }
+    const int H = a.H, nblk = H >> 5, ktiles = H >> 7;
+    const uint16_t* xrow = a.x + (size_t)t * H;
+    for (int blk = lane; blk < nblk; blk += 32) {
+        const uint4* src = reinterpret_cast<const uint4*>(xrow + blk * 32);
+        float f[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = __ldg(src + q);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[q * 8 + 2 * j] = __uint_as_float(w[j] << 16);
+                f[q * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+            }
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        int code = static_cast<int>(__float_as_uint(amax) >> 23) - 8;
+        code = code < 0 ? 0 : code;
+        const float mul = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            o[j] = pack_fp8x4(f[4 * j] * mul, f[4 * j + 1] * mul, f[4 * j + 2] * mul, f[4 * j + 3] * mul);
+        const uint4 o0 = make_uint4(o[0], o[1], o[2], o[3]), o1 = make_uint4(o[4], o[5], o[6], o[7]);
+        if (a.ws.xq) {
+            uint4* d = reinterpret_cast<uint4*>(a.ws.xq + (size_t)t * H + blk * 32);
+            d[0] = o0;
+            d[1] = o1;
+            a.ws.xs[(size_t)t * nblk + blk] = static_cast<uint8_t>(code);
+        }
+#pragma unroll
+        for (int k = 0; k < kMaxTopk; ++k) {
+            if (k < K && ((vmask >> k) & 1u)) {
+                uint4* d = reinterpret_cast<uint4*>(a.ws.aq + (size_t)pk[k] * H + blk * 32);
+                d[0] = o0;
+                d[1] = o1;
+                const int ci = ck[k];
+                a.ws.as[((size_t)gk[k] * ktiles + (blk >> 2)) * 512 + 16 * (ci & 31) + 4 * (ci >> 5) + (blk & 3)] =
+                    static_cast<uint8_t>(code);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- combine
+// out[t] = BF16( sum over valid slots, k ascending, of w[t,k] * y[row(t,k)] ),
+// float accumulation rounded once (ROCm/ATOM PR #2725: the MoE sum "in f32 and
+// rounds once"); -1 slots are skipped (aiter #6881: "its combine skips invalid
+// (-1) top-k slots"); rows with no valid slot are +0.
+struct CombineArgs {
+    const uint16_t* y;
+    const int32_t* yrow;
+    const float* w;
+    uint16_t* out;
+    int T, K, H;
+};
+
+__global__ void __launch_bounds__(128) k_combine(CombineArgs a) {
+    __shared__ int rows[kMaxTopk];
+    __shared__ float wk[kMaxTopk];
+    const int t = blockIdx.x;
+    if (threadIdx.x < a.K) {
+        rows[threadIdx.x] = a.yrow[(size_t)t * a.K + threadIdx.x];
+        wk[threadIdx.x] = a.w[(size_t)t * a.K + threadIdx.x];
+    }
+    __syncthreads();
+    const int nv = a.H >> 3;
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+        bool any = false;
+        for (int k = 0; k < a.K; ++k) {
+            const int r = rows[k];
+            if (r < 0) continue;
+            any = true;
+            const uint4 q = __ldg(reinterpret_cast<const uint4*>(a.y + (size_t)r * a.H) + v);
+            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+            const float wv = wk[k];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[2 * j] = __fadd_rn(acc[2 * j], __fmul_rn(wv, __uint_as_float(w4[j] << 16)));
+                acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __fmul_rn(wv, __uint_as_float(w4[j] & 0xffff0000u)));
+            }
+        }
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (any) {
+            uint32_t ow[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+                ow[j] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+        reinterpret_cast<uint4*>(a.out + (size_t)t * a.H)[v] = o;
+    }
+}
+
+DispatchArgs dispatch_args(const Geometry& g, const Workspace& ws, const int32_t* ids, int T, const int32_t* nvr) {
+    DispatchArgs a;
+    a.ids = ids;
+    a.nvr = nvr;
+    a.T = T;
+    a.K = g.K;
+    a.E = g.E;
+    a.mtpr = g.mtpr;
+    a.words = g.words;
+    a.NT = g.NT;
+    a.nchunks = (T * g.K + kChunk - 1) / kChunk;
+    a.ws = ws;
+    return a;
+}
+
+}  // namespace
+
+size_t workspace_layout(const Geometry& g, char* base, Workspace* ws) {
+    size_t off = 0;
+    auto carve = [&](size_t bytes) -> char* {
+        off = (off + 255) & ~size_t(255);
+        char* p = base ? base + off : nullptr;
+        off += bytes;
+        return p;
+    };
+    const size_t slots = (size_t)g.cap * g.K;
+    Workspace w{};
+    w.counts = reinterpret_cast<int32_t*>(carve(sizeof(int32_t) * g.E));
+    w.rowbase = reinterpret_cast<int32_t*>(carve(sizeof(int32_t) * (g.E + 1)));
+    w.tile_base = reinterpret_cast<int32_t*>(carve(sizeof(int32_t) * (g.E + 1)));
+    w.perm = reinterpret_cast<int32_t*>(carve(sizeof(int32_t) * slots));
+    w.route_row = reinterpret_cast<int32_t*>(carve(sizeof(int32_t) * slots));
+    w.route_slot = reinterpret_cast<int32_t*>(carve(sizeof(int32_t) * slots));
+    w.yrow = reinterpret_cast<int32_t*>(carve(sizeof(int32_t) * slots));
+    w.occ = reinterpret_cast<uint32_t*>(carve(sizeof(uint32_t) * (size_t)g.E * g.words));
+    w.chunk_base = reinterpret_cast<int32_t*>(carve(sizeof(int32_t) * (size_t)g.nchunks_cap * g.E));
+    w.ticket = reinterpret_cast<uint32_t*>(carve(sizeof(uint32_t) * 4));
+    w.status = reinterpret_cast<uint32_t*>(carve(sizeof(uint32_t) * 4));
+    w.aq = reinterpret_cast<uint8_t*>(carve((size_t)g.rows_cap * g.H));
+    w.as = reinterpret_cast<uint8_t*>(carve((size_t)g.tiles_cap * (g.H / 128) * 512));
+    w.hq = reinterpret_cast<uint8_t*>(carve((size_t)g.rows_cap * g.I));
+    w.hs = reinterpret_cast<uint8_t*>(carve((size_t)g.tiles_cap * (g.I / 128) * 512));
+    w.y = reinterpret_cast<uint16_t*>(carve((size_t)g.rows_cap * g.H * 2));
+    if (g.debug) {
+        w.xq = reinterpret_cast<uint8_t*>(carve((size_t)g.cap * g.H));
+        w.xs = reinterpret_cast<uint8_t*>(carve((size_t)g.cap * (g.H / 32)));
+        w.g = reinterpret_cast<float*>(carve((size_t)g.rows_cap * 2 * g.I * sizeof(float)));
+    }
+    off = (off + 255) & ~size_t(255);
+    if (ws) *ws = w;
+    return off;
+}
+
+cudaError_t launch_fixed_mark(const Geometry& g, const Workspace& ws, const int32_t* ids, int T,
+                              const int32_t* nvr, cudaStream_t s) {
+    DispatchArgs a = dispatch_args(g, ws, ids, T, nvr);
+    const int blocks = (T * g.K + 255) / 256;
+    k_fixed_mark<<<blocks, 256, sizeof(int) * (2 * g.E + 1), s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compact_dispatch(const Geometry& g, const Workspace& ws, const int32_t* ids, int T,
+                                    const int32_t* nvr, cudaStream_t s) {
+    DispatchArgs a = dispatch_args(g, ws, ids, T, nvr);
+    k_compact_count<<<a.nchunks, kChunk, sizeof(int) * (4 * g.E + 2), s>>>(a);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    k_compact_rank<<<a.nchunks, 32, sizeof(int) * g.E, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_scatter(const Geometry& g, const Workspace& ws, const uint16_t* x, const int32_t* ids,
+                                 int T, const int32_t* nvr, cudaStream_t s) {
+    QuantArgs a;
+    a.x = x;
+    a.ids = ids;
+    a.nvr = nvr;
+    a.T = T;
+    a.K = g.K;
+    a.E = g.E;
+    a.H = g.H;
+    a.mtpr = g.mtpr;
+    a.words = g.words;
+    a.NT = g.NT;
+    a.scheme = g.scheme;
+    a.ws = ws;
+    k_quant_scatter<<<(T + 7) / 8, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Geometry& g, const Workspace& ws, const float* wts, int T,
+                           const int32_t* /*nvr*/, uint16_t* out, cudaStream_t s) {
+    CombineArgs a;
+    a.y = ws.y;
+    a.yrow = ws.yrow;
+    a.w = wts;
+    a.out = out;
+    a.T = T;
+    a.K = g.K;
+    a.H = g.H;
+    k_combine<<<T, 128, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace bmoe

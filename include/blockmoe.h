@@ -1,0 +1,177 @@
+/*
+ * blockmoe.h -- C ABI of the fused block-scaled mixture-of-experts layer for
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * The layer (ROCm/aiter PR #6881 "[FlyDSL] MegaMoEV2: fuse Dispatch, GEMM1,
+ * GEMM2 and Combine into one kernel", Title and Technical Details; ROCm/aiter
+ * PR #6154 "Add full-expert DeepSeek V4.1 Flash MegaMoE tuning for gfx950",
+ * Summary), per token row t < num_valid_rows:
+ *   1. quantise the BF16 row to MXFP8: E4M3 codes, one E8M0 scale per 32
+ *      elements along H;
+ *   2. dispatch the row to each valid top-k expert (fixed-slot or compact
+ *      scheme, vLLM PR #61262 "second fixed-slot MegaMoEV2 runtime");
+ *   3. GEMM1 against the expert's MXFP4 W13 [2I,H] (E2M1 codes, one E8M0 scale
+ *      per 32 along H), SwiGLU epilogue (optional clamp), MXFP8 1x32
+ *      re-quantisation of the I intermediate values;
+ *   4. GEMM2 against the expert's MXFP4 W2 [H,I], rounded to BF16 per route;
+ *   5. combine: out[t] = BF16( sum over valid slots k, ascending, of
+ *      w[t,k] * y[t,k] ) accumulated in float and rounded once (ROCm/ATOM PR
+ *      #2725 "route before the rows move; per-pass real row counts", note on
+ *      the mono MoE sum).
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a CUDA device pointer to contiguous row-major
+ *     memory unless stated otherwise; the library never copies, frees or
+ *     keeps ownership of caller memory.
+ *   - Return value 0 is success; a negative MOE_E* code is an error and
+ *     moe_last_error() then describes it.  Nothing is thrown across the ABI.
+ *     A refused call changes no state of the handle.
+ *   - The library targets sm_103a only; moe_create refuses other devices.
+ *   - Entry points are not thread-safe on one handle; distinct handles are
+ *     independent.
+ */
+#ifndef BLOCKMOE_H
+#define BLOCKMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_ctx* moe_handle;
+/* A cudaStream_t; 0 is the legacy default stream (ROCm/aiter PR #6881, commit
+ * note on bindings: a null stream handle runs on the default stream, never on
+ * a newly created stream). */
+typedef void* moe_stream_t;
+
+/* ---------------------------------------------------------------- errors */
+#define MOE_OK 0
+#define MOE_EINVAL (-1)      /* bad argument (null pointer, bad size, bad option) */
+#define MOE_ENOTBOUND (-2)   /* moe_forward before moe_bind_weights */
+#define MOE_ESHAPE (-3)      /* H, I, E or topk not supported by the kernels */
+#define MOE_ECAPACITY (-4)   /* T larger than the capacity given to moe_create */
+#define MOE_ECUDA (-5)       /* a CUDA runtime or driver call failed */
+#define MOE_EDEVICE (-6)     /* current device is not an sm_103 GB300 */
+#define MOE_ENOMEM (-7)      /* workspace allocation failed or too small */
+#define MOE_ESTATE (-8)      /* call not allowed in the handle's state */
+
+/* ------------------------------------------------------ device status bits
+ * Written by the kernels into a device word, read with moe_read_status. */
+#define MOE_ST_BAD_ID 0x1u      /* a top-k id >= E was seen (skipped like -1) */
+#define MOE_ST_TIMEOUT 0x2u     /* a bounded device-side wait gave up */
+#define MOE_ST_OVERFLOW 0x4u    /* internal tile list overflow (bug guard) */
+
+/* ------------------------------------------------------------- options */
+#define MOE_OPT_DISPATCH 1        /* MOE_DISPATCH_* */
+#define MOE_OPT_SWIGLU_LIMIT 2    /* clamp L >= 0; 0 = plain SwiGLU (aiter #6154 "clamp-10 SwiGLU") */
+#define MOE_OPT_FIXED_SLOT_MAX 3  /* fixed-slot threshold on capacity, default 255
+                                     (vLLM PR #61262: FIXED_SLOT_MAX_MTPR) */
+#define MOE_OPT_DEBUG_CAPTURE 4   /* 1 = also keep canonical MXFP8 codes of x and raw GEMM1 outputs */
+#define MOE_OPT_ROUTE_TILE 5      /* route-tile width NT in {0 (auto), 32, 128} */
+
+#define MOE_DISPATCH_AUTO 0       /* fixed-slot iff capacity <= fixed-slot max */
+#define MOE_DISPATCH_FIXED 1
+#define MOE_DISPATCH_COMPACT 2
+
+/* --------------------------------------------------------- entry points */
+
+/* Create a layer instance for H (hidden), I (expert intermediate), E experts,
+ * top-k = topk, and at most `capacity` token rows per forward (the runtime's
+ * max tokens per rank, vLLM PR #61262).  Requirements: H and I multiples of
+ * 128 (MMA K-stage and 1x32 scale blocks), 1 <= topk <= 16, 1 <= E <= 4096,
+ * 1 <= capacity.  Allocates the device workspace with cudaMalloc on the
+ * current device unless moe_set_workspace is used before the first forward.
+ * On success *out receives the handle; on error *out is NULL. */
+int moe_create(moe_handle* out, int H, int I, int E, int topk, int capacity);
+
+/* Bind expert weights without copying (ROCm/aiter PR #6154, Changes and
+ * tuning: "a shared workspace bind[s] the current layer's prepared weights
+ * without copying them"):
+ *   w13_fp4 u8 [E, 2I, H/2]  E2M1 codes, element 2j in the low nibble of byte j;
+ *                            rows [0,I) gate, rows [I,2I) up
+ *   w13_sf  u8 [E, 2I, H/32] E8M0 scales (uint8 or float8_e8m0fnu bytes)
+ *   w2_fp4  u8 [E, H, I/2]
+ *   w2_sf   u8 [E, H, I/32]
+ * The caller keeps ownership; the memory must outlive the binding and every
+ * CUDA graph that captured a forward using it.  Everything is validated
+ * before any state changes, so a refused bind leaves the previous binding
+ * intact (aiter #6881, commit note: bind checks "everything that can refuse
+ * ... before changing any binding").  Rebinding is allowed between forwards. */
+int moe_bind_weights(moe_handle h, const void* w13_fp4, const void* w13_sf,
+                     const void* w2_fp4, const void* w2_sf);
+
+/* One forward on `stream`:
+ *   x              bf16 [T, H]
+ *   topk_ids       int32 [T, topk]; -1 (or any id outside [0,E)) marks an
+ *                  invalid slot that claims no slot and adds nothing (ROCm/ATOM
+ *                  PR #2725 linked fix: "a route with a negative id now claims
+ *                  no slot"); ids >= E also set MOE_ST_BAD_ID
+ *   topk_weights   float32 [T, topk]
+ *   num_valid_rows device int32, first element = rows to compute, clamped to
+ *                  [0,T]; NULL means T.  Read on the device, so a replayed CUDA
+ *                  graph follows the value at replay time (ATOM #2725,
+ *                  "Per-pass real row counts").  Rows at or past it give +0.
+ *   out            bf16 [T, H]; every row is written (T = 0 writes nothing)
+ * No host synchronisation, no allocation; enqueues only on `stream`, so the
+ * call can be captured in a CUDA graph.  Returns MOE_ECAPACITY if T exceeds
+ * the capacity, MOE_ENOTBOUND without weights. */
+int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const float* topk_weights,
+                const int32_t* num_valid_rows, void* out, int T, moe_stream_t stream);
+
+/* Release the handle and the workspace it allocated (not caller memory). */
+void moe_destroy(moe_handle h);
+
+/* ------------------------------------------------------ supporting calls */
+
+/* Set an option (MOE_OPT_*) before the first forward; MOE_ESTATE afterwards
+ * for options that change the workspace layout (dispatch, route tile). */
+int moe_set_option(moe_handle h, int key, double value);
+int moe_get_option(moe_handle h, int key, double* value);
+
+/* Bytes of device workspace the handle needs with its current options. */
+size_t moe_workspace_bytes(moe_handle h);
+
+/* Use caller memory (e.g. from the torch caching allocator) as workspace
+ * instead of the library's own allocation.  dev_ptr must be 256-byte aligned
+ * and hold moe_workspace_bytes(h) bytes; the caller keeps ownership and must
+ * keep it alive while the handle uses it. */
+int moe_set_workspace(moe_handle h, void* dev_ptr, size_t bytes);
+
+/* Read and clear the device status word (MOE_ST_* bits).  Synchronises
+ * `stream`; never called implicitly by moe_forward. */
+int moe_read_status(moe_handle h, uint32_t* flags, moe_stream_t stream);
+
+/* Text of the last error on this handle (or of the last failed moe_create
+ * when h is NULL).  Valid until the next call on the same handle. */
+const char* moe_last_error(moe_handle h);
+
+/* Which dispatch scheme the handle runs: MOE_DISPATCH_FIXED or _COMPACT. */
+int moe_dispatch_scheme(moe_handle h);
+
+/* ------------------------------------------- test-only introspection
+ * Copies one internal array of the last forward into host memory
+ * (synchronises `stream`).  `which` is a MOE_DBG_* id; *bytes receives the
+ * region size when host_dst is NULL.  The layouts are those documented next
+ * to each id; they exist so that tests can compare the dispatch and the MXFP8
+ * codes bit-exactly with an independent implementation. */
+#define MOE_DBG_COUNTS 1        /* int32 [E]: routes (compact) / occupied slots (fixed) per expert */
+#define MOE_DBG_OFFSETS 2       /* int32 [E+1]: compact exclusive scan of counts */
+#define MOE_DBG_PERM 3          /* int32 [T*topk]: compact packed position -> flat slot t*topk+k */
+#define MOE_DBG_ROUTE_ROW 4     /* int32 [T*topk]: compact slot -> packed position, -1 invalid */
+#define MOE_DBG_ROUTE_SLOT 5    /* int32 [T*topk]: fixed slot -> e*capacity+t, -1 invalid */
+#define MOE_DBG_OCC 6           /* uint32 [E][ceil(capacity/32)]: fixed-slot occupancy bits */
+#define MOE_DBG_XQ 7            /* uint8 [T][H]: canonical E4M3 codes of x (needs DEBUG_CAPTURE) */
+#define MOE_DBG_XS 8            /* uint8 [T][H/32]: canonical E8M0 scales of x (needs DEBUG_CAPTURE) */
+#define MOE_DBG_YROW 9          /* int32 [T*topk]: row of the GEMM2 output each slot combines, -1 invalid */
+#define MOE_DBG_HQ 10           /* uint8 [rows][I]: E4M3 codes of h per packed row */
+#define MOE_DBG_G 11            /* float [rows][2I]: raw GEMM1 outputs (needs DEBUG_CAPTURE) */
+#define MOE_DBG_Y 12            /* bf16 [rows][H]: GEMM2 outputs per packed row */
+#define MOE_DBG_TILES 13        /* int32 [1 + 3*tiles]: tile count, then (expert, row0, n) per tile */
+int moe_debug_copy(moe_handle h, int which, void* host_dst, size_t* bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BLOCKMOE_H */

@@ -1,0 +1,64 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads,
+exports every function include/blockmoe.h declares, and refuses bad shapes
+before touching the device."""
+
+import ctypes
+
+import pytest
+
+import block_scaled_moe_gb300 as bm
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_scaled_moe_gb300 import _build
+    _build.build()
+    return bm.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = bm.exported_symbols_from_header()
+    expected = {"moe_create", "moe_bind_weights", "moe_forward", "moe_destroy", "moe_set_option",
+                "moe_get_option", "moe_workspace_bytes", "moe_set_workspace", "moe_read_status",
+                "moe_last_error", "moe_dispatch_scheme", "moe_debug_copy"}
+    assert expected <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_header_constants_parse():
+    assert bm.MOE_OK == 0 and bm.MOE_ECAPACITY == -4 and bm.MOE_ST_TIMEOUT == 2
+    assert bm.MOE_DISPATCH_COMPACT == 2 and bm.MOE_DBG_TILES == 13
+
+
+@pytest.mark.parametrize("H,I,E,topk,cap,code", [
+    (100, 128, 8, 2, 64, -3),      # H not a multiple of 128
+    (256, 96, 8, 2, 64, -3),       # I not a multiple of 128
+    (256, 128, 0, 2, 64, -3),      # no experts
+    (256, 128, 8, 17, 64, -3),     # top-k above 16
+    (256, 128, 8, 2, 0, -1),       # zero capacity
+])
+def test_create_refuses_bad_shapes_before_cuda(lib, H, I, E, topk, cap, code):
+    h = ctypes.c_void_p()
+    rc = lib.moe_create(ctypes.byref(h), H, I, E, topk, cap)
+    assert rc == code
+    assert not h.value
+    assert lib.moe_last_error(None)
+
+
+def test_null_handle_calls_are_refused(lib):
+    assert lib.moe_forward(None, None, None, None, None, None, 0, None) == bm.MOE_EINVAL
+    assert lib.moe_bind_weights(None, None, None, None, None) == bm.MOE_EINVAL
+    assert lib.moe_set_option(None, 1, 0.0) == bm.MOE_EINVAL
+    assert lib.moe_workspace_bytes(None) == 0
+    lib.moe_destroy(None)
+
+
+def test_create_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    rc = lib.moe_create(ctypes.byref(h), 256, 128, 8, 2, 64)
+    assert rc in (bm.MOE_ECUDA, bm.MOE_EDEVICE)
+    assert not h.value

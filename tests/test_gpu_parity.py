@@ -1,0 +1,337 @@
+"""GPU parity: the CUDA layer (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+* dispatch indices and the input MXFP8 codes/scales: bit-exact;
+* outputs: relative L2 <= 1e-2 and |d| <= 0.08*|ref| + 1e-2*rms(ref);
+* edge cases: empty and ragged inputs, num_valid_rows 0 / NULL / beyond T,
+  all-invalid rows, ids >= E, repeated experts in a row, multi-tile experts;
+* behaviour: CUDA-graph replay equals eager bitwise, zero W2 gives zero and a
+  rebind restores the result bitwise, explicit and null streams, refused binds
+  keep the previous binding.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity_util import Case, assert_close, compare, torch_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a GB300"
+    torch.cuda.set_device(0)
+
+
+def _out_bits(t):
+    return torch_bf16_bits(t)
+
+
+# ------------------------------------------------------------------ tiny workload
+
+@pytest.mark.parametrize("dispatch", ["compact", "fixed"])
+@pytest.mark.parametrize("route_tile", [128, 32])
+def test_tiny_matches_oracle(dispatch, route_tile):
+    c = Case(synth.get("tiny"))
+    L = c.layer(dispatch=dispatch, route_tile=route_tile)
+    out = c.run(L)
+    torch.cuda.synchronize()
+    got = _out_bits(out)
+    ref = c.oracle()
+    assert_close(got, ref, f"tiny {dispatch} NT={route_tile}")
+    assert np.all(got[c.w.nvr:] == 0)
+    assert L.read_status() == 0
+
+
+def test_tiny_compact_dispatch_bit_exact():
+    c = Case(synth.get("tiny"))
+    L = c.layer(dispatch="compact", debug=True)
+    c.run(L)
+    torch.cuda.synchronize()
+    d = oracle.dispatch_compact(c.ids, c.w.E, c.w.nvr)
+    assert np.array_equal(L.debug_array("counts"), d["counts"])
+    assert np.array_equal(L.debug_array("offsets"), d["offsets"])
+    R = int(d["offsets"][-1])
+    assert np.array_equal(L.debug_array("perm")[:R], d["perm"])
+    assert np.array_equal(L.debug_array("route_row").reshape(c.w.T, c.w.K), d["route_row"])
+
+
+def test_tiny_fixed_dispatch_bit_exact():
+    c = Case(synth.get("tiny"))
+    L = c.layer(dispatch="fixed", debug=True)
+    assert L.scheme == "fixed"
+    c.run(L)
+    torch.cuda.synchronize()
+    d = oracle.dispatch_fixed(c.ids, c.w.E, c.w.capacity, c.w.nvr)
+    assert np.array_equal(L.debug_array("counts"), d["counts"])
+    assert np.array_equal(L.debug_array("occ").reshape(c.w.E, -1), d["occ"])
+    assert np.array_equal(L.debug_array("route_slot").reshape(c.w.T, c.w.K), d["route_slot"])
+
+
+def test_tiny_input_quantisation_bit_exact():
+    c = Case(synth.get("tiny"))
+    L = c.layer(debug=True)
+    c.run(L)
+    torch.cuda.synchronize()
+    n = c.w.nvr
+    codes, scales = oracle.quant_mxfp8_rows(c.x[:n])
+    xq = L.debug_array("xq").reshape(c.w.T, c.w.H)[:n]
+    xs = L.debug_array("xs").reshape(c.w.T, c.w.H // 32)[:n]
+    assert np.array_equal(xs, scales)
+    assert np.array_equal(xq, codes)
+
+
+def test_tiny_gemm1_outputs_match_oracle_intermediates():
+    """Raw GEMM1 outputs (debug capture) against the oracle's g of each route."""
+    c = Case(synth.get("tiny"))
+    L = c.layer(debug=True)
+    c.run(L)
+    torch.cuda.synchronize()
+    w = c.w
+    g = L.debug_array("g").reshape(-1, 2 * w.I)
+    yrow = L.debug_array("yrow").reshape(w.T, w.K)
+    errs = []
+    for t in range(0, w.nvr, 7):
+        for k in range(w.K):
+            e = int(c.ids[t, k])
+            if e < 0:
+                assert yrow[t, k] == -1
+                continue
+            ref = oracle.route_intermediates(c.x[t], e, c.Wh, w.swiglu_limit)["g"].astype(np.float64)
+            got = g[yrow[t, k]].astype(np.float64)
+            errs.append(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    assert errs and max(errs) < 1e-4, max(errs)
+
+
+# ------------------------------------------------------------------ edge cases
+
+MICRO = [
+    # T, H, I, E, K, nvr, routing, invalid, limit, dispatch, route_tile
+    (1, 128, 128, 1, 1, 1, "uniform", 0.0, 0.0, "compact", 128),
+    (5, 256, 128, 3, 2, 5, "uniform", 0.0, 0.0, "fixed", 32),
+    (37, 128, 256, 4, 3, 30, "uniform", 0.3, 10.0, "compact", 32),
+    (300, 128, 128, 2, 2, 300, "uniform", 0.0, 0.0, "compact", 128),   # experts with 3 route tiles
+    (300, 128, 128, 2, 2, 250, "uniform", 0.1, 0.0, "fixed", 128),     # fixed slots, capacity 300
+    (200, 256, 128, 6, 4, 190, "hot_zipf", 0.0, 0.0, "compact", 32),   # repeated experts per row
+    (64, 384, 384, 5, 2, 64, "hot_zipf", 0.0, 10.0, "fixed", 128),     # repeated experts share a slot
+]
+
+
+@pytest.mark.parametrize("cfg", MICRO, ids=[f"T{m[0]}H{m[1]}I{m[2]}E{m[3]}K{m[4]}{m[9]}{m[10]}" for m in MICRO])
+def test_micro_workloads(cfg):
+    T, H, I, E, K, nvr, routing, inv, lim, disp, nt = cfg
+    w = synth.micro(T, H, I, E, K, nvr=nvr, routing=routing, invalid_frac=inv, swiglu_limit=lim, dispatch=disp,
+                    seed=T * 7 + E, hot_frac=0.5)
+    c = Case(w)
+    L = c.layer(route_tile=nt)
+    out = c.run(L)
+    torch.cuda.synchronize()
+    got = _out_bits(out)
+    assert_close(got, c.oracle(), str(cfg))
+    assert L.read_status() == 0
+
+
+def test_num_valid_rows_variants():
+    w = synth.micro(40, 128, 128, 4, 2, nvr=40, invalid_frac=0.0, seed=3)
+    c = Case(w)
+    L = c.layer()
+    base = _out_bits(c.run(L, nvr=False))
+    assert_close(base, c.oracle(nvr=False), "nvr NULL")
+    for v, expect_rows in [(40, 40), (1000, 40), (17, 17), (0, 0), (-5, 0)]:
+        c.nvrd.fill_(v)
+        got = _out_bits(c.run(L))
+        torch.cuda.synchronize()
+        if expect_rows:
+            assert np.array_equal(got[:expect_rows], base[:expect_rows]), v
+        assert np.all(got[expect_rows:] == 0), v
+
+
+def test_all_invalid_and_zero_rows():
+    w = synth.micro(16, 128, 128, 4, 2, invalid_frac=0.0, seed=8)
+    c = Case(w)
+    c.idsd.fill_(-1)
+    L = c.layer()
+    got = _out_bits(c.run(L))
+    torch.cuda.synchronize()
+    assert np.all(got == 0)
+    # T = 0 is accepted and writes nothing
+    empty = torch.empty((0, w.H), dtype=torch.bfloat16, device="cuda")
+    L.forward(empty, torch.empty((0, w.K), dtype=torch.int32, device="cuda"),
+              torch.empty((0, w.K), dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+
+
+def test_ids_beyond_E_are_skipped_and_flagged():
+    w = synth.micro(16, 128, 128, 4, 2, invalid_frac=0.0, seed=12)
+    c = Case(w)
+    ids = c.ids.copy()
+    ids[3, 1] = 7
+    ids[9, 0] = 1000
+    c.idsd.copy_(torch.from_numpy(ids))
+    L = c.layer()
+    got = _out_bits(c.run(L))
+    torch.cuda.synchronize()
+    ref = oracle.moe_forward(c.x, ids, c.wts, c.Wh, num_valid_rows=w.nvr)
+    assert_close(got, ref, "ids >= E")
+    assert L.read_status() & 0x1
+    assert L.read_status() == 0      # read clears
+
+
+def test_capacity_is_enforced():
+    import block_scaled_moe_gb300 as bm
+    c = Case(synth.get("tiny"))
+    L = c.layer()
+    x = torch.zeros((65, c.w.H), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(bm.MoeError) as ei:
+        L.forward(x, torch.zeros((65, 2), dtype=torch.int32, device="cuda"),
+                  torch.zeros((65, 2), dtype=torch.float32, device="cuda"))
+    assert ei.value.code == bm.MOE_ECAPACITY
+
+
+# ------------------------------------------------------------------ behaviour
+
+def test_graph_replay_equals_eager():
+    c = Case(synth.get("tiny"))
+    L = c.layer()
+    eager = _out_bits(c.run(L))
+    s = torch.cuda.Stream()
+    out = torch.empty_like(c.xd)
+    with torch.cuda.stream(s):
+        c.run(L, out=out, stream=s)      # warm-up on the capture stream
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        c.run(L, out=out, stream=s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(_out_bits(out), eager)
+    # the graph follows num_valid_rows at replay time
+    c.nvrd.fill_(10)
+    g.replay()
+    torch.cuda.synchronize()
+    got = _out_bits(out)
+    assert np.array_equal(got[:10], eager[:10]) and np.all(got[10:] == 0)
+
+
+def test_zero_w2_then_rebind_restores_bitwise():
+    c = Case(synth.get("tiny"))
+    L = c.layer()
+    a = _out_bits(c.run(L))
+    zw2 = torch.zeros_like(c.Wd[2])
+    L.bind_weights(c.Wd[0], c.Wd[1], zw2, c.Wd[3])
+    z = _out_bits(c.run(L))
+    torch.cuda.synchronize()
+    assert np.all(z == 0)
+    L.bind_weights(*c.Wd)
+    b = _out_bits(c.run(L))
+    torch.cuda.synchronize()
+    assert np.array_equal(a, b)
+
+
+def test_explicit_and_null_streams():
+    c = Case(synth.get("tiny"))
+    L = c.layer()
+    ref = _out_bits(c.run(L))
+    s = torch.cuda.Stream()
+    out = torch.empty_like(c.xd)
+    with torch.cuda.stream(s):
+        L.forward(c.xd, c.idsd, c.wtsd, c.nvrd, out=out, stream=s)
+    s.synchronize()
+    assert np.array_equal(_out_bits(out), ref)
+    out2 = torch.empty_like(c.xd)
+    import block_scaled_moe_gb300 as bm
+    torch.cuda.synchronize()
+    bm.moe_forward(L.h, c.xd.data_ptr(), c.idsd.data_ptr(), c.wtsd.data_ptr(), c.nvrd.data_ptr(),
+                   out2.data_ptr(), c.w.T, 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(_out_bits(out2), ref)
+
+
+def test_refused_bind_keeps_previous_binding():
+    import block_scaled_moe_gb300 as bm
+    c = Case(synth.get("tiny"))
+    L = c.layer()
+    a = _out_bits(c.run(L))
+    with pytest.raises(bm.MoeError):
+        # an odd byte offset: misaligned for the tensor-map descriptor
+        bm.moe_bind_weights(L.h, c.Wd[0].data_ptr() + 1, c.Wd[1].data_ptr(), c.Wd[2].data_ptr(),
+                            c.Wd[3].data_ptr())
+    with pytest.raises(ValueError):
+        L.bind_weights(c.Wd[0][:, ::2], c.Wd[1], c.Wd[2], c.Wd[3])     # strided view refused
+    with pytest.raises(ValueError):
+        L.bind_weights(c.Wd[0], c.Wd[1].view(torch.float8_e4m3fn), c.Wd[2], c.Wd[3])  # not an E8M0 view
+    b = _out_bits(c.run(L))
+    torch.cuda.synchronize()
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def _full_size(name, n_rows, **kw):
+    w = synth.get(name)
+    c = Case(w, weights_on_device=True)
+    L = c.layer(**kw)
+    out = c.run(L)
+    torch.cuda.synchronize()
+    got = _out_bits(out)
+    rng = np.random.default_rng(0)
+    valid_rows = np.arange(min(w.nvr, w.T))
+    rows = np.sort(rng.choice(valid_rows, size=min(n_rows, len(valid_rows)), replace=False))
+    ref = c.oracle(rows=rows)
+    cmp_ = assert_close(got[rows], ref, name)
+    assert np.all(got[w.nvr:] == 0)
+    assert L.read_status() == 0
+    return c, L, cmp_
+
+
+def test_full_decode_flash():
+    c, L, _ = _full_size("decode_flash", 24)
+    assert L.scheme == "fixed"
+
+
+def test_full_decode_flash_dispatch_and_quant_bit_exact():
+    w = synth.get("decode_flash")
+    c = Case(w, weights_on_device=True)
+    L = c.layer(debug=True)
+    c.run(L)
+    torch.cuda.synchronize()
+    d = oracle.dispatch_fixed(c.ids, w.E, w.capacity, w.nvr)
+    assert np.array_equal(L.debug_array("counts"), d["counts"])
+    assert np.array_equal(L.debug_array("route_slot").reshape(w.T, w.K), d["route_slot"])
+    codes, scales = oracle.quant_mxfp8_rows(c.x)
+    assert np.array_equal(L.debug_array("xs").reshape(w.T, -1), scales)
+    assert np.array_equal(L.debug_array("xq").reshape(w.T, -1), codes)
+
+
+@pytest.mark.parametrize("name,rows", [("smallm_pro", 12), ("largem_pro", 8), ("skewed_flash", 12)])
+def test_full_size_prefill_workloads(name, rows):
+    _full_size(name, rows)
+
+
+def test_full_largem_compact_dispatch_bit_exact():
+    w = synth.get("largem_pro")
+    ids, _ = synth.make_routing(w)
+    c_ids = torch.from_numpy(ids).cuda()
+    import block_scaled_moe_gb300 as bm
+    L = bm.BlockScaledMoE(w.H, w.I, w.E, w.K, w.capacity, debug=False)
+    Wz = [torch.zeros(s, dtype=torch.uint8, device="cuda") for s in
+          [(w.E, 2 * w.I, w.H // 2), (w.E, 2 * w.I, w.H // 32), (w.E, w.H, w.I // 2), (w.E, w.H, w.I // 32)]]
+    L.bind_weights(*Wz)
+    x = torch.zeros((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+    out = L.forward(x, c_ids, torch.ones((w.T, w.K), dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    d = oracle.dispatch_compact(ids, w.E, w.nvr)
+    assert np.array_equal(L.debug_array("counts"), d["counts"])
+    assert np.array_equal(L.debug_array("offsets"), d["offsets"])
+    R = int(d["offsets"][-1])
+    assert np.array_equal(L.debug_array("perm")[:R], d["perm"])
+    assert np.array_equal(L.debug_array("route_row").reshape(w.T, w.K), d["route_row"])
+    assert torch.count_nonzero(out).item() == 0
