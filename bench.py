@@ -1,0 +1,355 @@
+"""Benchmark of the fused block-scaled MoE layer on GB300.
+
+One step = one forward of the whole layer (dispatch, MXFP8 quantisation,
+GEMM1 + SwiGLU + re-quantisation, GEMM2, combine) over one batch of synthetic
+rows.  Default workload: decode, fixed-slot, DeepSeek-V4-Flash shape (T=128,
+H=5120, I=2304, 384 experts, top-6, MTPR 128, clamp-10 SwiGLU).
+
+Prints one JSON line.  `value` is MoE-layer tokens/s with inputs resident in
+HBM; `e2e` is the same metric through the public API with host buffers (H2D of
+the step's inputs and D2H of its output inside the timed region); `roofline`
+reports GEMM1 (the dominant kernel: it streams 2/3 of the active-expert
+weight bytes) against the measured HBM copy bandwidth; `cpu_baseline` times
+the CPU oracle on a bounded sample of the same workload.
+
+--impl reference times the CPU oracle itself on the same workload (bounded
+row sample per step) and prints the same line with "impl": "reference".
+Multi-GPU (torchrun): every rank runs an independent replica (the layer does
+not shard on one GPU per box); value = tokens of all ranks / max rank time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Fused MoE tokens/s per T; decode % of HBM BW, prefill % of FP8 MMA peak"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="decode_flash")
+    p.add_argument("--cpu-rows", type=int, default=16, help="oracle sample rows for the CPU baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+                self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def workload_bytes_flops(w, ids):
+    """Algorithmic HBM bytes and FLOPs of one forward from the actual routing."""
+    import numpy as np
+    v = ids[: w.nvr].reshape(-1)
+    v = v[(v >= 0) & (v < w.E)]
+    if w.dispatch == "fixed":
+        rows = len({(int(t), int(e)) for t, row in enumerate(ids[: w.nvr]) for e in row if 0 <= e < w.E})
+    else:
+        rows = int(v.size)
+    active = int(np.unique(v).size)
+    H, I = w.H, w.I
+    w13 = active * 2 * I * H * 17 // 32          # codes (1/2 B) + scales (1/32 B) per element
+    w2 = active * H * I * 17 // 32
+    x_bytes = w.nvr * H * 2 + w.T * H * 2         # read x, write out (bf16)
+    gemm1_act = rows * (H + H // 32) + rows * (I + I // 32)  # read packed rows, write h
+    flops = 6 * H * I * rows
+    return {"active": active, "routes": rows, "w13": w13, "w2": w2, "step": w13 + w2 + x_bytes,
+            "gemm1": w13 + gemm1_act, "flops": flops}
+
+
+def source_sha():
+    h = hashlib.sha256()
+    for f in ("moe_gemm.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "block_scaled_moe_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload, ntiles_key):
+    """dram bytes of GEMM1 per launch from a committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_sha") == source_sha():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def cpu_baseline(w, x, ids, wts, Wh, rows_n):
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(np.arange(w.nvr), size=min(rows_n, w.nvr), replace=False)).astype(np.int32)
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    t0 = time.perf_counter()
+    oracle.moe_forward(x, ids, wts, Wh, num_valid_rows=w.nvr, swiglu_limit=w.swiglu_limit, rows=rows,
+                       nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": len(rows) / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} of {w.nvr} valid rows of the {w.name} workload (seeded), "
+                      f"{dt:.2f} s wall on {threads} threads"}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import numpy as np
+    import torch
+
+    import synth
+    w = synth.get(args.workload)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        import oracle
+        oracle.build()
+        x, ids, wts = synth.make_x(w), *synth.make_routing(w)
+        Wh = [t.cpu() for t in synth.make_weights(w, "cuda" if torch.cuda.is_available() else "cpu")]
+        threads = len(os.sched_getaffinity(0))
+        rng = np.random.default_rng(2)
+        times, ntok = [], 0
+        for i in range(args.warmup + args.steps):
+            rows = np.sort(rng.choice(np.arange(w.nvr), size=min(4, w.nvr), replace=False)).astype(np.int32)
+            t0 = time.perf_counter()
+            oracle.moe_forward(x, ids, wts, Wh, num_valid_rows=w.nvr, swiglu_limit=w.swiglu_limit, rows=rows,
+                               nthreads=threads)
+            dt = time.perf_counter() - t0
+            if i >= args.warmup:
+                times.append(dt)
+                ntok += len(rows)
+        total = sum(times)
+        val = ntok / total
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic",
+                "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "topk": w.K,
+                           "num_valid_rows": w.nvr, "dispatch": w.dispatch, "step_sample_rows": 4},
+                "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                 "sample": f"4 seeded rows of {w.nvr} per step, {args.steps} steps"},
+                "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_scaled_moe_gb300 as bm
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    x = synth.make_x(w)
+    ids, wts = synth.make_routing(w)
+    W = synth.make_weights(w, dev)
+    layer = bm.BlockScaledMoE(w.H, w.I, w.E, w.K, w.capacity, dispatch=w.dispatch, swiglu_limit=w.swiglu_limit)
+    layer.bind_weights(*W)
+    xd = x.to(dev)
+    idsd = torch.from_numpy(ids).to(dev)
+    wtsd = torch.from_numpy(wts).to(dev)
+    nvrd = torch.tensor([w.nvr], dtype=torch.int32, device=dev)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 512 MiB > 129 MB L2
+
+    def step():
+        layer.forward(xd, idsd, wtsd, nvrd, out=out, stream=stream)
+
+    layer.set_profile(True)
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    status = layer.read_status()
+    if status:
+        raise RuntimeError(f"device status {status:#x} after warm-up")
+
+    # ---- timed region: device-resident inputs, L2 flushed between steps (outside the events)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stage_ms = []
+    launches0 = layer.launches
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(1.0)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+            stage_ms.append(layer.profile_ms())
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = layer.launches - launches0
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens = w.nvr * args.steps * world
+    value = tokens / (total_ms / 1e3)
+
+    # ---- end to end: pinned host buffers, H2D inputs + forward + D2H output per step
+    xh = x.pin_memory()
+    idsh = torch.from_numpy(ids).pin_memory()
+    wtsh = torch.from_numpy(wts).pin_memory()
+    nvrh = torch.tensor([w.nvr], dtype=torch.int32).pin_memory()
+    outh = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+    xe, ie, we, ne = torch.empty_like(xd), torch.empty_like(idsd), torch.empty_like(wtsd), torch.empty_like(nvrd)
+    h2d = xh.numel() * 2 + idsh.numel() * 4 + wtsh.numel() * 4 + 4
+    d2h = outh.numel() * 2
+    layer.set_profile(False)
+
+    def e2e_step():
+        xe.copy_(xh, non_blocking=True)
+        ie.copy_(idsh, non_blocking=True)
+        we.copy_(wtsh, non_blocking=True)
+        ne.copy_(nvrh, non_blocking=True)
+        layer.forward(xe, ie, we, ne, out=out, stream=stream)
+        outh.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(1.0)
+        es[i].record(stream)
+        e2e_step()
+        ee[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee))
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = tokens / (e2e_ms / 1e3)
+
+    # ---- roofline of GEMM1 from its live CUDA-event durations
+    wb = workload_bytes_flops(w, ids)
+    g1_ms = statistics.mean(s[2] for s in stage_ms)
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = peaks()
+    achieved = wb["gemm1"] / (g1_ms / 1e3) / 1e9
+    traffic = traffic_for(w.name, None)
+    step_gbs = wb["step"] / (total_ms / args.steps / world / 1e3) / 1e9
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8 x mxfp4 (e4m3 x e2m1, fp32 accumulate)",
+            "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "topk": w.K,
+                       "num_valid_rows": w.nvr, "dispatch": layer.scheme, "capacity": w.capacity,
+                       "swiglu_limit": w.swiglu_limit, "routes": wb["routes"], "active_experts": wb["active"],
+                       "l2": "512 MiB buffer written between timed steps (outside the events)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"kernel": "GEMM1 (tcgen05 block-scaled, W13 stream + SwiGLU/MXFP8 epilogue)",
+                         "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "traffic": traffic, "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": wb["gemm1"], "launch_ms": g1_ms},
+            "step_roofline": {"bytes_per_step": wb["step"], "achieved_gbs": step_gbs,
+                              "frac_of_hbm": step_gbs / hbm_gbs,
+                              "tflops": wb["flops"] / (total_ms / args.steps / world / 1e3) / 1e12,
+                              "stage_ms_mean": [statistics.mean(s[i] for s in stage_ms) for i in range(5)],
+                              "stages": ["dispatch", "quant+scatter", "gemm1", "gemm2", "combine"]},
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches * world,
+            "clocks": clk.summary()}
+    if rank == 0 and not args.no_cpu_baseline:
+        Wh = [t.cpu() for t in W]
+        line["cpu_baseline"] = cpu_baseline(w, x, ids, wts, Wh, args.cpu_rows)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    layer.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

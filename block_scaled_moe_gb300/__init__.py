@@ -76,6 +76,8 @@ def load(path: Optional[str] = None):
         lib.moe_dispatch_scheme.restype = i32
         lib.moe_debug_copy.argtypes = [vp, i32, vp, ctypes.POINTER(sz), vp]
         lib.moe_debug_copy.restype = i32
+        lib.moe_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32]
+        lib.moe_profile_read.restype = i32
         _lib = lib
         return lib
 
@@ -149,6 +151,12 @@ def moe_dispatch_scheme(h) -> int:
     return load().moe_dispatch_scheme(h)
 
 
+def moe_profile_read(h) -> list:
+    ms = (ctypes.c_float * 5)()
+    _check(h, load().moe_profile_read(h, ms, 5))
+    return list(ms)
+
+
 def moe_debug_copy(h, which: int, stream: int = 0) -> bytes:
     lib = load()
     n = ctypes.c_size_t(0)
@@ -206,6 +214,17 @@ class BlockScaledMoE:
     @property
     def workspace_bytes(self) -> int:
         return moe_workspace_bytes(self.h)
+
+    @property
+    def launches(self) -> int:
+        return int(moe_get_option(self.h, MOE_OPT_LAUNCHES))
+
+    def set_profile(self, on: bool = True):
+        moe_set_option(self.h, MOE_OPT_PROFILE, 1 if on else 0)
+
+    def profile_ms(self) -> list:
+        """[dispatch, quant, GEMM1, GEMM2, combine] ms of the last profiled forward."""
+        return moe_profile_read(self.h)
 
     def _dev(self, t, name, shape, dtypes):
         import torch

@@ -41,6 +41,10 @@ struct moe_ctx {
     const uint8_t* w2s = nullptr;
     CUtensorMap tm_w13{}, tm_w2{}, tm_aq{}, tm_hq{};
     int last_T = 0;
+    int profile = 0;
+    bool profiled = false;
+    cudaEvent_t ev[MOE_PROFILE_STAGES + 1] = {};
+    unsigned long long launches = 0;
     std::string err;
 };
 
@@ -246,6 +250,8 @@ int moe_create(moe_handle* out, int H, int I, int E, int topk, int capacity) {
 
 void moe_destroy(moe_handle h) {
     if (!h) return;
+    for (auto& e : h->ev)
+        if (e) cudaEventDestroy(e);
     release_workspace(h);
     delete h;
 }
@@ -294,6 +300,11 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Workspace& ws = h->ws;
     cudaError_t e;
+    const bool prof = h->profile != 0;
+    auto mark = [&](int i) {
+        if (prof) cudaEventRecord(h->ev[i], s);
+    };
+    mark(0);
     if (g.scheme == 1) {
         e = cudaMemsetAsync(ws.occ, 0, sizeof(uint32_t) * (size_t)g.E * g.words, s);
         if (e != cudaSuccess) return cuda_fail(h, e, "clearing occupancy");
@@ -302,8 +313,12 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
         e = bmoe::launch_compact_dispatch(g, ws, topk_ids, T, num_valid_rows, s);
     }
     if (e != cudaSuccess) return cuda_fail(h, e, "dispatch launch");
+    h->launches += g.scheme == 1 ? 1 : 2;
+    mark(1);
     e = bmoe::launch_quant_scatter(g, ws, static_cast<const uint16_t*>(x), topk_ids, T, num_valid_rows, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "quant launch");
+    h->launches += 1;
+    mark(2);
 
     bmoe::GemmArgs a{};
     a.counts = ws.counts;
@@ -327,6 +342,8 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     a.g_dbg = g.debug ? ws.g : nullptr;
     e = bmoe::launch_gemm1(a, &h->tm_w13, &h->tm_aq, g.NT, h->num_sms, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "GEMM1 launch");
+    h->launches += 1;
+    mark(3);
     // GEMM2: W2 x h rows, K = I
     a.w_sf = h->w2s;
     a.w_rows = g.H;
@@ -339,8 +356,13 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     a.g_dbg = nullptr;
     e = bmoe::launch_gemm2(a, &h->tm_w2, &h->tm_hq, g.NT, h->num_sms, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "GEMM2 launch");
+    h->launches += 1;
+    mark(4);
     e = bmoe::launch_combine(g, ws, topk_weights, T, num_valid_rows, static_cast<uint16_t*>(out), s);
     if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
+    h->launches += 1;
+    mark(5);
+    h->profiled = prof;
     h->forwarded = true;
     h->last_T = T;
     return MOE_OK;
@@ -353,6 +375,20 @@ int moe_set_option(moe_handle h, int key, double value) {
             if (!(value >= 0.0)) return fail(h, MOE_EINVAL, "swiglu limit must be >= 0");
             h->swiglu_limit = value;
             return MOE_OK;
+        case MOE_OPT_PROFILE: {
+            const int v = value != 0.0 ? 1 : 0;
+            if (v)
+                for (auto& ev : h->ev)
+                    if (!ev) {
+                        cudaError_t e = cudaEventCreate(&ev);
+                        if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventCreate");
+                    }
+            h->profile = v;
+            h->profiled = false;
+            return MOE_OK;
+        }
+        case MOE_OPT_LAUNCHES:
+            return fail(h, MOE_EINVAL, "option %d is read-only", key);
         case MOE_OPT_DISPATCH:
         case MOE_OPT_FIXED_SLOT_MAX:
         case MOE_OPT_DEBUG_CAPTURE:
@@ -405,6 +441,8 @@ int moe_get_option(moe_handle h, int key, double* value) {
         case MOE_OPT_FIXED_SLOT_MAX: *value = h->fixed_slot_max; return MOE_OK;
         case MOE_OPT_DEBUG_CAPTURE: *value = h->debug; return MOE_OK;
         case MOE_OPT_ROUTE_TILE: *value = h->geo.NT; return MOE_OK;
+        case MOE_OPT_PROFILE: *value = h->profile; return MOE_OK;
+        case MOE_OPT_LAUNCHES: *value = static_cast<double>(h->launches); return MOE_OK;
         default: return fail(h, MOE_EINVAL, "unknown option %d", key);
     }
 }
@@ -443,6 +481,18 @@ const char* moe_last_error(moe_handle h) {
 int moe_dispatch_scheme(moe_handle h) {
     if (!h) return MOE_EINVAL;
     return h->geo.scheme == 1 ? MOE_DISPATCH_FIXED : MOE_DISPATCH_COMPACT;
+}
+
+int moe_profile_read(moe_handle h, float* ms, int n) {
+    if (!h || !ms || n < 0) return MOE_EINVAL;
+    if (!h->profiled) return fail(h, MOE_ESTATE, "no profiled forward (set MOE_OPT_PROFILE before the forward)");
+    cudaError_t e = cudaEventSynchronize(h->ev[MOE_PROFILE_STAGES]);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventSynchronize");
+    for (int i = 0; i < MOE_PROFILE_STAGES && i < n; ++i) {
+        e = cudaEventElapsedTime(&ms[i], h->ev[i], h->ev[i + 1]);
+        if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventElapsedTime");
+    }
+    return MOE_OK;
 }
 
 int moe_debug_copy(moe_handle h, int which, void* host_dst, size_t* bytes, moe_stream_t stream) {

@@ -40,6 +40,9 @@ template <bool G1, int NT>
 struct Cfg {
     static constexpr int NA = G1 ? 2 : 1;                  // weight tiles per stage
     static constexpr int A_BYTES = 128 * 128;              // one weight tile in smem (1 byte per code)
+    // Transaction bytes of one 128x128 FP4 box: the TMA counts the packed bytes it
+    // reads (two codes per byte), not the 16-byte-aligned footprint it writes.
+    static constexpr int A_TX = 128 * 128 / 2;
     static constexpr int B_BYTES = NT * 128;               // row tile in smem
     static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES + (NA + 1) * 512;
     static constexpr int STAGES = (220 * 1024) / STAGE_BYTES > 12 ? 12 : (220 * 1024) / STAGE_BYTES;
@@ -176,11 +179,11 @@ __global__ void __launch_bounds__(192, 1)
                         cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, a, NT);
                         cu_ui = ui;
                     }
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, kStTimeout, kWaitLimitNs)) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
                         ok = false;
                     } else {
                         if (lane == 0) {
-                            mbar_expect_tx(&full[stage], NA * C::A_BYTES + C::B_BYTES + 512);
+                            mbar_expect_tx(&full[stage], NA * C::A_TX + C::B_BYTES + 512);
                             const int wrow = cu.e * a.w_rows + cu.m * 128;
                             tma_load_2d(sA + (stage * NA) * C::A_BYTES, &tm_w, &full[stage], kk * 128, wrow, pol_w);
                             if constexpr (G1)
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(192, 1)
                 } else {
                     --st;
                 }
-                (void)mbar_wait(&full[st], ph, &never, a.status, kStTimeout, kWaitLimitNs / 4);
+                (void)mbar_wait(&full[st], ph, &never, a.status, kStTimeout | (1u << (kSiteShift + 1)), kWaitLimitNs / 4);
             }
         }
     } else if (warp == 1) {
@@ -230,13 +233,13 @@ __global__ void __launch_bounds__(192, 1)
             const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, a, NT);
             const int N = (cu.n + 15) & ~15;
             const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * C::ACC_COLS);
-            if (!mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, a.status, kStTimeout, kWaitLimitNs)) {
+            if (!mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             for (int kk = 0; kk < KT; ++kk) {
-                if (!mbar_wait(&full[stage], phase, abort_flag, a.status, kStTimeout, kWaitLimitNs)) {
+                if (!mbar_wait(&full[stage], phase, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 3)), kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
@@ -280,7 +283,7 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
         {
             volatile int never = 0;
-            (void)mbar_wait(drain, 0, &never, a.status, kStTimeout, kWaitLimitNs);
+            (void)mbar_wait(drain, 0, &never, a.status, kStTimeout | (1u << (kSiteShift + 4)), kWaitLimitNs);
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -290,7 +293,7 @@ __global__ void __launch_bounds__(192, 1)
         const float L = a.swiglu_limit;
         for (int ui = 0; ui < my_units; ++ui) {
             const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, a, NT);
-            if (!mbar_wait(&accf[acc], acc_phase, abort_flag, a.status, kStTimeout, kWaitLimitNs)) break;
+            if (!mbar_wait(&accf[acc], acc_phase, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 5)), kWaitLimitNs)) break;
             tc_fence_after();
             const uint32_t tb = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * C::ACC_COLS);
             const int feat = cu.m * 128 + 32 * q + lane;

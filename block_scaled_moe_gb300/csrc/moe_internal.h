@@ -14,6 +14,10 @@ constexpr int kMaxTopk = 16;
 constexpr int kMaxExperts = 4096;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per device-side wait
 constexpr uint32_t kStBadId = 0x1u, kStTimeout = 0x2u, kStOverflow = 0x4u;
+// Wait sites recorded next to kStTimeout (bit 8 + site): 0 producer/empty,
+// 1 producer drain, 2 MMA/accumulator-free, 3 MMA/stage-full, 4 MMA drain,
+// 5 epilogue/accumulator-full.
+constexpr uint32_t kSiteShift = 8;
 
 // Device workspace, carved from one allocation.
 struct Workspace {

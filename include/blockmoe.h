@@ -62,6 +62,9 @@ typedef void* moe_stream_t;
 #define MOE_ST_BAD_ID 0x1u      /* a top-k id >= E was seen (skipped like -1) */
 #define MOE_ST_TIMEOUT 0x2u     /* a bounded device-side wait gave up */
 #define MOE_ST_OVERFLOW 0x4u    /* internal tile list overflow (bug guard) */
+/* With MOE_ST_TIMEOUT, bits 8..13 name the wait that gave up (diagnostic):
+ * 8 producer/stage-free, 9 producer drain, 10 MMA/accumulator-free,
+ * 11 MMA/stage-full, 12 MMA drain, 13 epilogue/accumulator-full. */
 
 /* ------------------------------------------------------------- options */
 #define MOE_OPT_DISPATCH 1        /* MOE_DISPATCH_* */
@@ -70,6 +73,9 @@ typedef void* moe_stream_t;
                                      (vLLM PR #61262: FIXED_SLOT_MAX_MTPR) */
 #define MOE_OPT_DEBUG_CAPTURE 4   /* 1 = also keep canonical MXFP8 codes of x and raw GEMM1 outputs */
 #define MOE_OPT_ROUTE_TILE 5      /* route-tile width NT in {0 (auto), 32, 128} */
+#define MOE_OPT_PROFILE 6         /* 1 = bracket each stage of every forward with CUDA events
+                                     (eager use only: keep 0 while capturing a CUDA graph) */
+#define MOE_OPT_LAUNCHES 7        /* read-only: CUDA kernels this handle has launched so far */
 
 #define MOE_DISPATCH_AUTO 0       /* fixed-slot iff capacity <= fixed-slot max */
 #define MOE_DISPATCH_FIXED 1
@@ -149,6 +155,14 @@ const char* moe_last_error(moe_handle h);
 
 /* Which dispatch scheme the handle runs: MOE_DISPATCH_FIXED or _COMPACT. */
 int moe_dispatch_scheme(moe_handle h);
+
+/* Stage times in milliseconds of the last forward run with MOE_OPT_PROFILE=1,
+ * measured by CUDA events recorded on the forward's stream:
+ *   ms[0] dispatch, ms[1] quantisation + scatter, ms[2] GEMM1, ms[3] GEMM2,
+ *   ms[4] combine.  Waits for the last event; n = entries ms can hold (<= 5
+ * written).  MOE_ESTATE if profiling is off or no profiled forward ran. */
+#define MOE_PROFILE_STAGES 5
+int moe_profile_read(moe_handle h, float* ms, int n);
 
 /* ------------------------------------------- test-only introspection
  * Copies one internal array of the last forward into host memory

@@ -84,6 +84,11 @@ WORKLOADS = {
     "skewed_flash": Workload("skewed_flash", T=4096, H=5120, I=2304, E=384, K=6, nvr=3500,
                              routing="hot_zipf", invalid_frac=0.0, swiglu_limit=10.0,
                              dispatch="compact", capacity=4096, hot_frac=0.25),
+    # Profiling stand-in for the decode workload: same H, I, top-k and clamp,
+    # 64 experts (1.2 GB of MXFP4 weights) so a full ncu capture stays small.
+    "decode_flash_e64": Workload("decode_flash_e64", T=32, H=5120, I=2304, E=64, K=6, nvr=32,
+                                 routing="uniform", invalid_frac=0.0, swiglu_limit=10.0,
+                                 dispatch="fixed", capacity=32),
 }
 
 
