@@ -78,6 +78,8 @@ def load(path: Optional[str] = None):
         lib.moe_debug_copy.restype = i32
         lib.moe_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32]
         lib.moe_profile_read.restype = i32
+        lib.moe_dispatch_compact_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        lib.moe_dispatch_compact_noalloc.restype = i32
         _lib = lib
         return lib
 
@@ -155,6 +157,13 @@ def moe_profile_read(h) -> list:
     ms = (ctypes.c_float * 5)()
     _check(h, load().moe_profile_read(h, ms, 5))
     return list(ms)
+
+
+def moe_dispatch_compact_noalloc(topk_ids: int, T: int, topk: int, E: int, num_valid_rows: Optional[int],
+                                 counts: int, offsets: int, perm: int, route_row: int, stream: int = 0):
+    """Compact dispatch without any device allocation (raw device pointers)."""
+    _check(None, load().moe_dispatch_compact_noalloc(topk_ids, T, topk, E, num_valid_rows, counts, offsets, perm,
+                                                     route_row, stream))
 
 
 def moe_debug_copy(h, which: int, stream: int = 0) -> bytes:

@@ -204,6 +204,8 @@ int check_device_ptr(moe_ctx* h, const void* p, const char* name, size_t align) 
 
 }  // namespace
 
+void bmoe::note_unbound_error(const char* msg) { g_create_err = msg; }
+
 extern "C" {
 
 int moe_create(moe_handle* out, int H, int I, int E, int topk, int capacity) {

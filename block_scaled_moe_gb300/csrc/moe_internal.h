@@ -96,4 +96,7 @@ cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUten
                          cudaStream_t s);
 cudaError_t gemm_set_attributes();
 
+// Error text of a failed call made without a handle (read by moe_last_error(NULL)).
+void note_unbound_error(const char* msg);
+
 }  // namespace bmoe

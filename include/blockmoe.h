@@ -149,8 +149,9 @@ int moe_set_workspace(moe_handle h, void* dev_ptr, size_t bytes);
  * `stream`; never called implicitly by moe_forward. */
 int moe_read_status(moe_handle h, uint32_t* flags, moe_stream_t stream);
 
-/* Text of the last error on this handle (or of the last failed moe_create
- * when h is NULL).  Valid until the next call on the same handle. */
+/* Text of the last error on this handle (or, when h is NULL, of the last
+ * failed call on this thread that had no handle: moe_create,
+ * moe_dispatch_compact_noalloc).  Valid until the next call on the same handle. */
 const char* moe_last_error(moe_handle h);
 
 /* Which dispatch scheme the handle runs: MOE_DISPATCH_FIXED or _COMPACT. */
@@ -163,6 +164,28 @@ int moe_dispatch_scheme(moe_handle h);
  * written).  MOE_ESTATE if profiling is off or no profiled forward ran. */
 #define MOE_PROFILE_STAGES 5
 int moe_profile_read(moe_handle h, float* ms, int n);
+
+/* ------------------------------------------- allocation-free dispatch
+ * The pages have no counterpart of this call; it serves callers that may not
+ * allocate device memory: code running while a CUDA graph is captured (where
+ * cudaMalloc is not allowed) and serving engines that reserve the whole GPU up
+ * front and forbid later allocations.  It runs the compact dispatch of
+ * moe_forward on its own, with the same results (counts, offsets = exclusive
+ * scan of counts with E+1 entries, perm, route_row; see MOE_DBG_* below for
+ * their layouts), and allocates nothing: its scratch is a 1 MiB array built
+ * into the library (every GPU that loads the library keeps it until the
+ * process exits), so it accepts only sizes with (ceil(T*topk/512) + 1) * E
+ * int32 values plus 256 bytes within 1 MiB, and refuses larger ones with
+ * MOE_ECAPACITY.  All calls share that array, so calls that overlap on the GPU
+ * (other streams, other threads) race and must be serialised by the caller.
+ * The first call on a device looks up the array's device address; make that
+ * first call before any stream capture.  Outputs: counts int32 [E],
+ * offsets int32 [E+1], perm int32 [T*topk] (first offsets[E] entries
+ * written), route_row int32 [T*topk]; all device memory of the caller.
+ * num_valid_rows as in moe_forward.  Errors: moe_last_error(NULL). */
+int moe_dispatch_compact_noalloc(const int32_t* topk_ids, int T, int topk, int E, const int32_t* num_valid_rows,
+                                 int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* route_row,
+                                 moe_stream_t stream);
 
 /* ------------------------------------------- test-only introspection
  * Copies one internal array of the last forward into host memory
