@@ -15,8 +15,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "lib", "libblockmoe.so")
 SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_gemm.cu", "moe_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
-                "--expt-relaxed-constexpr"]
+FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC,-Wall", "-I", INCLUDE, "-I", CSRC,
+                "--expt-relaxed-constexpr", "-Werror", "all-warnings"]
 
 
 def nvcc() -> str:

@@ -20,6 +20,12 @@
 using bmoe::Geometry;
 using bmoe::Workspace;
 
+#ifdef BMOE_TRACE
+extern "C" {
+long long* bmoe_trace_buffer = nullptr;  // device pointer of the pipeline trace (tracing builds)
+}
+#endif
+
 struct moe_ctx {
     int device = -1;
     int num_sms = 0;
@@ -329,6 +335,13 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     a.E = g.E;
     a.swiglu_limit = static_cast<float>(h->swiglu_limit);
     a.status = ws.status;
+    a.trace = nullptr;
+#ifdef BMOE_TRACE
+    static long long* trace_buf = nullptr;  // [2 GEMMs][2 CTAs][6][512] clock64 stamps
+    if (!trace_buf) cudaMalloc(&trace_buf, sizeof(long long) * 2 * 2 * 6 * 512);
+    a.trace = trace_buf;
+    bmoe_trace_buffer = trace_buf;
+#endif
     a.I = g.I;
     a.H = g.H;
     // GEMM1: W13 (gate/up pairs) x dispatched rows, K = H
@@ -343,6 +356,9 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     a.hs = ws.hs;
     a.g_dbg = g.debug ? ws.g : nullptr;
     e = bmoe::launch_gemm1(a, &h->tm_w13, &h->tm_aq, g.NT, h->num_sms, s);
+#ifdef BMOE_TRACE
+    a.trace = trace_buf + 2 * 6 * 512;
+#endif
     if (e != cudaSuccess) return cuda_fail(h, e, "GEMM1 launch");
     h->launches += 1;
     mark(3);

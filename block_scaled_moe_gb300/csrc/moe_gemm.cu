@@ -17,15 +17,20 @@
 //     Epilogue: BF16 rows y (aiter #6881: GEMM2 rows go to the combine as BF16).
 //
 // Pipeline per CTA (persistent, one CTA per SM, units strided over the grid):
-//   warp 0     producer: TMA of the FP4 weight tile (16U4_ALIGN16B expands each
-//              16 codes to 16 bytes in shared memory, the layout kind::mxf8f6f4
-//              reads), TMA of the FP8 row tile, bulk copy of the rows' scale
-//              atom, and the weight scales gathered from their natural
-//              [rows, K/32] layout into a 128x4 scale atom by the warp's lanes.
-//   warp 1     MMA issuer: tcgen05.cp of the scale atoms into TMEM, 4 MMAs of
-//              K=32 per 128-wide K stage (scale byte k of each TMEM word).
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator (lane = output feature,
-//              column = routed row), math, global stores.
+//   warp 0      producer: TMA of the FP4 weight tile (16U4_ALIGN16B expands each
+//               16 codes to 16 bytes in shared memory, the layout kind::mxf8f6f4
+//               reads), TMA of the FP8 row tile, bulk copy of the rows' scale
+//               atom, and the weight scales gathered from their natural
+//               [rows, K/32] layout into a 128x4 scale atom by the warp's lanes
+//               with 4-byte cp.async (no register staging).
+//   warps 1..MW MMA issuers.  One thread can issue a tcgen05.mma only every
+//               ~170 cycles whatever N is, so small-N decode MMAs are issue
+//               bound; MW warps each own an accumulator chain (gate or up, and
+//               a residue class of the K-steps) and issue in parallel.  Each
+//               copies the stage's scale atoms into its own TMEM columns.
+//   next 4 warps epilogue: tcgen05.ld of the MW partial accumulators (lane =
+//               output feature, column = routed row), their fixed-order sum,
+//               then the SwiGLU/MXFP8 or BF16 epilogue and global stores.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -45,47 +50,81 @@ struct Cfg {
     static constexpr int A_TX = 128 * 128 / 2;
     static constexpr int B_BYTES = NT * 128;               // row tile in smem
     static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES + (NA + 1) * 512;
-    static constexpr int STAGES = (220 * 1024) / STAGE_BYTES > 12 ? 12 : (220 * 1024) / STAGE_BYTES;
-    static constexpr int ACC_COLS = G1 ? 2 * NT : NT;
-    static constexpr int NUM_ACC = (2 * ACC_COLS <= 256) ? 2 : 1;
-    static constexpr int SF_COL0 = 256;
-    static constexpr int SF_COLS = 4 * (NA + 1);           // TMEM columns of scales per stage
+    static constexpr int TAB_E = 512;                      // experts whose plan fits the smem tables
+    static constexpr int TAB_BYTES = 4 * (3 * TAB_E + 4);
+    static constexpr int STAGES = (220 * 1024 - TAB_BYTES) / STAGE_BYTES > 12 ? 12
+                                                                             : (220 * 1024 - TAB_BYTES) / STAGE_BYTES;
+    // MMA issuers and their accumulator chains
+    static constexpr int MW = NT <= 64 ? 4 : 2;            // accumulator chains
+    static constexpr int NI = MW;                          // MMA-issuing warps (chain w is issued by warp w % NI)
+    static constexpr int KS = G1 ? MW / 2 : MW;            // K-steps of a stage split over KS chains per operand
+    static constexpr int ACC_COLS = MW * NT;               // one accumulator set: MW chains of NT columns
+    static constexpr int SF_SLOTS = 2;                     // scale slots per chain (alternating stages)
+    static constexpr int SF_BASE = 512 - MW * SF_SLOTS * 8;
+    static constexpr int NUM_ACC = (2 * ACC_COLS <= SF_BASE) ? 2 : 1;
+    static constexpr int THREADS = 32 * (1 + NI + 4);
+    static constexpr int EPI_WARP0 = 1 + NI;
     static constexpr int BAR_BYTES = (2 * STAGES + 2 * 2 + 1) * 8 + 16;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
-    static_assert(SF_COL0 + STAGES * SF_COLS <= 512, "TMEM columns");
-    static_assert(NUM_ACC * ACC_COLS <= SF_COL0, "TMEM accumulators");
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + TAB_BYTES + BAR_BYTES;
+    static_assert(NUM_ACC * ACC_COLS <= SF_BASE, "TMEM columns");
     static_assert(SMEM <= 232448, "shared memory");
+    static_assert(4 % KS == 0, "K-steps per stage must split evenly");
 };
+
+// Pipeline tracing (compiled in with -DBMOE_TRACE): clock64 stamps of the first
+// kTraceJobs K stages of CTAs 0 and 1, per role, into GemmArgs::trace
+// ([2 CTAs][6 events][kTraceJobs] int64): 0 producer got a free stage, 1 producer
+// issued it, 2 first MMA warp saw it full, 3 that warp issued its MMAs; per
+// unit: 4 epilogue saw the accumulator, 5 epilogue released it.
+__device__ __forceinline__ void trace(const GemmArgs& a, int ev, long idx) {
+#ifdef BMOE_TRACE
+    constexpr int kTraceJobs = 512;
+    if (a.trace && blockIdx.x < 2 && idx < kTraceJobs)
+        a.trace[(static_cast<long>(blockIdx.x) * 6 + ev) * kTraceJobs + idx] = clock64();
+#else
+    (void)a;
+    (void)ev;
+    (void)idx;
+#endif
+}
 
 struct UnitInfo {
     int e, m, g, row0, n;
+};
+
+// Routing plan as read by the GEMM roles: shared-memory copies when E fits the
+// tables, else the global arrays.
+struct Plan {
+    const int32_t* tile_base;  // [E+1]
+    const int32_t* rowbase;    // [E+1]
+    const int32_t* counts;     // [E]
 };
 
 // Unit u of the global list: experts ascending; inside an expert, weight tile m
 // major and route tile j minor, so CTAs running consecutive units share a
 // weight tile (L2 reuse when an expert has several route tiles).  `ecur` only
 // moves forward because every role walks its units in increasing order.
-__device__ __forceinline__ UnitInfo decode_unit(int u, int& ecur, const GemmArgs& a, int NT) {
-    const int q = u / a.mtiles;
-    while (__ldg(a.tile_base + ecur + 1) <= q) ++ecur;
-    const int tb = __ldg(a.tile_base + ecur);
-    const int nt = __ldg(a.tile_base + ecur + 1) - tb;
-    const int ul = u - tb * a.mtiles;
+__device__ __forceinline__ UnitInfo decode_unit(int u, int& ecur, const Plan& pl, int mtiles, int NT) {
+    const int q = u / mtiles;
+    while (pl.tile_base[ecur + 1] <= q) ++ecur;
+    const int tb = pl.tile_base[ecur];
+    const int nt = pl.tile_base[ecur + 1] - tb;
+    const int ul = u - tb * mtiles;
     UnitInfo r;
     r.e = ecur;
     r.m = ul / nt;
     const int j = ul - r.m * nt;
     r.g = tb + j;
-    r.row0 = __ldg(a.rowbase + ecur) + j * NT;
-    r.n = min(NT, __ldg(a.counts + ecur) - j * NT);
+    r.row0 = pl.rowbase[ecur] + j * NT;
+    r.n = min(NT, pl.counts[ecur] - j * NT);
     return r;
 }
 
 template <bool G1, int NT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(Cfg<G1, NT>::THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b, const GemmArgs a) {
     using C = Cfg<G1, NT>;
-    constexpr int STAGES = C::STAGES, NA = C::NA;
+    constexpr int STAGES = C::STAGES, NA = C::NA, MW = C::MW, KS = C::KS, NI = C::NI;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = sm;
@@ -99,6 +138,7 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* drain = acce + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int32_t* tab = reinterpret_cast<int32_t*>(sSFB + STAGES * 512 + C::BAR_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntiles = __ldg(a.tile_base + a.E);
@@ -107,16 +147,25 @@ __global__ void __launch_bounds__(192, 1)
     const int my_units = (n_units - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1;
     const int KT = a.ktiles;
 
+    Plan pl{a.tile_base, a.rowbase, a.counts};
+    if (a.E <= C::TAB_E) {
+        for (int i = threadIdx.x; i <= a.E; i += blockDim.x) {
+            tab[i] = __ldg(a.tile_base + i);
+            tab[C::TAB_E + 1 + i] = __ldg(a.rowbase + i);
+            if (i < a.E) tab[2 * C::TAB_E + 2 + i] = __ldg(a.counts + i);
+        }
+        pl = Plan{tab, tab + C::TAB_E + 1, tab + 2 * C::TAB_E + 2};
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 32);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], NI);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&accf[b], 1);
+            mbar_init(&accf[b], NI);
             mbar_init(&acce[b], 128);
         }
-        mbar_init(drain, 1);
+        mbar_init(drain, NI);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -137,74 +186,51 @@ __global__ void __launch_bounds__(192, 1)
             prefetch_tmap(&tm_w);
             prefetch_tmap(&tm_b);
         }
-        const long njobs = static_cast<long>(my_units) * KT;
-        constexpr int D = 4;  // weight-scale prefetch distance, in stages
-        uint32_t sfr[D][4 * NA];
-        int pf_ecur = 0, pf_ui = -1;
-        UnitInfo pfu{};
-        auto load_sf = [&](long J, uint32_t(&dst)[4 * NA]) {
-            if (J >= njobs) return;
-            const int ui = static_cast<int>(J / KT), kk = static_cast<int>(J % KT);
-            if (ui != pf_ui) {
-                pfu = decode_unit(blockIdx.x + ui * gridDim.x, pf_ecur, a, NT);
-                pf_ui = ui;
-            }
-            const uint8_t* base =
-                a.w_sf + (static_cast<size_t>(pfu.e) * a.w_rows + pfu.m * 128 + lane) * a.ld_sf + kk * 4;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                dst[i] = __ldg(reinterpret_cast<const uint32_t*>(base + static_cast<size_t>(32 * i) * a.ld_sf));
-            if constexpr (G1) {
-                const uint8_t* b2 = base + static_cast<size_t>(a.up_off) * a.ld_sf;
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dst[4 + i] = __ldg(reinterpret_cast<const uint32_t*>(b2 + static_cast<size_t>(32 * i) * a.ld_sf));
-            }
-        };
-#pragma unroll
-        for (int d = 0; d < D; ++d) load_sf(d, sfr[d]);
-        int stage = 0;
+        int stage = 0, ecur = 0;
         uint32_t phase = 0;
-        int ecur = 0, cu_ui = -1;
-        UnitInfo cu{};
-        bool ok = true;
         long issued = 0;
-        for (long J0 = 0; J0 < njobs && ok; J0 += D) {
+        bool ok = true;
+        for (int ui = 0; ui < my_units && ok; ++ui) {
+            const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
+            const int wrow = cu.e * a.w_rows + cu.m * 128;
+            const uint8_t* sf_src = a.w_sf + (static_cast<size_t>(wrow) + lane) * a.ld_sf;
+            const uint8_t* b_sf = a.b_sf + static_cast<size_t>(cu.g) * KT * 512;
+            for (int kk = 0; kk < KT; ++kk) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
+                               kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    trace(a, 0, issued);
+                    mbar_expect_tx(&full[stage], NA * C::A_TX + C::B_BYTES + 512);
+                    tma_load_2d(sA + (stage * NA) * C::A_BYTES, &tm_w, &full[stage], kk * 128, wrow, pol_w);
+                    if constexpr (G1)
+                        tma_load_2d(sA + (stage * NA + 1) * C::A_BYTES, &tm_w, &full[stage], kk * 128,
+                                    wrow + a.up_off, pol_w);
+                    tma_load_2d(sB + stage * C::B_BYTES, &tm_b, &full[stage], kk * 128, cu.row0, pol_b);
+                    bulk_load(sSFB + stage * 512, b_sf + kk * 512, 512, &full[stage]);
+                }
+                // Weight scales: the 4 K-blocks of this stage for rows lane, lane+32, lane+64,
+                // lane+96 form line `lane` of the 128x4 scale atom (bytes 16*lane + 4*i).
+                {
+                    uint8_t* dst = sSFA + stage * NA * 512 + 16 * lane;
+                    const uint8_t* src = sf_src + kk * 4;
 #pragma unroll
-            for (int d = 0; d < D; ++d) {
-                const long J = J0 + d;
-                if (J < njobs && ok) {
-                    const int ui = static_cast<int>(J / KT), kk = static_cast<int>(J % KT);
-                    if (ui != cu_ui) {
-                        cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, a, NT);
-                        cu_ui = ui;
+                    for (int i = 0; i < 4; ++i) cp_async4(dst + 4 * i, src + static_cast<size_t>(32 * i) * a.ld_sf);
+                    if constexpr (G1) {
+                        const uint8_t* src2 = src + static_cast<size_t>(a.up_off) * a.ld_sf;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            cp_async4(dst + 512 + 4 * i, src2 + static_cast<size_t>(32 * i) * a.ld_sf);
                     }
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
-                        ok = false;
-                    } else {
-                        if (lane == 0) {
-                            mbar_expect_tx(&full[stage], NA * C::A_TX + C::B_BYTES + 512);
-                            const int wrow = cu.e * a.w_rows + cu.m * 128;
-                            tma_load_2d(sA + (stage * NA) * C::A_BYTES, &tm_w, &full[stage], kk * 128, wrow, pol_w);
-                            if constexpr (G1)
-                                tma_load_2d(sA + (stage * NA + 1) * C::A_BYTES, &tm_w, &full[stage], kk * 128,
-                                            wrow + a.up_off, pol_w);
-                            tma_load_2d(sB + stage * C::B_BYTES, &tm_b, &full[stage], kk * 128, cu.row0, pol_b);
-                            bulk_load(sSFB + stage * 512, a.b_sf + (static_cast<size_t>(cu.g) * KT + kk) * 512, 512,
-                                      &full[stage]);
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(sSFA + stage * NA * 512) + lane;
-                        dst[0] = make_uint4(sfr[d][0], sfr[d][1], sfr[d][2], sfr[d][3]);
-                        if constexpr (G1) dst[32] = make_uint4(sfr[d][4], sfr[d][5], sfr[d][6], sfr[d][7]);
-                        fence_proxy_async_smem();
-                        mbar_arrive(&full[stage]);
-                        ++issued;
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
-                    load_sf(J + D, sfr[d]);
+                }
+                cp_async_mbar_arrive(&full[stage]);
+                if (lane == 0) trace(a, 1, issued);
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
         }
@@ -221,48 +247,63 @@ __global__ void __launch_bounds__(192, 1)
                 } else {
                     --st;
                 }
-                (void)mbar_wait(&full[st], ph, &never, a.status, kStTimeout | (1u << (kSiteShift + 1)), kWaitLimitNs / 4);
+                (void)mbar_wait(&full[st], ph, &never, a.status, kStTimeout | (1u << (kSiteShift + 1)),
+                                kWaitLimitNs / 4);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp <= NI) {
+        // ------------------------------------------------------------ MMA issuers
+        const int wi = warp - 1;           // this warp issues chains wi, wi + NI, ...
         int stage = 0, acc = 0, ecur = 0;
         uint32_t phase = 0, acc_phase = 0;
+        long job = 0;
         bool ok = true;
         for (int ui = 0; ui < my_units && ok; ++ui) {
-            const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, a, NT);
+            const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
             const int N = (cu.n + 15) & ~15;
-            const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * C::ACC_COLS);
-            if (!mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs)) {
+            if (!mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 2)),
+                           kWaitLimitNs)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             for (int kk = 0; kk < KT; ++kk) {
-                if (!mbar_wait(&full[stage], phase, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 3)), kWaitLimitNs)) {
+                if (!mbar_wait(&full[stage], phase, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 3)),
+                               kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t sfc = tmem + static_cast<uint32_t>(C::SF_COL0 + stage * C::SF_COLS);
-                    tc_cp_32x128b_x4(sfc, desc_sf_atom(smem_u32(sSFA + stage * NA * 512)));
-                    if constexpr (G1) tc_cp_32x128b_x4(sfc + 4, desc_sf_atom(smem_u32(sSFA + stage * NA * 512 + 512)));
-                    tc_cp_32x128b_x4(sfc + 4 * NA, desc_sf_atom(smem_u32(sSFB + stage * 512)));
-                    const uint64_t da0 = desc_kmajor_sw128(smem_u32(sA + (stage * NA) * C::A_BYTES));
-                    const uint64_t da1 = desc_kmajor_sw128(smem_u32(sA + (stage * NA + NA - 1) * C::A_BYTES));
+                    if (wi == 0) trace(a, 2, job);
+                    // the weight-scale atoms were written by cp.async (generic proxy); tcgen05.cp
+                    // reads them through the async proxy
+                    fence_proxy_async_smem();
                     const uint64_t db = desc_kmajor_sw128(smem_u32(sB + stage * C::B_BYTES));
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t idesc = idesc_mx(128, N, 5, 0, k, k);
-                        const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);
-                        const uint32_t accum = (kk | k) != 0 ? 1u : 0u;
-                        tc_mma_mx(d_tmem, da0 + koff, db + koff, idesc, sfc, sfc + 4 * NA, accum);
-                        if constexpr (G1) tc_mma_mx(d_tmem + NT, da1 + koff, db + koff, idesc, sfc + 4, sfc + 4 * NA, accum);
+                    for (int w = wi; w < MW; w += NI) {
+                        const int op = G1 ? (w & 1) : 0;   // GEMM1: 0 gate, 1 up
+                        const int kq = G1 ? (w >> 1) : w;  // chain w takes the K-steps k with k % KS == kq
+                        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * C::ACC_COLS + w * NT);
+                        const uint32_t sfc =
+                            tmem + static_cast<uint32_t>(C::SF_BASE + (w * C::SF_SLOTS + (job & 1)) * 8);
+                        tc_cp_32x128b_x4(sfc, desc_sf_atom(smem_u32(sSFA + (stage * NA + op) * 512)));
+                        tc_cp_32x128b_x4(sfc + 4, desc_sf_atom(smem_u32(sSFB + stage * 512)));
+                        const uint64_t da = desc_kmajor_sw128(smem_u32(sA + (stage * NA + op) * C::A_BYTES));
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            if (k % KS != kq) continue;
+                            const uint32_t idesc = idesc_mx(128, N, 5, 0, k, k);
+                            const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);
+                            tc_mma_mx(d_tmem, da + koff, db + koff, idesc, sfc, sfc + 4,
+                                      (kk > 0 || k != kq) ? 1u : 0u);
+                        }
                     }
                     tc_commit(&empty[stage]);
+                    if (wi == 0) trace(a, 3, job);
                 }
                 __syncwarp();
+                ++job;
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -291,24 +332,45 @@ __global__ void __launch_bounds__(192, 1)
         int acc = 0, ecur = 0;
         uint32_t acc_phase = 0;
         const float L = a.swiglu_limit;
+        const bool tracer = warp == C::EPI_WARP0 && lane == 0;
         for (int ui = 0; ui < my_units; ++ui) {
-            const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, a, NT);
-            if (!mbar_wait(&accf[acc], acc_phase, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 5)), kWaitLimitNs)) break;
+            const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
+            if (!mbar_wait(&accf[acc], acc_phase, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 5)),
+                           kWaitLimitNs))
+                break;
             tc_fence_after();
-            const uint32_t tb = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * C::ACC_COLS);
+            if (tracer) trace(a, 4, ui);
+            const uint32_t tb =
+                tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * C::ACC_COLS);
             const int feat = cu.m * 128 + 32 * q + lane;
             for (int c0 = 0; c0 < cu.n; c0 += 16) {
-                uint32_t ra[16], rb[16];
-                tmem_ld16(tb + c0, ra);
-                if constexpr (G1) tmem_ld16(tb + NT + c0, rb);
+                // partial accumulators of the MW chains, summed in a fixed order
+                uint32_t r[MW][16];
+#pragma unroll
+                for (int w = 0; w < MW; ++w) tmem_ld16(tb + w * NT + c0, r[w]);
                 tmem_ld_wait();
+                float va[16], vb[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    va[i] = 0.f;
+                    vb[i] = 0.f;
+                }
+#pragma unroll
+                for (int w = 0; w < MW; ++w)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (G1 && (w & 1))
+                            vb[i] += __uint_as_float(r[w][i]);
+                        else
+                            va[i] += __uint_as_float(r[w][i]);
+                    }
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int c = c0 + i;
                     if (c < cu.n) {
                         const size_t prow = static_cast<size_t>(cu.row0 + c);
                         if constexpr (G1) {
-                            float ga = __uint_as_float(ra[i]), ub = __uint_as_float(rb[i]);
+                            float ga = va[i], ub = vb[i];
                             if (a.g_dbg) {
                                 a.g_dbg[prow * 2 * a.I + feat] = ga;
                                 a.g_dbg[prow * 2 * a.I + a.I + feat] = ub;
@@ -327,13 +389,13 @@ __global__ void __launch_bounds__(192, 1)
                                 a.hs[(static_cast<size_t>(cu.g) * (a.I >> 7) + cu.m) * 512 + 16 * (c & 31) +
                                      4 * (c >> 5) + q] = static_cast<uint8_t>(code);
                         } else {
-                            a.y[prow * a.H + feat] =
-                                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(ra[i])));
+                            a.y[prow * a.H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(va[i]));
                         }
                     }
                 }
             }
             tc_fence_before();
+            if (tracer) trace(a, 5, ui);
             mbar_arrive(&acce[acc]);
             if (C::NUM_ACC == 2) {
                 acc ^= 1;
@@ -359,7 +421,7 @@ cudaError_t set_attr() {
 
 template <bool G1, int NT>
 cudaError_t launch(const GemmArgs& a, const CUtensorMap* tw, const CUtensorMap* tb, int grid, cudaStream_t s) {
-    k_gemm<G1, NT><<<grid, 192, Cfg<G1, NT>::SMEM, s>>>(*tw, *tb, a);
+    k_gemm<G1, NT><<<grid, Cfg<G1, NT>::THREADS, Cfg<G1, NT>::SMEM, s>>>(*tw, *tb, a);
     return cudaGetLastError();
 }
 

@@ -88,6 +88,7 @@ struct GemmArgs {
     uint16_t* y;  int H;                    // GEMM2
     float swiglu_limit;
     uint32_t* status;
+    long long* trace;      // pipeline trace buffer (tracing builds only), else null
 };
 
 cudaError_t launch_gemm1(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_x, int NT, int grid,
