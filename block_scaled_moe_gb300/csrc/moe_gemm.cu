@@ -17,20 +17,23 @@
 //     Epilogue: BF16 rows y (aiter #6881: GEMM2 rows go to the combine as BF16).
 //
 // Pipeline per CTA (persistent, one CTA per SM, units strided over the grid):
-//   warp 0      producer: TMA of the FP4 weight tile (16U4_ALIGN16B expands each
-//               16 codes to 16 bytes in shared memory, the layout kind::mxf8f6f4
-//               reads), TMA of the FP8 row tile, bulk copy of the rows' scale
-//               atom, and the weight scales gathered from their natural
-//               [rows, K/32] layout into a 128x4 scale atom by the warp's lanes
-//               with 4-byte cp.async (no register staging).
-//   warps 1..MW MMA issuers.  One thread can issue a tcgen05.mma only every
+//   warp 0      TMA producer (one thread): TMA of the FP4 weight tile
+//               (16U4_ALIGN16B expands each 16 codes to 16 bytes in shared
+//               memory, the layout kind::mxf8f6f4 reads), TMA of the FP8 row
+//               tile and bulk copy of the rows' scale atom.
+//   warp 1      scale producer: the weight scales gathered from their natural
+//               [rows, K/32] layout into a 128x4 scale atom by the warp's 32
+//               lanes, loaded 8 stages ahead into registers and stored with a
+//               proxy fence before the stage's arrival.
+//   warps 2..   MMA issuers.  One thread can issue a tcgen05.mma only every
 //               ~170 cycles whatever N is, so small-N decode MMAs are issue
 //               bound; MW warps each own an accumulator chain (gate or up, and
 //               a residue class of the K-steps) and issue in parallel.  Each
 //               copies the stage's scale atoms into its own TMEM columns.
-//   next 4 warps epilogue: tcgen05.ld of the MW partial accumulators (lane =
-//               output feature, column = routed row), their fixed-order sum,
-//               then the SwiGLU/MXFP8 or BF16 epilogue and global stores.
+//   last EW     epilogue warps: tcgen05.ld of the MW partial accumulators (lane =
+//               output feature, column = routed row) and their fixed-order sum
+//               into registers, release of the accumulator, then the
+//               SwiGLU/MXFP8 or BF16 epilogue and global stores.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -41,34 +44,43 @@ namespace bmoe {
 
 namespace {
 
-template <bool G1, int NT>
+template <bool G1, int NT, int KC>
 struct Cfg {
-    static constexpr int NA = G1 ? 2 : 1;                  // weight tiles per stage
-    static constexpr int A_BYTES = 128 * 128;              // one weight tile in smem (1 byte per code)
+    // A K stage is KC chunks of 128 K-elements (one 128-byte swizzle atom each).
+    static constexpr int NA = G1 ? 2 : 1;                  // weight operands per stage (gate/up or W2)
+    static constexpr int A_BYTES = 128 * 128;              // one 128x128 weight chunk in smem (1 byte per code)
     // Transaction bytes of one 128x128 FP4 box: the TMA counts the packed bytes it
     // reads (two codes per byte), not the 16-byte-aligned footprint it writes.
     static constexpr int A_TX = 128 * 128 / 2;
-    static constexpr int B_BYTES = NT * 128;               // row tile in smem
-    static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES + (NA + 1) * 512;
+    static constexpr int B_BYTES = NT * 128;               // one row chunk in smem
+    static constexpr int STAGE_BYTES = KC * (NA * A_BYTES + B_BYTES + (NA + 1) * 512);
     static constexpr int TAB_E = 512;                      // experts whose plan fits the smem tables
     static constexpr int TAB_BYTES = 4 * (3 * TAB_E + 4);
     static constexpr int STAGES = (220 * 1024 - TAB_BYTES) / STAGE_BYTES > 12 ? 12
                                                                              : (220 * 1024 - TAB_BYTES) / STAGE_BYTES;
-    // MMA issuers and their accumulator chains
-    static constexpr int MW = NT <= 64 ? 4 : 2;            // accumulator chains
+    // MMA issuers and their accumulator chains: 4 for the decode tile width (issue
+    // bound); for 128-wide tiles GEMM1 keeps its gate/up pair and GEMM2 one chain,
+    // so that GEMM2's accumulator can be double-buffered in TMEM.
+    static constexpr int MW = NT <= 64 ? 4 : (G1 ? 2 : 1);
     static constexpr int NI = MW;                          // MMA-issuing warps (chain w is issued by warp w % NI)
     static constexpr int KS = G1 ? MW / 2 : MW;            // K-steps of a stage split over KS chains per operand
+    static constexpr int EW = NT <= 64 ? 4 : 8;            // epilogue warps (EW/4 per TMEM lane quadrant)
+    static constexpr int CW = NT / (EW / 4);               // accumulator columns per epilogue warp
     static constexpr int ACC_COLS = MW * NT;               // one accumulator set: MW chains of NT columns
     static constexpr int SF_SLOTS = 2;                     // scale slots per chain (alternating stages)
-    static constexpr int SF_BASE = 512 - MW * SF_SLOTS * 8;
+    static constexpr int SF_SLOT_COLS = 8 * KC;            // KC weight atoms then KC row atoms, 4 columns each
+    static constexpr int SF_BASE = 512 - MW * SF_SLOTS * SF_SLOT_COLS;
     static constexpr int NUM_ACC = (2 * ACC_COLS <= SF_BASE) ? 2 : 1;
-    static constexpr int THREADS = 32 * (1 + NI + 4);
-    static constexpr int EPI_WARP0 = 1 + NI;
+    // warps: 0 TMA producer, 1 scale producer, 2..1+NI MMA issuers, then EW epilogue warps
+    static constexpr int MMA_WARP0 = 2;
+    static constexpr int EPI_WARP0 = 2 + NI;
+    static constexpr int THREADS = 32 * (2 + NI + EW);
     static constexpr int BAR_BYTES = (2 * STAGES + 2 * 2 + 1) * 8 + 16;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + TAB_BYTES + BAR_BYTES;
     static_assert(NUM_ACC * ACC_COLS <= SF_BASE, "TMEM columns");
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(4 % KS == 0, "K-steps per stage must split evenly");
+    static_assert(CW % 16 == 0, "epilogue column split");
 };
 
 // Pipeline tracing (compiled in with -DBMOE_TRACE): clock64 stamps of the first
@@ -120,32 +132,51 @@ __device__ __forceinline__ UnitInfo decode_unit(int u, int& ecur, const Plan& pl
     return r;
 }
 
-template <bool G1, int NT>
-__global__ void __launch_bounds__(Cfg<G1, NT>::THREADS, 1)
+// The loads of the last STAGES jobs this producer issued land before the CTA
+// exits (they are consumed already unless another role gave up).  Bounded.
+template <int STAGES>
+__device__ __forceinline__ void drain_stages(uint64_t* full, int stage, uint32_t phase, long issued,
+                                             uint32_t* status) {
+    volatile int never = 0;
+    for (long i = 0; i < STAGES && i < issued; ++i) {
+        if (stage == 0) {
+            stage = STAGES - 1;
+            phase ^= 1u;
+        } else {
+            --stage;
+        }
+        (void)mbar_wait(&full[stage], phase, &never, status, kStTimeout | (1u << (kSiteShift + 1)),
+                        kWaitLimitNs / 4);
+    }
+}
+
+template <bool G1, int NT, int KC>
+__global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b, const GemmArgs a) {
-    using C = Cfg<G1, NT>;
+    using C = Cfg<G1, NT, KC>;
     constexpr int STAGES = C::STAGES, NA = C::NA, MW = C::MW, KS = C::KS, NI = C::NI;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = sm;
-    uint8_t* sB = sA + STAGES * NA * C::A_BYTES;
-    uint8_t* sSFA = sB + STAGES * C::B_BYTES;
-    uint8_t* sSFB = sSFA + STAGES * NA * 512;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * 512);
+    // per stage: sA [NA][KC] chunks, sB [KC] chunks, sSFA [NA][KC] atoms, sSFB [KC] atoms
+    uint8_t* sB = sA + STAGES * NA * KC * C::A_BYTES;
+    uint8_t* sSFA = sB + STAGES * KC * C::B_BYTES;
+    uint8_t* sSFB = sSFA + STAGES * NA * KC * 512;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * KC * 512);
     uint64_t* empty = full + STAGES;
     uint64_t* accf = empty + STAGES;
     uint64_t* acce = accf + 2;
     uint64_t* drain = acce + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int32_t* tab = reinterpret_cast<int32_t*>(sSFB + STAGES * 512 + C::BAR_BYTES);
+    int32_t* tab = reinterpret_cast<int32_t*>(sSFB + STAGES * KC * 512 + C::BAR_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntiles = __ldg(a.tile_base + a.E);
     const int n_units = ntiles * a.mtiles;
     if (static_cast<int>(blockIdx.x) >= n_units) return;  // whole CTA
     const int my_units = (n_units - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1;
-    const int KT = a.ktiles;
+    const int KT = a.ktiles / KC;  // K stages per unit
 
     Plan pl{a.tile_base, a.rowbase, a.counts};
     if (a.E <= C::TAB_E) {
@@ -158,18 +189,18 @@ __global__ void __launch_bounds__(Cfg<G1, NT>::THREADS, 1)
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 32);
+            mbar_init(&full[s], 1 + 32);  // TMA issuer + the 32 scale-copying lanes
             mbar_init(&empty[s], NI);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf[b], NI);
-            mbar_init(&acce[b], 128);
+            mbar_init(&acce[b], 32 * C::EW);
         }
         mbar_init(drain, NI);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == C::MMA_WARP0) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
@@ -179,81 +210,118 @@ __global__ void __launch_bounds__(Cfg<G1, NT>::THREADS, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        const uint64_t pol_w = policy_evict_first();
-        const uint64_t pol_b = policy_evict_last();
+        // ------------------------------------------------------------ TMA producer (one thread)
         if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_b = policy_evict_last();
             prefetch_tmap(&tm_w);
             prefetch_tmap(&tm_b);
-        }
-        int stage = 0, ecur = 0;
-        uint32_t phase = 0;
-        long issued = 0;
-        bool ok = true;
-        for (int ui = 0; ui < my_units && ok; ++ui) {
-            const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
-            const int wrow = cu.e * a.w_rows + cu.m * 128;
-            const uint8_t* sf_src = a.w_sf + (static_cast<size_t>(wrow) + lane) * a.ld_sf;
-            const uint8_t* b_sf = a.b_sf + static_cast<size_t>(cu.g) * KT * 512;
-            for (int kk = 0; kk < KT; ++kk) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
-                               kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
+            int stage = 0, ecur = 0;
+            uint32_t phase = 0;
+            long issued = 0;
+            bool ok = true;
+            for (int ui = 0; ui < my_units && ok; ++ui) {
+                const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
+                const int wrow = cu.e * a.w_rows + cu.m * 128;
+                const uint8_t* b_sf = a.b_sf + static_cast<size_t>(cu.g) * a.ktiles * 512;
+                for (int kk = 0; kk < KT; ++kk) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
+                                   kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
                     trace(a, 0, issued);
-                    mbar_expect_tx(&full[stage], NA * C::A_TX + C::B_BYTES + 512);
-                    tma_load_2d(sA + (stage * NA) * C::A_BYTES, &tm_w, &full[stage], kk * 128, wrow, pol_w);
-                    if constexpr (G1)
-                        tma_load_2d(sA + (stage * NA + 1) * C::A_BYTES, &tm_w, &full[stage], kk * 128,
-                                    wrow + a.up_off, pol_w);
-                    tma_load_2d(sB + stage * C::B_BYTES, &tm_b, &full[stage], kk * 128, cu.row0, pol_b);
-                    bulk_load(sSFB + stage * 512, b_sf + kk * 512, 512, &full[stage]);
-                }
-                // Weight scales: the 4 K-blocks of this stage for rows lane, lane+32, lane+64,
-                // lane+96 form line `lane` of the 128x4 scale atom (bytes 16*lane + 4*i).
-                {
-                    uint8_t* dst = sSFA + stage * NA * 512 + 16 * lane;
-                    const uint8_t* src = sf_src + kk * 4;
+                    mbar_expect_tx(&full[stage], KC * (NA * C::A_TX + C::B_BYTES + 512));
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) cp_async4(dst + 4 * i, src + static_cast<size_t>(32 * i) * a.ld_sf);
-                    if constexpr (G1) {
-                        const uint8_t* src2 = src + static_cast<size_t>(a.up_off) * a.ld_sf;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            cp_async4(dst + 512 + 4 * i, src2 + static_cast<size_t>(32 * i) * a.ld_sf);
+                    for (int c = 0; c < KC; ++c) {
+                        const int k0 = (kk * KC + c) * 128;
+                        tma_load_2d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0, wrow, pol_w);
+                        if constexpr (G1)
+                            tma_load_2d(sA + ((stage * NA + 1) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0,
+                                        wrow + a.up_off, pol_w);
+                        tma_load_2d(sB + (stage * KC + c) * C::B_BYTES, &tm_b, &full[stage], k0, cu.row0, pol_b);
+                    }
+                    bulk_load(sSFB + stage * KC * 512, b_sf + kk * KC * 512, KC * 512, &full[stage]);
+                    mbar_arrive(&full[stage]);
+                    trace(a, 1, issued);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
                 }
-                cp_async_mbar_arrive(&full[stage]);
-                if (lane == 0) trace(a, 1, issued);
-                ++issued;
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+            }
+            drain_stages<STAGES>(full, stage, phase, issued, a.status);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ weight-scale producer (32 lanes)
+        // Lane l gathers the 4 K-blocks of the stage for rows l, l+32, l+64, l+96 (one
+        // 32-bit word each) and writes them as line l of the 128x4 scale atom.  The
+        // words are loaded SD stages ahead of their stage into registers so that
+        // their latency stays off this warp's path; the stores are made visible to
+        // the tensor core's async proxy here, before the warp arrives on the stage.
+        constexpr int SD = 8;
+        constexpr int NW = 4 * NA * KC;  // words per lane per stage: [op][chunk][row group]
+        uint32_t ring[SD][NW];
+        int p_ui = 0, p_kk = 0, p_ecur = 0;  // load cursor (SD stages ahead)
+        const uint8_t* p_src = nullptr;
+        auto load_next = [&](uint32_t(&dst)[NW]) {
+            if (p_ui >= my_units) return;
+            if (p_kk == 0) {
+                const UnitInfo pu = decode_unit(blockIdx.x + p_ui * gridDim.x, p_ecur, pl, a.mtiles, NT);
+                p_src = a.w_sf + (static_cast<size_t>(pu.e) * a.w_rows + pu.m * 128 + lane) * a.ld_sf;
+            }
+#pragma unroll
+            for (int op = 0; op < NA; ++op)
+#pragma unroll
+                for (int c = 0; c < KC; ++c) {
+                    const uint8_t* src = p_src + static_cast<size_t>(op * a.up_off) * a.ld_sf + (p_kk * KC + c) * 4;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[(op * KC + c) * 4 + i] =
+                            __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(32 * i) * a.ld_sf));
+                }
+            if (++p_kk == KT) {
+                p_kk = 0;
+                ++p_ui;
+            }
+        };
+#pragma unroll
+        for (int d = 0; d < SD; ++d) load_next(ring[d]);
+        const long njobs = static_cast<long>(my_units) * KT;
+        int stage = 0;
+        uint32_t phase = 0;
+        long issued = 0;
+        for (long J0 = 0; J0 < njobs; J0 += SD) {
+            bool ok = true;
+#pragma unroll
+            for (int d = 0; d < SD; ++d) {
+                if (J0 + d < njobs && ok) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
+                                   kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
+                        ok = false;
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(sSFA + stage * NA * KC * 512) + lane;
+#pragma unroll
+                        for (int a4 = 0; a4 < NA * KC; ++a4)  // atom (op, chunk) is 32 uint4 further
+                            dst[32 * a4] = make_uint4(ring[d][4 * a4], ring[d][4 * a4 + 1], ring[d][4 * a4 + 2],
+                                                      ring[d][4 * a4 + 3]);
+                        fence_proxy_async_smem();
+                        mbar_arrive(&full[stage]);
+                        ++issued;
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        load_next(ring[d]);
+                    }
                 }
             }
+            if (!ok) break;
         }
-        // Drain: the loads of the last STAGES issued jobs land before the CTA exits
-        // (they are consumed already unless another role gave up).
-        {
-            volatile int never = 0;
-            int st = stage;
-            uint32_t ph = phase;
-            for (long i = 0; i < STAGES && i < issued; ++i) {
-                if (st == 0) {
-                    st = STAGES - 1;
-                    ph ^= 1u;
-                } else {
-                    --st;
-                }
-                (void)mbar_wait(&full[st], ph, &never, a.status, kStTimeout | (1u << (kSiteShift + 1)),
-                                kWaitLimitNs / 4);
-            }
-        }
-    } else if (warp <= NI) {
+    } else if (warp < C::EPI_WARP0) {
         // ------------------------------------------------------------ MMA issuers
-        const int wi = warp - 1;           // this warp issues chains wi, wi + NI, ...
+        const int wi = warp - C::MMA_WARP0;  // this warp issues chains wi, wi + NI, ...
         int stage = 0, acc = 0, ecur = 0;
         uint32_t phase = 0, acc_phase = 0;
         long job = 0;
@@ -276,26 +344,30 @@ __global__ void __launch_bounds__(Cfg<G1, NT>::THREADS, 1)
                 tc_fence_after();
                 if (lane == 0) {
                     if (wi == 0) trace(a, 2, job);
-                    // the weight-scale atoms were written by cp.async (generic proxy); tcgen05.cp
-                    // reads them through the async proxy
-                    fence_proxy_async_smem();
-                    const uint64_t db = desc_kmajor_sw128(smem_u32(sB + stage * C::B_BYTES));
 #pragma unroll
                     for (int w = wi; w < MW; w += NI) {
                         const int op = G1 ? (w & 1) : 0;   // GEMM1: 0 gate, 1 up
                         const int kq = G1 ? (w >> 1) : w;  // chain w takes the K-steps k with k % KS == kq
                         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * C::ACC_COLS + w * NT);
-                        const uint32_t sfc =
-                            tmem + static_cast<uint32_t>(C::SF_BASE + (w * C::SF_SLOTS + (job & 1)) * 8);
-                        tc_cp_32x128b_x4(sfc, desc_sf_atom(smem_u32(sSFA + (stage * NA + op) * 512)));
-                        tc_cp_32x128b_x4(sfc + 4, desc_sf_atom(smem_u32(sSFB + stage * 512)));
-                        const uint64_t da = desc_kmajor_sw128(smem_u32(sA + (stage * NA + op) * C::A_BYTES));
+                        const uint32_t sfc = tmem + static_cast<uint32_t>(
+                                                        C::SF_BASE + (w * C::SF_SLOTS + (job & 1)) * C::SF_SLOT_COLS);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
+                        for (int c = 0; c < KC; ++c) {
+                            tc_cp_32x128b_x4(sfc + 4 * c,
+                                             desc_sf_atom(smem_u32(sSFA + ((stage * NA + op) * KC + c) * 512)));
+                            tc_cp_32x128b_x4(sfc + 4 * KC + 4 * c, desc_sf_atom(smem_u32(sSFB + (stage * KC + c) * 512)));
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4 * KC; ++k) {
                             if (k % KS != kq) continue;
-                            const uint32_t idesc = idesc_mx(128, N, 5, 0, k, k);
-                            const uint64_t koff = static_cast<uint64_t>((k * 32) >> 4);
-                            tc_mma_mx(d_tmem, da + koff, db + koff, idesc, sfc, sfc + 4,
+                            const int c = k >> 2, k4 = k & 3;
+                            const uint64_t da =
+                                desc_kmajor_sw128(smem_u32(sA + ((stage * NA + op) * KC + c) * C::A_BYTES)) +
+                                static_cast<uint64_t>((k4 * 32) >> 4);
+                            const uint64_t db = desc_kmajor_sw128(smem_u32(sB + (stage * KC + c) * C::B_BYTES)) +
+                                                static_cast<uint64_t>((k4 * 32) >> 4);
+                            const uint32_t idesc = idesc_mx(128, N, 5, 0, k4, k4);
+                            tc_mma_mx(d_tmem, da, db, idesc, sfc + 4 * c, sfc + 4 * KC + 4 * c,
                                       (kk > 0 || k != kq) ? 1u : 0u);
                         }
                     }
@@ -328,7 +400,12 @@ __global__ void __launch_bounds__(Cfg<G1, NT>::THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        // Each warp drains CW columns of its TMEM lane quadrant into registers
+        // (summing the MW chains in a fixed order), releases the accumulator so
+        // the next unit's MMAs can start, then finishes the columns from registers.
+        constexpr int CW = C::CW;
+        const int q = warp & 3;                              // TMEM lane quadrant this warp may access
+        const int cbase = ((warp - C::EPI_WARP0) >> 2) * CW;  // first column of this warp
         int acc = 0, ecur = 0;
         uint32_t acc_phase = 0;
         const float L = a.swiglu_limit;
@@ -343,35 +420,28 @@ __global__ void __launch_bounds__(Cfg<G1, NT>::THREADS, 1)
             const uint32_t tb =
                 tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * C::ACC_COLS);
             const int feat = cu.m * 128 + 32 * q + lane;
-            for (int c0 = 0; c0 < cu.n; c0 += 16) {
-                // partial accumulators of the MW chains, summed in a fixed order
-                uint32_t r[MW][16];
+            float v[CW];  // GEMM1: h = SwiGLU(gate, up); GEMM2: y
 #pragma unroll
-                for (int w = 0; w < MW; ++w) tmem_ld16(tb + w * NT + c0, r[w]);
-                tmem_ld_wait();
-                float va[16], vb[16];
+            for (int j = 0; j < CW / 16; ++j) {
+                const int c0 = cbase + 16 * j;
+                if (c0 < cu.n) {
+                    uint32_t r[MW][16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    va[i] = 0.f;
-                    vb[i] = 0.f;
-                }
-#pragma unroll
-                for (int w = 0; w < MW; ++w)
+                    for (int w = 0; w < MW; ++w) tmem_ld16(tb + w * NT + c0, r[w]);
+                    tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        if (G1 && (w & 1))
-                            vb[i] += __uint_as_float(r[w][i]);
-                        else
-                            va[i] += __uint_as_float(r[w][i]);
-                    }
+                        float ga = 0.f, ub = 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int c = c0 + i;
-                    if (c < cu.n) {
-                        const size_t prow = static_cast<size_t>(cu.row0 + c);
+                        for (int w = 0; w < MW; ++w) {
+                            if (G1 && (w & 1))
+                                ub += __uint_as_float(r[w][i]);
+                            else
+                                ga += __uint_as_float(r[w][i]);
+                        }
                         if constexpr (G1) {
-                            float ga = va[i], ub = vb[i];
-                            if (a.g_dbg) {
+                            if (a.g_dbg && c0 + i < cu.n) {
+                                const size_t prow = static_cast<size_t>(cu.row0 + c0 + i);
                                 a.g_dbg[prow * 2 * a.I + feat] = ga;
                                 a.g_dbg[prow * 2 * a.I + a.I + feat] = ub;
                             }
@@ -379,17 +449,9 @@ __global__ void __launch_bounds__(Cfg<G1, NT>::THREADS, 1)
                                 ga = fminf(ga, L);
                                 ub = fminf(fmaxf(ub, -L), L);
                             }
-                            const float h = ga * (1.0f / (1.0f + expf(-ga))) * ub;
-                            const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
-                            int code = static_cast<int>(amax >> 23) - 8;
-                            code = code < 0 ? 0 : code;
-                            const float mul = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
-                            a.hq[prow * a.I + feat] = __nv_cvt_float_to_fp8(h * mul, __NV_SATFINITE, __NV_E4M3);
-                            if (lane == 0)
-                                a.hs[(static_cast<size_t>(cu.g) * (a.I >> 7) + cu.m) * 512 + 16 * (c & 31) +
-                                     4 * (c >> 5) + q] = static_cast<uint8_t>(code);
+                            v[16 * j + i] = ga * (1.0f / (1.0f + expf(-ga))) * ub;
                         } else {
-                            a.y[prow * a.H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(va[i]));
+                            v[16 * j + i] = ga;
                         }
                     }
                 }
@@ -403,25 +465,46 @@ __global__ void __launch_bounds__(Cfg<G1, NT>::THREADS, 1)
             } else {
                 acc_phase ^= 1u;
             }
+#pragma unroll
+            for (int j = 0; j < CW; ++j) {
+                const int c = cbase + j;
+                if (c < cu.n) {
+                    const size_t prow = static_cast<size_t>(cu.row0 + c);
+                    if constexpr (G1) {
+                        const float h = v[j];
+                        const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
+                        int code = static_cast<int>(amax >> 23) - 8;
+                        code = code < 0 ? 0 : code;
+                        const float mul = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
+                        a.hq[prow * a.I + feat] = __nv_cvt_float_to_fp8(h * mul, __NV_SATFINITE, __NV_E4M3);
+                        if (lane == 0)
+                            a.hs[(static_cast<size_t>(cu.g) * (a.I >> 7) + cu.m) * 512 + 16 * (c & 31) +
+                                 4 * (c >> 5) + q] = static_cast<uint8_t>(code);
+                    } else {
+                        a.y[prow * a.H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+                    }
+                }
+            }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == C::MMA_WARP0) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
 }
 
-template <bool G1, int NT>
+template <bool G1, int NT, int KC>
 cudaError_t set_attr() {
-    return cudaFuncSetAttribute(k_gemm<G1, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<G1, NT>::SMEM);
+    return cudaFuncSetAttribute(k_gemm<G1, NT, KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<G1, NT, KC>::SMEM);
 }
 
-template <bool G1, int NT>
+template <bool G1, int NT, int KC>
 cudaError_t launch(const GemmArgs& a, const CUtensorMap* tw, const CUtensorMap* tb, int grid, cudaStream_t s) {
-    k_gemm<G1, NT><<<grid, Cfg<G1, NT>::THREADS, Cfg<G1, NT>::SMEM, s>>>(*tw, *tb, a);
+    k_gemm<G1, NT, KC><<<grid, Cfg<G1, NT, KC>::THREADS, Cfg<G1, NT, KC>::SMEM, s>>>(*tw, *tb, a);
     return cudaGetLastError();
 }
 
@@ -429,20 +512,24 @@ cudaError_t launch(const GemmArgs& a, const CUtensorMap* tw, const CUtensorMap* 
 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
-    if ((e = set_attr<true, 128>()) != cudaSuccess) return e;
-    if ((e = set_attr<true, 32>()) != cudaSuccess) return e;
-    if ((e = set_attr<false, 128>()) != cudaSuccess) return e;
-    return set_attr<false, 32>();
+    if ((e = set_attr<true, 128, 1>()) != cudaSuccess) return e;
+    if ((e = set_attr<true, 32, 1>()) != cudaSuccess) return e;
+    if ((e = set_attr<false, 128, 1>()) != cudaSuccess) return e;
+    if ((e = set_attr<false, 32, 1>()) != cudaSuccess) return e;
+    return set_attr<false, 32, 2>();
 }
 
 cudaError_t launch_gemm1(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_x, int NT, int grid,
                          cudaStream_t s) {
-    return NT == 32 ? launch<true, 32>(a, tm_w, tm_x, grid, s) : launch<true, 128>(a, tm_w, tm_x, grid, s);
+    return NT == 32 ? launch<true, 32, 1>(a, tm_w, tm_x, grid, s) : launch<true, 128, 1>(a, tm_w, tm_x, grid, s);
 }
 
 cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_h, int NT, int grid,
                          cudaStream_t s) {
-    return NT == 32 ? launch<false, 32>(a, tm_w, tm_h, grid, s) : launch<false, 128>(a, tm_w, tm_h, grid, s);
+    // decode tiles stream W2 in 256-wide K stages when I allows it (halves the per-stage cost per byte)
+    if (NT == 32) return a.ktiles % 2 == 0 ? launch<false, 32, 2>(a, tm_w, tm_h, grid, s)
+                                           : launch<false, 32, 1>(a, tm_w, tm_h, grid, s);
+    return launch<false, 128, 1>(a, tm_w, tm_h, grid, s);
 }
 
 }  // namespace bmoe
