@@ -8,9 +8,10 @@ H=5120, I=2304, 384 experts, top-6, MTPR 128, clamp-10 SwiGLU).
 Prints one JSON line.  `value` is MoE-layer tokens/s with inputs resident in
 HBM; `e2e` is the same metric through the public API with host buffers (H2D of
 the step's inputs and D2H of its output inside the timed region); `roofline`
-reports GEMM1 (the dominant kernel: it streams 2/3 of the active-expert
-weight bytes) against the measured HBM copy bandwidth; `cpu_baseline` times
-the CPU oracle on a bounded sample of the same workload.
+reports the dominant kernel against the measured HBM copy bandwidth: the
+single-launch fused kernel (the whole layer) when the forward takes that path,
+as decode does, else GEMM1 (it streams 2/3 of the active-expert weight bytes);
+`cpu_baseline` times the CPU oracle on a bounded sample of the same workload.
 
 --impl reference times the CPU oracle itself on the same workload (bounded
 row sample per step) and prints the same line with "impl": "reference".
@@ -46,6 +47,8 @@ def parse():
     p.add_argument("--workload", default="decode_flash")
     p.add_argument("--cpu-rows", type=int, default=16, help="oracle sample rows for the CPU baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--path", default="auto", choices=["auto", "fused", "multi"],
+                   help="layer path (auto: the fused kernel where the handle allows it)")
     return p.parse_args()
 
 
@@ -130,22 +133,29 @@ def workload_bytes_flops(w, ids):
             "gemm1": w13 + gemm1_act, "flops": flops}
 
 
-def source_sha():
+# source files of each kernel whose ncu traffic figure is committed under profiles/
+KERNEL_SOURCES = {
+    "gemm1": ("moe_gemm.cu", "gemm_common.cuh", "ptx.cuh"),
+    "fused": ("moe_fused.cu", "gemm_common.cuh", "layer_rows.cuh", "ptx.cuh"),
+}
+
+
+def source_sha(kernel):
     h = hashlib.sha256()
-    for f in ("moe_gemm.cu", "ptx.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "block_scaled_moe_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def traffic_for(workload, ntiles_key):
-    """dram bytes of GEMM1 per launch from a committed ncu summary, if the kernel is unchanged."""
-    path = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
+def traffic_for(kernel, workload):
+    """dram bytes per launch of `kernel` from a committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(workload)
-        if e and e.get("source_sha") == source_sha():
+        if e and e.get("source_sha") == source_sha(kernel):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -224,7 +234,8 @@ def main():
     x = synth.make_x(w)
     ids, wts = synth.make_routing(w)
     W = synth.make_weights(w, dev)
-    layer = bm.BlockScaledMoE(w.H, w.I, w.E, w.K, w.capacity, dispatch=w.dispatch, swiglu_limit=w.swiglu_limit)
+    layer = bm.BlockScaledMoE(w.H, w.I, w.E, w.K, w.capacity, dispatch=w.dispatch, swiglu_limit=w.swiglu_limit,
+                              path=args.path)
     layer.bind_weights(*W)
     xd = x.to(dev)
     idsd = torch.from_numpy(ids).to(dev)
@@ -311,12 +322,16 @@ def main():
         e2e_ms = float(t.item())
     e2e_value = tokens / (e2e_ms / 1e3)
 
-    # ---- roofline of GEMM1 from its live CUDA-event durations
+    # ---- roofline of the dominant kernel from its live CUDA-event durations (stage slot 2 holds GEMM1, or
+    # the whole fused kernel on the single-launch path)
     wb = workload_bytes_flops(w, ids)
-    g1_ms = statistics.mean(s[2] for s in stage_ms)
+    fused = layer.last_path == "fused"
+    kern = "fused" if fused else "gemm1"
+    k_ms = statistics.mean(s[2] for s in stage_ms)
     hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = peaks()
-    achieved = wb["gemm1"] / (g1_ms / 1e3) / 1e9
-    traffic = traffic_for(w.name, None)
+    k_bytes = wb["step"] if fused else wb["gemm1"]
+    achieved = k_bytes / (k_ms / 1e3) / 1e9
+    traffic = traffic_for(kern, w.name)
     step_gbs = wb["step"] / (total_ms / args.steps / world / 1e3) / 1e9
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -325,18 +340,22 @@ def main():
             "data": "synthetic",
             "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "topk": w.K,
                        "num_valid_rows": w.nvr, "dispatch": layer.scheme, "capacity": w.capacity,
+                       "path": layer.last_path,
                        "swiglu_limit": w.swiglu_limit, "routes": wb["routes"], "active_experts": wb["active"],
                        "l2": "512 MiB buffer written between timed steps (outside the events)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "roofline": {"kernel": "GEMM1 (tcgen05 block-scaled, W13 stream + SwiGLU/MXFP8 epilogue)",
+            "roofline": {"kernel": ("fused layer (one cooperative launch: dispatch, MXFP8 quant, tcgen05 GEMM1 + "
+                                    "SwiGLU/MXFP8, tcgen05 GEMM2, combine)") if fused else
+                                   "GEMM1 (tcgen05 block-scaled, W13 stream + SwiGLU/MXFP8 epilogue)",
                          "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": achieved / hbm_gbs, "traffic": traffic, "peak_source": peak_src,
-                         "algorithmic_bytes_per_launch": wb["gemm1"], "launch_ms": g1_ms},
+                         "algorithmic_bytes_per_launch": k_bytes, "launch_ms": k_ms},
             "step_roofline": {"bytes_per_step": wb["step"], "achieved_gbs": step_gbs,
                               "frac_of_hbm": step_gbs / hbm_gbs,
                               "tflops": wb["flops"] / (total_ms / args.steps / world / 1e3) / 1e12,
                               "stage_ms_mean": [statistics.mean(s[i] for s in stage_ms) for i in range(5)],
-                              "stages": ["dispatch", "quant+scatter", "gemm1", "gemm2", "combine"]},
+                              "stages": (["-", "-", "fused kernel", "-", "-"] if fused else
+                                         ["dispatch", "quant+scatter", "gemm1", "gemm2", "combine"])},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches * world,
             "clocks": clk.summary()}

@@ -78,6 +78,8 @@ def load(path: Optional[str] = None):
         lib.moe_debug_copy.restype = i32
         lib.moe_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32]
         lib.moe_profile_read.restype = i32
+        lib.moe_last_path.argtypes = [vp]
+        lib.moe_last_path.restype = i32
         lib.moe_dispatch_compact_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         lib.moe_dispatch_compact_noalloc.restype = i32
         _lib = lib
@@ -182,7 +184,7 @@ class BlockScaledMoE:
 
     def __init__(self, H: int, I: int, E: int, topk: int, capacity: int, *, dispatch: Optional[str] = None,
                  swiglu_limit: float = 0.0, route_tile: int = 0, debug: bool = False,
-                 fixed_slot_max: Optional[int] = None, workspace=None):
+                 fixed_slot_max: Optional[int] = None, workspace=None, path: Optional[str] = None):
         self.H, self.I, self.E, self.topk, self.capacity = H, I, E, topk, capacity
         self.h = moe_create(H, I, E, topk, capacity)
         try:
@@ -197,6 +199,9 @@ class BlockScaledMoE:
             if debug:
                 moe_set_option(self.h, MOE_OPT_DEBUG_CAPTURE, 1)
             moe_set_option(self.h, MOE_OPT_SWIGLU_LIMIT, swiglu_limit)
+            if path is not None:
+                moe_set_option(self.h, MOE_OPT_PATH, {"auto": MOE_PATH_AUTO, "fused": MOE_PATH_FUSED,
+                                                      "multi": MOE_PATH_MULTI}[path])
             if workspace is not None:
                 moe_set_workspace(self.h, workspace.data_ptr(), workspace.numel() * workspace.element_size())
         except Exception:
@@ -223,6 +228,10 @@ class BlockScaledMoE:
     @property
     def workspace_bytes(self) -> int:
         return moe_workspace_bytes(self.h)
+
+    @property
+    def last_path(self) -> str:
+        return {MOE_PATH_FUSED: "fused", MOE_PATH_MULTI: "multi"}.get(load().moe_last_path(self.h), "none")
 
     @property
     def launches(self) -> int:

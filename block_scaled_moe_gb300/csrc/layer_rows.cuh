@@ -1,0 +1,185 @@
+// layer_rows.cuh -- per-row device code shared by the stand-alone kernels
+// (moe_kernels.cu) and the single-launch fused kernel (moe_fused.cu): MXFP8
+// quantisation of one token row fused with its scatter into the experts' packed
+// rows, and the top-k weighted combine of one output row.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "moe_internal.h"
+
+namespace bmoe {
+namespace rows {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ int read_nvr(const int32_t* p, int T) {
+    int v = p ? __ldg(p) : T;
+    return v < 0 ? 0 : (v > T ? T : v);
+}
+
+__device__ __forceinline__ uint32_t pack_fp8x4(float a, float b, float c, float d) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+struct QuantArgs {
+    const uint16_t* x;
+    const int32_t* ids;
+    int T, K, E, H, mtpr, words, NT, scheme;
+    Workspace ws;
+};
+
+// One warp quantises token row t to MXFP8 (E4M3 codes, one E8M0 scale per 32
+// along H, OCP MX rule: code = max(exponent(amax) - 8, 0), element =
+// RNE_satfinite(x * 2^(127-code))) and writes the codes once per valid slot into
+// the expert's packed rows, the scale into the route tile's 128x4 scale atom
+// (byte 16*(c%32) + 4*(c/32) + kblock%4 for row c of the tile); it also records
+// the packed row each slot combines (yrow, -1 for an invalid slot).
+// `rowbase` / `tile_base` may point to global or shared memory.  Routing data
+// written earlier by other CTAs is read with L2-coherent loads.
+__device__ __forceinline__ void quant_scatter_row(const QuantArgs& a, const int32_t* rowbase,
+                                                  const int32_t* tile_base, int t, int nvr, int lane) {
+    const int K = a.K;
+    int p = -1, gt = 0, c = 0;
+    bool valid = false;
+    if (lane < K) {
+        const int e = a.ids[(size_t)t * K + lane];
+        if (t < nvr && e >= a.E) atomicOr(a.ws.status, kStBadId);
+        valid = t < nvr && e >= 0 && e < a.E;
+        if (valid) {
+            int i;
+            if (a.scheme == 1) {
+                const uint32_t* wb = a.ws.occ + (size_t)e * a.words;
+                i = 0;
+                for (int w = 0; w < (t >> 5); ++w) i += __popc(__ldcg(wb + w));
+                i += __popc(__ldcg(wb + (t >> 5)) & ((1u << (t & 31)) - 1u));
+                p = e * a.mtpr + i;
+            } else {
+                p = __ldcg(a.ws.route_row + (size_t)t * K + lane);
+                i = p - rowbase[e];
+            }
+            gt = tile_base[e] + i / a.NT;
+            c = i % a.NT;
+        }
+        a.ws.yrow[(size_t)t * K + lane] = valid ? p : -1;
+    }
+    if (t >= nvr) return;  // warp-uniform
+    const unsigned vmask = __ballot_sync(kFull, valid);
+    int pk[kMaxTopk], gk[kMaxTopk], ck[kMaxTopk];
+#pragma unroll
+    for (int k = 0; k < kMaxTopk; ++k) {
+        pk[k] = __shfl_sync(kFull, p, k);
+        gk[k] = __shfl_sync(kFull, gt, k);
+        ck[k] = __shfl_sync(kFull, c, k);
+    }
+    const int H = a.H, nblk = H >> 5, ktiles = H >> 7;
+    const uint16_t* xrow = a.x + (size_t)t * H;
+    for (int blk = lane; blk < nblk; blk += 32) {
+        const uint4* src = reinterpret_cast<const uint4*>(xrow + blk * 32);
+        float f[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = __ldg(src + q);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[q * 8 + 2 * j] = __uint_as_float(w[j] << 16);
+                f[q * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+            }
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        int code = static_cast<int>(__float_as_uint(amax) >> 23) - 8;
+        code = code < 0 ? 0 : code;
+        const float mul = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            o[j] = pack_fp8x4(f[4 * j] * mul, f[4 * j + 1] * mul, f[4 * j + 2] * mul, f[4 * j + 3] * mul);
+        const uint4 o0 = make_uint4(o[0], o[1], o[2], o[3]), o1 = make_uint4(o[4], o[5], o[6], o[7]);
+        if (a.ws.xq) {
+            uint4* d = reinterpret_cast<uint4*>(a.ws.xq + (size_t)t * H + blk * 32);
+            d[0] = o0;
+            d[1] = o1;
+            a.ws.xs[(size_t)t * nblk + blk] = static_cast<uint8_t>(code);
+        }
+#pragma unroll
+        for (int k = 0; k < kMaxTopk; ++k) {
+            if (k < K && ((vmask >> k) & 1u)) {
+                uint4* d = reinterpret_cast<uint4*>(a.ws.aq + (size_t)pk[k] * H + blk * 32);
+                d[0] = o0;
+                d[1] = o1;
+                const int ci = ck[k];
+                a.ws.as[((size_t)gk[k] * ktiles + (blk >> 2)) * 512 + 16 * (ci & 31) + 4 * (ci >> 5) + (blk & 3)] =
+                    static_cast<uint8_t>(code);
+            }
+        }
+    }
+}
+
+// out[t] = BF16( sum over valid slots, k ascending, of w[t,k] * y[row(t,k)] ),
+// float accumulation rounded once (ROCm/ATOM PR #2725: the MoE sum "in f32 and
+// rounds once"); -1 slots are skipped (ROCm/aiter PR #6881: "its combine skips
+// invalid (-1) top-k slots"); rows with no valid slot are +0.  One warp per
+// row, 16-byte vectors; y is read with L2-coherent loads (the fused kernel
+// combines rows other CTAs wrote in the same launch).
+struct CombineArgs {
+    const uint16_t* y;
+    const int32_t* yrow;
+    const float* w;
+    uint16_t* out;
+    int T, K, H;
+};
+
+__device__ __forceinline__ void combine_row(const CombineArgs& a, int t, int lane) {
+    int r_l = -1;
+    float w_l = 0.f;
+    if (lane < a.K) {
+        r_l = __ldcg(a.yrow + (size_t)t * a.K + lane);
+        w_l = a.w[(size_t)t * a.K + lane];
+    }
+    int rows[kMaxTopk];
+    float wk[kMaxTopk];
+#pragma unroll
+    for (int k = 0; k < kMaxTopk; ++k) {
+        rows[k] = __shfl_sync(kFull, r_l, k);
+        wk[k] = __shfl_sync(kFull, w_l, k);
+    }
+    const int nv = a.H >> 3;
+    for (int v = lane; v < nv; v += 32) {
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+        bool any = false;
+#pragma unroll
+        for (int k = 0; k < kMaxTopk; ++k) {
+            if (k >= a.K || rows[k] < 0) continue;
+            any = true;
+            const uint4 q = __ldcg(reinterpret_cast<const uint4*>(a.y + (size_t)rows[k] * a.H) + v);
+            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+            const float wv = wk[k];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[2 * j] = __fadd_rn(acc[2 * j], __fmul_rn(wv, __uint_as_float(w4[j] << 16)));
+                acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __fmul_rn(wv, __uint_as_float(w4[j] & 0xffff0000u)));
+            }
+        }
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (any) {
+            uint32_t ow[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+                ow[j] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+        reinterpret_cast<uint4*>(a.out + (size_t)t * a.H)[v] = o;
+    }
+}
+
+}  // namespace rows
+}  // namespace bmoe

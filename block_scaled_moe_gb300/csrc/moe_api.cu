@@ -49,6 +49,9 @@ struct moe_ctx {
     int last_T = 0;
     int profile = 0;
     bool profiled = false;
+    int opt_path = MOE_PATH_AUTO;
+    int last_path = 0;
+    bool coop = false;  // device supports cooperative launches
     cudaEvent_t ev[MOE_PROFILE_STAGES + 1] = {};
     unsigned long long launches = 0;
     std::string err;
@@ -233,11 +236,15 @@ int moe_create(moe_handle* out, int H, int I, int E, int topk, int capacity) {
         return fail(nullptr, MOE_EDEVICE, "device %d is sm_%d%d; this library is built for sm_103a (GB300)", dev,
                     prop.major, prop.minor);
     e = bmoe::gemm_set_attributes();
+    if (e == cudaSuccess) e = bmoe::fused_set_attributes();
     if (e != cudaSuccess) return fail(nullptr, MOE_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    int coop = 0;
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
     moe_ctx* h = new (std::nothrow) moe_ctx();
     if (!h) return fail(nullptr, MOE_ENOMEM, "host allocation failed");
     h->device = dev;
     h->num_sms = prop.multiProcessorCount;
+    h->coop = coop != 0;
     h->geo.H = H;
     h->geo.I = I;
     h->geo.E = E;
@@ -313,6 +320,33 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
         if (prof) cudaEventRecord(h->ev[i], s);
     };
     mark(0);
+    const bool fused = h->opt_path != MOE_PATH_MULTI && h->coop && bmoe::fused_supported(g) &&
+                       (h->opt_path == MOE_PATH_FUSED || T <= 512);
+    if (fused) {
+        bmoe::FusedLaunch fl;
+        fl.x = static_cast<const uint16_t*>(x);
+        fl.ids = topk_ids;
+        fl.wts = topk_weights;
+        fl.nvr = num_valid_rows;
+        fl.out = static_cast<uint16_t*>(out);
+        fl.w13s = h->w13s;
+        fl.w2s = h->w2s;
+        fl.swiglu_limit = static_cast<float>(h->swiglu_limit);
+        fl.T = T;
+        mark(1);
+        mark(2);
+        e = bmoe::launch_fused(g, ws, fl, &h->tm_w13, &h->tm_aq, &h->tm_w2, &h->tm_hq, h->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(h, e, "fused launch");
+        h->launches += 1;
+        mark(3);
+        mark(4);
+        mark(5);
+        h->profiled = prof;
+        h->forwarded = true;
+        h->last_T = T;
+        h->last_path = MOE_PATH_FUSED;
+        return MOE_OK;
+    }
     if (g.scheme == 1) {
         e = cudaMemsetAsync(ws.occ, 0, sizeof(uint32_t) * (size_t)g.E * g.words, s);
         if (e != cudaSuccess) return cuda_fail(h, e, "clearing occupancy");
@@ -383,6 +417,7 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     h->profiled = prof;
     h->forwarded = true;
     h->last_T = T;
+    h->last_path = MOE_PATH_MULTI;
     return MOE_OK;
 }
 
@@ -407,6 +442,16 @@ int moe_set_option(moe_handle h, int key, double value) {
         }
         case MOE_OPT_LAUNCHES:
             return fail(h, MOE_EINVAL, "option %d is read-only", key);
+        case MOE_OPT_PATH: {
+            const int v = static_cast<int>(value);
+            if (static_cast<double>(v) != value || v < MOE_PATH_AUTO || v > MOE_PATH_MULTI)
+                return fail(h, MOE_EINVAL, "bad path %g", value);
+            if (v == MOE_PATH_FUSED && !(h->coop && bmoe::fused_supported(h->geo)))
+                return fail(h, MOE_EINVAL, "the fused path needs capacity <= 512, route tile 32, E <= 512 and a "
+                                           "cooperative-launch device");
+            h->opt_path = v;
+            return MOE_OK;
+        }
         case MOE_OPT_DISPATCH:
         case MOE_OPT_FIXED_SLOT_MAX:
         case MOE_OPT_DEBUG_CAPTURE:
@@ -461,6 +506,7 @@ int moe_get_option(moe_handle h, int key, double* value) {
         case MOE_OPT_ROUTE_TILE: *value = h->geo.NT; return MOE_OK;
         case MOE_OPT_PROFILE: *value = h->profile; return MOE_OK;
         case MOE_OPT_LAUNCHES: *value = static_cast<double>(h->launches); return MOE_OK;
+        case MOE_OPT_PATH: *value = h->opt_path; return MOE_OK;
         default: return fail(h, MOE_EINVAL, "unknown option %d", key);
     }
 }
@@ -487,6 +533,8 @@ int moe_read_status(moe_handle h, uint32_t* flags, moe_stream_t stream) {
     cudaError_t e = cudaMemcpyAsync(&v, h->ws.status, sizeof(v), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->ws.status, 0, sizeof(uint32_t), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    // a timed-out fused launch may leave its grid-barrier words mid-count
+    if (e == cudaSuccess && (v & MOE_ST_TIMEOUT)) e = cudaMemset(h->ws.ticket + 2, 0, 2 * sizeof(uint32_t));
     if (e != cudaSuccess) return cuda_fail(h, e, "reading the status word");
     *flags = v;
     return MOE_OK;
@@ -494,6 +542,11 @@ int moe_read_status(moe_handle h, uint32_t* flags, moe_stream_t stream) {
 
 const char* moe_last_error(moe_handle h) {
     return h ? h->err.c_str() : g_create_err.c_str();
+}
+
+int moe_last_path(moe_handle h) {
+    if (!h) return MOE_EINVAL;
+    return h->last_path;
 }
 
 int moe_dispatch_scheme(moe_handle h) {

@@ -37,6 +37,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include "gemm_common.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -82,73 +83,6 @@ struct Cfg {
     static_assert(4 % KS == 0, "K-steps per stage must split evenly");
     static_assert(CW % 16 == 0, "epilogue column split");
 };
-
-// Pipeline tracing (compiled in with -DBMOE_TRACE): clock64 stamps of the first
-// kTraceJobs K stages of CTAs 0 and 1, per role, into GemmArgs::trace
-// ([2 CTAs][6 events][kTraceJobs] int64): 0 producer got a free stage, 1 producer
-// issued it, 2 first MMA warp saw it full, 3 that warp issued its MMAs; per
-// unit: 4 epilogue saw the accumulator, 5 epilogue released it.
-__device__ __forceinline__ void trace(const GemmArgs& a, int ev, long idx) {
-#ifdef BMOE_TRACE
-    constexpr int kTraceJobs = 512;
-    if (a.trace && blockIdx.x < 2 && idx < kTraceJobs)
-        a.trace[(static_cast<long>(blockIdx.x) * 6 + ev) * kTraceJobs + idx] = clock64();
-#else
-    (void)a;
-    (void)ev;
-    (void)idx;
-#endif
-}
-
-struct UnitInfo {
-    int e, m, g, row0, n;
-};
-
-// Routing plan as read by the GEMM roles: shared-memory copies when E fits the
-// tables, else the global arrays.
-struct Plan {
-    const int32_t* tile_base;  // [E+1]
-    const int32_t* rowbase;    // [E+1]
-    const int32_t* counts;     // [E]
-};
-
-// Unit u of the global list: experts ascending; inside an expert, weight tile m
-// major and route tile j minor, so CTAs running consecutive units share a
-// weight tile (L2 reuse when an expert has several route tiles).  `ecur` only
-// moves forward because every role walks its units in increasing order.
-__device__ __forceinline__ UnitInfo decode_unit(int u, int& ecur, const Plan& pl, int mtiles, int NT) {
-    const int q = u / mtiles;
-    while (pl.tile_base[ecur + 1] <= q) ++ecur;
-    const int tb = pl.tile_base[ecur];
-    const int nt = pl.tile_base[ecur + 1] - tb;
-    const int ul = u - tb * mtiles;
-    UnitInfo r;
-    r.e = ecur;
-    r.m = ul / nt;
-    const int j = ul - r.m * nt;
-    r.g = tb + j;
-    r.row0 = pl.rowbase[ecur] + j * NT;
-    r.n = min(NT, pl.counts[ecur] - j * NT);
-    return r;
-}
-
-// The loads of the last STAGES jobs this producer issued land before the CTA
-// exits (they are consumed already unless another role gave up).  Bounded.
-template <int STAGES>
-__device__ __forceinline__ void drain_stages(uint64_t* full, int stage, uint32_t phase, long issued,
-                                             uint32_t* status) {
-    volatile int never = 0;
-    for (long i = 0; i < STAGES && i < issued; ++i) {
-        if (stage == 0) {
-            stage = STAGES - 1;
-            phase ^= 1u;
-        } else {
-            --stage;
-        }
-        (void)mbar_wait(&full[stage], phase, &never, status, kStTimeout | (1u << (kSiteShift + 1)),
-                        kWaitLimitNs / 4);
-    }
-}
 
 template <bool G1, int NT, int KC>
 __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)

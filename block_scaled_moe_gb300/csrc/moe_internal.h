@@ -18,6 +18,8 @@ constexpr uint32_t kStBadId = 0x1u, kStTimeout = 0x2u, kStOverflow = 0x4u;
 // 1 producer drain, 2 MMA/accumulator-free, 3 MMA/stage-full, 4 MMA drain,
 // 5 epilogue/accumulator-full.
 constexpr uint32_t kSiteShift = 8;
+constexpr uint32_t kSiteGrid = 1u << (kSiteShift + 6);   // fused path: a grid barrier gave up
+constexpr uint32_t kSiteReady = 1u << (kSiteShift + 7);  // fused path: a GEMM1->GEMM2 readiness wait gave up
 
 // Device workspace, carved from one allocation.
 struct Workspace {
@@ -40,6 +42,7 @@ struct Workspace {
     uint8_t* xq;           // [cap][H] canonical codes (debug capture only)
     uint8_t* xs;           // [cap][H/32] canonical scales (debug capture only)
     float* g;              // [rows_cap][2I] raw GEMM1 outputs (debug capture only)
+    uint32_t* ready;       // [tiles_cap] fused path: GEMM1 units finished per route tile
 };
 
 struct Geometry {
@@ -96,6 +99,24 @@ cudaError_t launch_gemm1(const GemmArgs& a, const CUtensorMap* tm_w, const CUten
 cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_h, int NT, int grid,
                          cudaStream_t s);
 cudaError_t gemm_set_attributes();
+
+// ------------------------------------------------------------------ single-launch fused path (moe_fused.cu)
+struct FusedLaunch {
+    const uint16_t* x;
+    const int32_t* ids;
+    const float* wts;
+    const int32_t* nvr;
+    uint16_t* out;
+    const uint8_t* w13s;
+    const uint8_t* w2s;
+    float swiglu_limit;
+    int T;
+};
+bool fused_supported(const Geometry& g);
+cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaunch& f, const CUtensorMap* tm_w13,
+                         const CUtensorMap* tm_aq, const CUtensorMap* tm_w2, const CUtensorMap* tm_hq, int grid,
+                         cudaStream_t s);
+cudaError_t fused_set_attributes();
 
 // Error text of a failed call made without a handle (read by moe_last_error(NULL)).
 void note_unbound_error(const char* msg);

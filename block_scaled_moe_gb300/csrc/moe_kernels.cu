@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include "layer_rows.cuh"
 #include "moe_internal.h"
 
 namespace bmoe {
@@ -12,10 +13,7 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-__device__ __forceinline__ int read_nvr(const int32_t* p, int T) {
-    int v = p ? __ldg(p) : T;
-    return v < 0 ? 0 : (v > T ? T : v);
-}
+using rows::read_nvr;
 
 // Exclusive scan of in[0..n) into out[0..n], out[n] = total.  Whole block.
 __device__ void block_exclusive_scan(const int* in, int* out, int n, int* warp_sums) {
@@ -187,162 +185,20 @@ __global__ void __launch_bounds__(32) k_compact_rank(DispatchArgs a) {
 }
 
 // ---------------------------------------------------------------- quant + scatter
-// MXFP8 quantisation of each valid row (E4M3 codes, one E8M0 scale per 32
-// along H, OCP MX rule: code = max(exponent(amax) - 8, 0), element =
-// RNE_satfinite(x * 2^(127-code))), written once per valid slot into the
-// expert's packed rows; the scale goes into the route tile's 128x4 scale atom
-// (byte 16*(c%32) + 4*(c/32) + kblock%4 for row c of the tile).
-struct QuantArgs {
-    const uint16_t* x;
-    const int32_t* ids;
-    const int32_t* nvr;
-    int T, K, E, H, mtpr, words, NT, scheme;
-    Workspace ws;
-};
-
-__device__ __forceinline__ uint32_t pack_fp8x4(float a, float b, float c, float d) {
-    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-    return lo | (hi << 16);
-}
-
-__global__ void __launch_bounds__(256) k_quant_scatter(QuantArgs a) {
+// One warp per token row (rows::quant_scatter_row).
+__global__ void __launch_bounds__(256) k_quant_scatter(rows::QuantArgs a, const int32_t* nvr_ptr) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= a.T) return;
-    const int nvr = read_nvr(a.nvr, a.T);
-    const int K = a.K;
-    int p = -1, gt = 0, c = 0;
-    bool valid = false;
-    if (lane < K) {
-        const int e = a.ids[(size_t)t * K + lane];
-        if (t < nvr && e >= a.E) atomicOr(a.ws.status, kStBadId);
-        valid = t < nvr && e >= 0 && e < a.E;
-        if (valid) {
-            int i;
-            if (a.scheme == 1) {
-                const uint32_t* wb = a.ws.occ + (size_t)e * a.words;
-                i = 0;
-                for (int w = 0; w < (t >> 5); ++w) i += __popc(__ldg(wb + w));
-                i += __popc(__ldg(wb + (t >> 5)) & ((1u << (t & 31)) - 1u));
-                p = e * a.mtpr + i;
-            } else {
-                p = a.ws.route_row[(size_t)t * K + lane];
-                i = p - __ldg(a.ws.rowbase + e);
-            }
-            gt = __ldg(a.ws.tile_base + e) + i / a.NT;
-            c = i % a.NT;
-        }
-        a.ws.yrow[(size_t)t * K + lane] = valid ? p : -1;
-    }
-    if (t >= nvr) return;
-    const unsigned vmask = __ballot_sync(kFull, valid);
-    int pk[kMaxTopk], gk[kMaxTopk], ck[kMaxTopk];
-#pragma unroll
-    for (int k = 0; k < kMaxTopk; ++k) {
-        pk[k] = __shfl_sync(kFull, p, k);
-        gk[k] = __shfl_sync(kFull, gt, k);
-        ck[k] = __shfl_sync(kFull, c, k);
-    }
-    const int H = a.H, nblk = H >> 5, ktiles = H >> 7;
-    const uint16_t* xrow = a.x + (size_t)t * H;
-    for (int blk = lane; blk < nblk; blk += 32) {
-        const uint4* src = reinterpret_cast<const uint4*>(xrow + blk * 32);
-        float f[32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 v = __ldg(src + q);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                f[q * 8 + 2 * j] = __uint_as_float(w[j] << 16);
-                f[q * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-            }
-        }
-        float amax = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(f[j]));
-        int code = static_cast<int>(__float_as_uint(amax) >> 23) - 8;
-        code = code < 0 ? 0 : code;
-        const float mul = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
-        uint32_t o[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            o[j] = pack_fp8x4(f[4 * j] * mul, f[4 * j + 1] * mul, f[4 * j + 2] * mul, f[4 * j + 3] * mul);
-        const uint4 o0 = make_uint4(o[0], o[1], o[2], o[3]), o1 = make_uint4(o[4], o[5], o[6], o[7]);
-        if (a.ws.xq) {
-            uint4* d = reinterpret_cast<uint4*>(a.ws.xq + (size_t)t * H + blk * 32);
-            d[0] = o0;
-            d[1] = o1;
-            a.ws.xs[(size_t)t * nblk + blk] = static_cast<uint8_t>(code);
-        }
-#pragma unroll
-        for (int k = 0; k < kMaxTopk; ++k) {
-            if (k < K && ((vmask >> k) & 1u)) {
-                uint4* d = reinterpret_cast<uint4*>(a.ws.aq + (size_t)pk[k] * H + blk * 32);
-                d[0] = o0;
-                d[1] = o1;
-                const int ci = ck[k];
-                a.ws.as[((size_t)gk[k] * ktiles + (blk >> 2)) * 512 + 16 * (ci & 31) + 4 * (ci >> 5) + (blk & 3)] =
-                    static_cast<uint8_t>(code);
-            }
-        }
-    }
+    rows::quant_scatter_row(a, a.ws.rowbase, a.ws.tile_base, t, rows::read_nvr(nvr_ptr, a.T), lane);
 }
 
 // ---------------------------------------------------------------- combine
-// out[t] = BF16( sum over valid slots, k ascending, of w[t,k] * y[row(t,k)] ),
-// float accumulation rounded once (ROCm/ATOM PR #2725: the MoE sum "in f32 and
-// rounds once"); -1 slots are skipped (aiter #6881: "its combine skips invalid
-// (-1) top-k slots"); rows with no valid slot are +0.
-struct CombineArgs {
-    const uint16_t* y;
-    const int32_t* yrow;
-    const float* w;
-    uint16_t* out;
-    int T, K, H;
-};
-
-__global__ void __launch_bounds__(128) k_combine(CombineArgs a) {
-    __shared__ int rows[kMaxTopk];
-    __shared__ float wk[kMaxTopk];
-    const int t = blockIdx.x;
-    if (threadIdx.x < a.K) {
-        rows[threadIdx.x] = a.yrow[(size_t)t * a.K + threadIdx.x];
-        wk[threadIdx.x] = a.w[(size_t)t * a.K + threadIdx.x];
-    }
-    __syncthreads();
-    const int nv = a.H >> 3;
-    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-        float acc[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-        bool any = false;
-        for (int k = 0; k < a.K; ++k) {
-            const int r = rows[k];
-            if (r < 0) continue;
-            any = true;
-            const uint4 q = __ldg(reinterpret_cast<const uint4*>(a.y + (size_t)r * a.H) + v);
-            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-            const float wv = wk[k];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                acc[2 * j] = __fadd_rn(acc[2 * j], __fmul_rn(wv, __uint_as_float(w4[j] << 16)));
-                acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __fmul_rn(wv, __uint_as_float(w4[j] & 0xffff0000u)));
-            }
-        }
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if (any) {
-            uint32_t ow[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
-                ow[j] = *reinterpret_cast<const uint32_t*>(&b);
-            }
-            o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-        }
-        reinterpret_cast<uint4*>(a.out + (size_t)t * a.H)[v] = o;
-    }
+// One warp per output row (rows::combine_row).
+__global__ void __launch_bounds__(256) k_combine(rows::CombineArgs a) {
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= a.T) return;
+    rows::combine_row(a, t, threadIdx.x & 31);
 }
 
 DispatchArgs dispatch_args(const Geometry& g, const Workspace& ws, const int32_t* ids, int T, const int32_t* nvr) {
@@ -388,6 +244,7 @@ size_t workspace_layout(const Geometry& g, char* base, Workspace* ws) {
     w.hq = reinterpret_cast<uint8_t*>(carve((size_t)g.rows_cap * g.I));
     w.hs = reinterpret_cast<uint8_t*>(carve((size_t)g.tiles_cap * (g.I / 128) * 512));
     w.y = reinterpret_cast<uint16_t*>(carve((size_t)g.rows_cap * g.H * 2));
+    w.ready = reinterpret_cast<uint32_t*>(carve(sizeof(uint32_t) * (size_t)g.tiles_cap));
     if (g.debug) {
         w.xq = reinterpret_cast<uint8_t*>(carve((size_t)g.cap * g.H));
         w.xs = reinterpret_cast<uint8_t*>(carve((size_t)g.cap * (g.H / 32)));
@@ -418,10 +275,9 @@ cudaError_t launch_compact_dispatch(const Geometry& g, const Workspace& ws, cons
 
 cudaError_t launch_quant_scatter(const Geometry& g, const Workspace& ws, const uint16_t* x, const int32_t* ids,
                                  int T, const int32_t* nvr, cudaStream_t s) {
-    QuantArgs a;
+    rows::QuantArgs a;
     a.x = x;
     a.ids = ids;
-    a.nvr = nvr;
     a.T = T;
     a.K = g.K;
     a.E = g.E;
@@ -431,13 +287,13 @@ cudaError_t launch_quant_scatter(const Geometry& g, const Workspace& ws, const u
     a.NT = g.NT;
     a.scheme = g.scheme;
     a.ws = ws;
-    k_quant_scatter<<<(T + 7) / 8, 256, 0, s>>>(a);
+    k_quant_scatter<<<(T + 7) / 8, 256, 0, s>>>(a, nvr);
     return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const Geometry& g, const Workspace& ws, const float* wts, int T,
                            const int32_t* /*nvr*/, uint16_t* out, cudaStream_t s) {
-    CombineArgs a;
+    rows::CombineArgs a;
     a.y = ws.y;
     a.yrow = ws.yrow;
     a.w = wts;
@@ -445,7 +301,7 @@ cudaError_t launch_combine(const Geometry& g, const Workspace& ws, const float* 
     a.T = T;
     a.K = g.K;
     a.H = g.H;
-    k_combine<<<T, 128, 0, s>>>(a);
+    k_combine<<<(T + 7) / 8, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -62,9 +62,11 @@ typedef void* moe_stream_t;
 #define MOE_ST_BAD_ID 0x1u      /* a top-k id >= E was seen (skipped like -1) */
 #define MOE_ST_TIMEOUT 0x2u     /* a bounded device-side wait gave up */
 #define MOE_ST_OVERFLOW 0x4u    /* internal tile list overflow (bug guard) */
-/* With MOE_ST_TIMEOUT, bits 8..13 name the wait that gave up (diagnostic):
+/* With MOE_ST_TIMEOUT, bits 8..15 name the wait that gave up (diagnostic):
  * 8 producer/stage-free, 9 producer drain, 10 MMA/accumulator-free,
- * 11 MMA/stage-full, 12 MMA drain, 13 epilogue/accumulator-full. */
+ * 11 MMA/stage-full, 12 MMA drain, 13 epilogue/accumulator-full,
+ * 14 fused path grid barrier, 15 fused path GEMM1->GEMM2 readiness.
+ * Reading a timeout also resets the fused path's grid-barrier words. */
 
 /* ------------------------------------------------------------- options */
 #define MOE_OPT_DISPATCH 1        /* MOE_DISPATCH_* */
@@ -76,6 +78,19 @@ typedef void* moe_stream_t;
 #define MOE_OPT_PROFILE 6         /* 1 = bracket each stage of every forward with CUDA events
                                      (eager use only: keep 0 while capturing a CUDA graph) */
 #define MOE_OPT_LAUNCHES 7        /* read-only: CUDA kernels this handle has launched so far */
+#define MOE_OPT_PATH 8            /* MOE_PATH_*: which kernels a forward runs */
+
+/* MOE_PATH_AUTO runs the single-launch fused kernel (ROCm/aiter PR #6881,
+ * MegaMoEV2 small-input fusion, "Technical Details": for inputs of at most 512
+ * tokens every step of the layer happens inside one kernel launch) when the
+ * handle allows it: capacity <= 512, route tile 32, E <= 512, and a device
+ * that supports cooperative launches; otherwise it runs the multi-kernel path.
+ * MOE_PATH_FUSED insists on the fused kernel (setting it is refused when the
+ * handle does not allow it); MOE_PATH_MULTI always runs the separate kernels.  Both
+ * paths produce the same bits. */
+#define MOE_PATH_AUTO 0
+#define MOE_PATH_FUSED 1
+#define MOE_PATH_MULTI 2
 
 #define MOE_DISPATCH_AUTO 0       /* fixed-slot iff capacity <= fixed-slot max */
 #define MOE_DISPATCH_FIXED 1
@@ -157,10 +172,14 @@ const char* moe_last_error(moe_handle h);
 /* Which dispatch scheme the handle runs: MOE_DISPATCH_FIXED or _COMPACT. */
 int moe_dispatch_scheme(moe_handle h);
 
+/* Path the last forward took: MOE_PATH_FUSED or MOE_PATH_MULTI (0 before any forward). */
+int moe_last_path(moe_handle h);
+
 /* Stage times in milliseconds of the last forward run with MOE_OPT_PROFILE=1,
  * measured by CUDA events recorded on the forward's stream:
  *   ms[0] dispatch, ms[1] quantisation + scatter, ms[2] GEMM1, ms[3] GEMM2,
- *   ms[4] combine.  Waits for the last event; n = entries ms can hold (<= 5
+ *   ms[4] combine.  A forward on the fused path reports its single kernel in
+ *   ms[2] and 0 elsewhere.  Waits for the last event; n = entries ms can hold (<= 5
  * written).  MOE_ESTATE if profiling is off or no profiled forward ran. */
 #define MOE_PROFILE_STAGES 5
 int moe_profile_read(moe_handle h, float* ms, int n);
@@ -199,8 +218,8 @@ int moe_dispatch_compact_noalloc(const int32_t* topk_ids, int T, int topk, int E
 #define MOE_DBG_ROUTE_ROW 4     /* int32 [T*topk]: compact slot -> packed position, -1 invalid */
 #define MOE_DBG_ROUTE_SLOT 5    /* int32 [T*topk]: fixed slot -> e*capacity+t, -1 invalid */
 #define MOE_DBG_OCC 6           /* uint32 [E][ceil(capacity/32)]: fixed-slot occupancy bits */
-#define MOE_DBG_XQ 7            /* uint8 [T][H]: canonical E4M3 codes of x (needs DEBUG_CAPTURE) */
-#define MOE_DBG_XS 8            /* uint8 [T][H/32]: canonical E8M0 scales of x (needs DEBUG_CAPTURE) */
+#define MOE_DBG_XQ 7            /* uint8 [T][H]: canonical E4M3 codes of x, rows < num_valid_rows (needs DEBUG_CAPTURE) */
+#define MOE_DBG_XS 8            /* uint8 [T][H/32]: canonical E8M0 scales of x, rows < num_valid_rows (needs DEBUG_CAPTURE) */
 #define MOE_DBG_YROW 9          /* int32 [T*topk]: row of the GEMM2 output each slot combines, -1 invalid */
 #define MOE_DBG_HQ 10           /* uint8 [rows][I]: E4M3 codes of h per packed row */
 #define MOE_DBG_G 11            /* float [rows][2I]: raw GEMM1 outputs (needs DEBUG_CAPTURE) */
