@@ -122,10 +122,12 @@ __device__ __forceinline__ void quant_scatter_row(const QuantArgs& a, const int3
 
 // out[t] = BF16( sum over valid slots, k ascending, of w[t,k] * y[row(t,k)] ),
 // float accumulation rounded once (ROCm/ATOM PR #2725: the MoE sum "in f32 and
-// rounds once"); -1 slots are skipped (ROCm/aiter PR #6881: "its combine skips
-// invalid (-1) top-k slots"); rows with no valid slot are +0.  One warp per
-// row, 16-byte vectors; y is read with L2-coherent loads (the fused kernel
+// rounds once"); -1 slots are skipped (ROCm/aiter PR #6881, Technical
+// Details: both paths leave out top-k slots marked -1); rows with no valid slot
+// are +0.  Work item = one segment of kCombineVecs 16-byte vectors of one row,
+// one warp per item; y is read with L2-coherent loads (the fused kernel
 // combines rows other CTAs wrote in the same launch).
+constexpr int kCombineVecs = 64;  // 512 BF16 elements per work item
 struct CombineArgs {
     const uint16_t* y;
     const int32_t* yrow;
@@ -134,7 +136,13 @@ struct CombineArgs {
     int T, K, H;
 };
 
-__device__ __forceinline__ void combine_row(const CombineArgs& a, int t, int lane) {
+__device__ __forceinline__ int combine_items(const CombineArgs& a) {
+    return a.T * ((a.H / 8 + kCombineVecs - 1) / kCombineVecs);
+}
+
+__device__ __forceinline__ void combine_item(const CombineArgs& a, int item, int lane) {
+    const int segs = (a.H / 8 + kCombineVecs - 1) / kCombineVecs;
+    const int t = item / segs, seg = item - t * segs;
     int r_l = -1;
     float w_l = 0.f;
     if (lane < a.K) {
@@ -148,8 +156,8 @@ __device__ __forceinline__ void combine_row(const CombineArgs& a, int t, int lan
         rows[k] = __shfl_sync(kFull, r_l, k);
         wk[k] = __shfl_sync(kFull, w_l, k);
     }
-    const int nv = a.H >> 3;
-    for (int v = lane; v < nv; v += 32) {
+    const int v1 = min(a.H >> 3, (seg + 1) * kCombineVecs);
+    for (int v = seg * kCombineVecs + lane; v < v1; v += 32) {
         float acc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.f;

@@ -28,6 +28,20 @@
 #include "moe_internal.h"
 #include "ptx.cuh"
 
+#ifdef BMOE_TRACE
+// Phase trace (tracing builds only): per CTA 16 int64 slots of globaltimer ns
+// stamps and counters, read back with bmoe_fused_trace_copy.
+__device__ long long g_fused_trace[1024 * 16];
+#define FTRACE(ev, val)                                              \
+    do {                                                             \
+        if (blockIdx.x < 1024) g_fused_trace[blockIdx.x * 16 + (ev)] = (val); \
+    } while (0)
+#else
+#define FTRACE(ev, val) \
+    do {                \
+    } while (0)
+#endif
+
 namespace bmoe {
 
 namespace {
@@ -146,6 +160,190 @@ __device__ __forceinline__ FUnit fused_unit(int u, int U1, FCursor& c, const Pla
     return r;
 }
 
+// Phase-1 pipeline: the stage ring in shared memory and the TMEM base.
+struct P1 {
+    uint8_t* sA;     // [stage][2] weight chunks
+    uint8_t* sB;     // [stage][2] row chunks
+    uint8_t* sSFA;   // [stage][2] weight scale atoms
+    uint8_t* sSFB;   // [stage][2] row scale atoms
+    uint64_t* full;
+    uint64_t* empty;
+    volatile int* abort_flag;
+    uint32_t* status;
+    uint32_t tmem;
+};
+
+struct Ring {
+    int stage = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next() {
+        if (++stage == F_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// TMA producer, one unit of kt K stages.  GEMM1 (G2 false): gate and up chunks (rows wrow and
+// wrow + up_off), one row chunk and its scale atom per stage; GEMM2: KC (W2 chunk, h chunk)
+// pairs and KC h-scale atoms per stage.  The row-scale atoms of the unit start at bsf.
+template <bool G2, int KC>
+__device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued, const CUtensorMap* tw,
+                                             const CUtensorMap* tb, int wrow, int up_off, int row0,
+                                             const uint8_t* bsf, int kt, uint64_t pol_w, uint64_t pol_b) {
+    for (int kk = 0; kk < kt; ++kk) {
+        if (!mbar_wait(&p.empty[r.stage], r.phase ^ 1u, p.abort_flag, p.status, kStTimeout | (1u << (kSiteShift + 0)),
+                       kWaitLimitNs))
+            return false;
+        uint64_t* fb = &p.full[r.stage];
+        uint8_t* a0 = p.sA + (r.stage * 2) * F_A_BYTES;
+        uint8_t* b0 = p.sB + (r.stage * 2) * F_B_BYTES;
+        if constexpr (!G2) {
+            mbar_expect_tx(fb, 2 * F_A_TX + F_B_BYTES + 512);
+            tma_load_2d(a0, tw, fb, kk * 128, wrow, pol_w);
+            tma_load_2d(a0 + F_A_BYTES, tw, fb, kk * 128, wrow + up_off, pol_w);
+            tma_load_2d(b0, tb, fb, kk * 128, row0, pol_b);
+            bulk_load(p.sSFB + (r.stage * 2) * 512, bsf + static_cast<size_t>(kk) * 512, 512, fb);
+        } else {
+            mbar_expect_tx(fb, KC * (F_A_TX + F_B_BYTES + 512));
+#pragma unroll
+            for (int c = 0; c < KC; ++c) {
+                const int k0 = (kk * KC + c) * 128;
+                tma_load_2d(a0 + c * F_A_BYTES, tw, fb, k0, wrow, pol_w);
+                tma_load_2d(b0 + c * F_B_BYTES, tb, fb, k0, row0, pol_b);
+            }
+            bulk_load(p.sSFB + (r.stage * 2) * 512, bsf + static_cast<size_t>(kk) * KC * 512, KC * 512, fb);
+        }
+        mbar_arrive(fb);
+        ++issued;
+        r.next();
+    }
+    return true;
+}
+
+// MMA issue of one unit by chain w (its warp's lane 0).  GEMM1: chain w multiplies operand
+// w & 1 (gate / up) over the K-steps k with k % 2 == w >> 1; GEMM2: the K-steps k with
+// k % 4 == w of the stage's KC chunks.  Each chain copies its own scale atoms to TMEM
+// (two slots, alternating stages).
+template <bool G2, int KC>
+__device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w, int lane, uint32_t d_tmem, int N,
+                                         int kt) {
+    constexpr int KS = G2 ? F_MW : F_MW / 2;
+    constexpr int NCH = G2 ? KC : 1;
+    const int op = G2 ? 0 : (w & 1);
+    const int kq = G2 ? w : (w >> 1);
+    for (int kk = 0; kk < kt; ++kk) {
+        if (!mbar_wait(&p.full[r.stage], r.phase, p.abort_flag, p.status, kStTimeout | (1u << (kSiteShift + 3)),
+                       kWaitLimitNs))
+            return false;
+        tc_fence_after();
+        if (lane == 0) {
+            const uint32_t sfc = p.tmem + static_cast<uint32_t>(F_SF_BASE + (w * 2 + (job & 1)) * F_SF_SLOT);
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                tc_cp_32x128b_x4(sfc + 4 * c, desc_sf_atom(smem_u32(p.sSFA + (r.stage * 2 + (G2 ? c : op)) * 512)));
+                tc_cp_32x128b_x4(sfc + 8 + 4 * c, desc_sf_atom(smem_u32(p.sSFB + (r.stage * 2 + c) * 512)));
+            }
+#pragma unroll
+            for (int k = 0; k < 4 * NCH; ++k) {
+                if (k % KS != kq) continue;
+                const int c = k >> 2, k4 = k & 3;
+                const uint64_t da = desc_kmajor_sw128(smem_u32(p.sA + (r.stage * 2 + (G2 ? c : op)) * F_A_BYTES)) +
+                                    static_cast<uint64_t>((k4 * 32) >> 4);
+                const uint64_t db = desc_kmajor_sw128(smem_u32(p.sB + (r.stage * 2 + c) * F_B_BYTES)) +
+                                    static_cast<uint64_t>((k4 * 32) >> 4);
+                tc_mma_mx(d_tmem, da, db, idesc_mx(128, N, 5, 0, k4, k4), sfc + 4 * c, sfc + 8 + 4 * c,
+                          (kk > 0 || k != kq) ? 1u : 0u);
+            }
+            tc_commit(&p.empty[r.stage]);
+        }
+        __syncwarp();
+        ++job;
+        r.next();
+    }
+    return true;
+}
+
+// Epilogue of one unit by one warp (TMEM lane quadrant qd = its 32 output features).  The
+// chains are summed in the stand-alone GEMMs' order, from +0, so both paths give the same
+// bits.  GEMM1: gate/up -> optional clamp -> SwiGLU -> MXFP8 per 32 features (OCP MX rule)
+// into the h rows and their scale atom, then this warp's share of tile g is released to the
+// GEMM2 units; GEMM2: BF16 rows of y.  The accumulator is handed back before the stores.
+template <bool G2>
+__device__ __forceinline__ void epilogue_unit(const P1& p, uint64_t* acce_b, const Workspace& ws, const UnitInfo& cu,
+                                              int acc, int qd, int lane, int I, int H, float L) {
+    const uint32_t tb = p.tmem + (static_cast<uint32_t>(32 * qd) << 16) + static_cast<uint32_t>(acc * F_ACC_COLS);
+    const int feat = cu.m * 128 + 32 * qd + lane;
+    float v[F_NT];
+#pragma unroll
+    for (int j = 0; j < F_NT / 16; ++j) {
+        const int c0 = 16 * j;
+        if (c0 < cu.n) {
+            uint32_t r[F_MW][16];
+#pragma unroll
+            for (int w = 0; w < F_MW; ++w) tmem_ld16(tb + w * F_NT + c0, r[w]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float ga = 0.f, ub = 0.f;
+#pragma unroll
+                for (int w = 0; w < F_MW; ++w) {
+                    if (!G2 && (w & 1))
+                        ub += __uint_as_float(r[w][i]);
+                    else
+                        ga += __uint_as_float(r[w][i]);
+                }
+                if constexpr (!G2) {
+                    if (ws.g && c0 + i < cu.n) {
+                        const size_t prow = static_cast<size_t>(cu.row0 + c0 + i);
+                        ws.g[prow * 2 * I + feat] = ga;
+                        ws.g[prow * 2 * I + I + feat] = ub;
+                    }
+                    if (L > 0.f) {
+                        ga = fminf(ga, L);
+                        ub = fminf(fmaxf(ub, -L), L);
+                    }
+                    v[c0 + i] = ga * (1.0f / (1.0f + expf(-ga))) * ub;
+                } else {
+                    v[c0 + i] = ga;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    mbar_arrive(acce_b);
+#pragma unroll
+    for (int c = 0; c < F_NT; ++c) {
+        if (c < cu.n) {
+            const size_t prow = static_cast<size_t>(cu.row0 + c);
+            if constexpr (!G2) {
+                const float h = v[c];
+                const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
+                int code = static_cast<int>(amax >> 23) - 8;
+                code = code < 0 ? 0 : code;
+                const float mul = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
+                ws.hq[prow * I + feat] = __nv_cvt_float_to_fp8(h * mul, __NV_SATFINITE, __NV_E4M3);
+                if (lane == 0)
+                    ws.hs[((size_t)cu.g * (I >> 7) + cu.m) * 512 + 16 * (c & 31) + 4 * (c >> 5) + qd] =
+                        static_cast<uint8_t>(code);
+            } else {
+                ws.y[prow * H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(v[c]));
+            }
+        }
+    }
+    if constexpr (!G2) {
+        // Release this warp's 32 features of tile g's h rows to the GEMM2 units (TMA reads them
+        // from any CTA); warps release independently, nobody waits here.
+        fence_proxy_async_all();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence();
+            atom_add_release_u32(&ws.ready[cu.g], 1u);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(F_THREADS, 1)
     k_fused(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_aq,
             const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_hq, const FusedArgs f) {
@@ -176,7 +374,10 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     int32_t* t_tile = tab;                  // [E+1]
     int32_t* t_row = tab + F_TAB_E + 1;     // [E+1]
     int32_t* t_cnt = tab + 2 * F_TAB_E + 2; // [E]
-    if (threadIdx.x == 0) *abort_flag = 0;
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        FTRACE(0, (long long)globaltimer_ns());
+    }
     __syncthreads();
 
     // ------------------------------------------------------------------ phase 0: dispatch + quant
@@ -314,12 +515,26 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         tc_fence_after();
         const uint32_t tmem = *tmem_slot;
 
+        if (threadIdx.x == 0) FTRACE(1, (long long)globaltimer_ns());
+        P1 p;
+        p.sA = sA;
+        p.sB = sB;
+        p.sSFA = sSFA;
+        p.sSFB = sSFB;
+        p.full = full;
+        p.empty = empty;
+        p.abort_flag = abort_flag;
+        p.status = ws.status;
+        p.tmem = tmem;
         if (warp == 0) {
             // -------------------------------------------------------- TMA producer (one thread)
             if (lane == 0 && my_units > 0) {
+#ifdef BMOE_TRACE
+                long long wait_ns = 0;
+                bool first_g2 = true;
+#endif
                 const uint64_t pol_w = policy_evict_first(), pol_b = policy_evict_last();
-                int stage = 0;
-                uint32_t phase = 0;
+                Ring ring;
                 long issued = 0;
                 bool ok = true;
                 FCursor cur;
@@ -327,167 +542,157 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 for (int ui = 0; ui < my_units && ok; ++ui) {
                     const FUnit fu = fused_unit(blockIdx.x + ui * gridDim.x, U1, cur, pl, mt1, mt2);
                     const UnitInfo& cu = fu.u;
-                    const int kt = fu.g2 ? kt2 : kt1;
-                    if (fu.g2) {
-                        // the h rows of tile g are complete once all epilogue warps of its I/128 GEMM1
-                        // units released them
-                        const uint64_t t0 = globaltimer_ns();
-                        while (ld_acquire_u32(&ws.ready[cu.g]) != static_cast<uint32_t>(mt1 * F_EW)) {
-                            if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
-                                atomicOr(ws.status, kStTimeout | kSiteReady);
-                                *abort_flag = 1;
-                                ok = false;
-                                break;
-                            }
-                            __nanosleep(64);
-                        }
-                        if (!ok) break;
-                        fence_proxy_async_all();
+                    if (!fu.g2) {
+                        ok = produce_unit<false, 1>(p, ring, issued, &tm_w13, &tm_aq, cu.e * 2 * I + cu.m * 128, I,
+                                                    cu.row0, ws.as + (size_t)cu.g * kt1 * 512, kt1, pol_w, pol_b);
+                        continue;
                     }
-                    for (int kk = 0; kk < kt; ++kk) {
-                        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, ws.status,
-                                       kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
+                    // the h rows of tile g are complete once all epilogue warps of its I/128 GEMM1
+                    // units released them
+                    const uint64_t t0 = globaltimer_ns();
+#ifdef BMOE_TRACE
+                    if (first_g2) FTRACE(2, (long long)t0);
+#endif
+                    while (ld_acquire_u32(&ws.ready[cu.g]) != static_cast<uint32_t>(mt1 * F_EW)) {
+                        if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+                            atomicOr(ws.status, kStTimeout | kSiteReady);
+                            *abort_flag = 1;
                             ok = false;
                             break;
                         }
-                        if (!fu.g2) {
-                            const int wrow = cu.e * 2 * I + cu.m * 128;
-                            mbar_expect_tx(&full[stage], 2 * F_A_TX + F_B_BYTES + 512);
-                            tma_load_2d(sA + (stage * 2) * F_A_BYTES, &tm_w13, &full[stage], kk * 128, wrow, pol_w);
-                            tma_load_2d(sA + (stage * 2 + 1) * F_A_BYTES, &tm_w13, &full[stage], kk * 128, wrow + I,
-                                        pol_w);
-                            tma_load_2d(sB + (stage * 2) * F_B_BYTES, &tm_aq, &full[stage], kk * 128, cu.row0, pol_b);
-                            bulk_load(sSFB + (stage * 2) * 512, ws.as + ((size_t)cu.g * kt1 + kk) * 512, 512,
-                                      &full[stage]);
-                        } else {
-                            const int wrow = cu.e * H + cu.m * 128;
-                            mbar_expect_tx(&full[stage], f.kc2 * (F_A_TX + F_B_BYTES + 512));
-                            for (int c = 0; c < f.kc2; ++c) {
-                                const int k0 = (kk * f.kc2 + c) * 128;
-                                tma_load_2d(sA + (stage * 2 + c) * F_A_BYTES, &tm_w2, &full[stage], k0, wrow, pol_w);
-                                tma_load_2d(sB + (stage * 2 + c) * F_B_BYTES, &tm_hq, &full[stage], k0, cu.row0,
-                                            pol_b);
-                            }
-                            bulk_load(sSFB + (stage * 2) * 512, ws.hs + ((size_t)cu.g * ktot2 + kk * f.kc2) * 512,
-                                      f.kc2 * 512, &full[stage]);
-                        }
-                        mbar_arrive(&full[stage]);
-                        ++issued;
-                        if (++stage == F_STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                        __nanosleep(64);
                     }
+                    if (!ok) break;
+#ifdef BMOE_TRACE
+                    {
+                        const long long t1 = (long long)globaltimer_ns();
+                        if (first_g2) FTRACE(3, t1);
+                        first_g2 = false;
+                        wait_ns += t1 - (long long)t0;
+                    }
+#endif
+                    fence_proxy_async_all();
+                    const int wrow = cu.e * H + cu.m * 128;
+                    const uint8_t* bsf = ws.hs + (size_t)cu.g * ktot2 * 512;
+                    ok = f.kc2 == 2 ? produce_unit<true, 2>(p, ring, issued, &tm_w2, &tm_hq, wrow, 0, cu.row0, bsf,
+                                                            kt2, pol_w, pol_b)
+                                    : produce_unit<true, 1>(p, ring, issued, &tm_w2, &tm_hq, wrow, 0, cu.row0, bsf,
+                                                            kt2, pol_w, pol_b);
                 }
-                drain_stages<F_STAGES>(full, stage, phase, issued, ws.status);
+#ifdef BMOE_TRACE
+                FTRACE(4, wait_ns);
+                FTRACE(5, (long long)globaltimer_ns());
+#endif
+                drain_stages<F_STAGES>(full, ring.stage, ring.phase, issued, ws.status);
             }
         } else if (warp == 1) {
             // -------------------------------------------------------- weight-scale producer (32 lanes)
-            int stage = 0;
-            uint32_t phase = 0;
-            FCursor cur;
-            bool ok = true;
-            for (int ui = 0; ui < my_units && ok; ++ui) {
-                const FUnit fu = fused_unit(blockIdx.x + ui * gridDim.x, U1, cur, pl, mt1, mt2);
-                const UnitInfo& cu = fu.u;
-                const int kt = fu.g2 ? kt2 : kt1;
-                const uint8_t* wsf = fu.g2 ? f.w2s : f.w13s;
-                const int ld = fu.g2 ? I / 32 : H / 32;
-                const int wrow = fu.g2 ? cu.e * H + cu.m * 128 : cu.e * 2 * I + cu.m * 128;
-                const uint8_t* base = wsf + (static_cast<size_t>(wrow) + lane) * ld;
-                for (int kk = 0; kk < kt; ++kk) {
-                    uint32_t wv[8];
-                    // atom a: GEMM1 -> (gate, up) rows, K chunk kk; GEMM2 -> K chunk kk*kc2 + a
+            // Lane l writes, per stage, line l of two 128x4 scale atoms (GEMM1: gate and up rows;
+            // GEMM2: two K chunks): the 4 K-block bytes of rows l, l+32, l+64, l+96.  Stages are
+            // handled in groups of up to 4 of one unit, loaded one group ahead into registers
+            // (component j of each uint4 = stage j).  GEMM1 rows whose scale stride is a multiple
+            // of 16 bytes take one 16-byte load per row and group: the weight-scale lines then need
+            // not stay in L1, which this kernel's shared-memory footprint leaves small.
+            const bool g1_vec = (H % 512) == 0;
+            int q_ui = 0, q_kk = 0, q_kt = 0, q_ld = 0;
+            bool q_g2 = false;
+            const uint8_t* q_base = nullptr;
+            FCursor qcur;
+            auto load_group = [&](uint4(&g)[2][4]) -> int {
+                if (q_ui >= my_units) return 0;
+                if (q_kk == 0) {
+                    const FUnit fu = fused_unit(blockIdx.x + q_ui * gridDim.x, U1, qcur, pl, mt1, mt2);
+                    q_g2 = fu.g2;
+                    q_kt = fu.g2 ? kt2 : kt1;
+                    q_ld = fu.g2 ? I / 32 : H / 32;
+                    const int wrow = fu.g2 ? fu.u.e * H + fu.u.m * 128 : fu.u.e * 2 * I + fu.u.m * 128;
+                    q_base = (fu.g2 ? f.w2s : f.w13s) + (static_cast<size_t>(wrow) + lane) * q_ld;
+                }
+                const int len = min(4, q_kt - q_kk);
+                if (!q_g2 && g1_vec) {
 #pragma unroll
-                    for (int a4 = 0; a4 < 2; ++a4) {
-                        const bool use = !fu.g2 || a4 < f.kc2;
-                        const uint8_t* src = fu.g2 ? base + (kk * f.kc2 + a4) * 4
-                                                   : base + static_cast<size_t>(a4 * I) * ld + kk * 4;
+                    for (int a4 = 0; a4 < 2; ++a4)
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            wv[4 * a4 + i] =
-                                use ? __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(32 * i) * ld))
-                                    : 0u;
-                    }
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, ws.status,
-                                   kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    uint4* dst = reinterpret_cast<uint4*>(sSFA + (stage * 2) * 512) + lane;
-                    dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                    dst[32] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-                    fence_proxy_async_smem();
-                    mbar_arrive(&full[stage]);
-                    if (++stage == F_STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                            g[a4][i] = __ldg(reinterpret_cast<const uint4*>(
+                                q_base + static_cast<size_t>(a4 * I + 32 * i) * q_ld + q_kk * 4));
+                } else {
+#pragma unroll
+                    for (int a4 = 0; a4 < 2; ++a4) {
+                        const bool use = !q_g2 || a4 < f.kc2;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int kk = q_kk + j;
+                                const uint8_t* src = q_g2 ? q_base + (kk * f.kc2 + a4) * 4
+                                                          : q_base + static_cast<size_t>(a4 * I) * q_ld + kk * 4;
+                                w4[j] = (use && j < len) ? __ldg(reinterpret_cast<const uint32_t*>(
+                                                               src + static_cast<size_t>(32 * i) * q_ld))
+                                                         : 0u;
+                            }
+                            g[a4][i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
                     }
                 }
+                q_kk += len;
+                if (q_kk == q_kt) {
+                    q_kk = 0;
+                    ++q_ui;
+                }
+                return len;
+            };
+            auto word = [](const uint4& v, int j) { return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w; };
+            uint4 cur[2][4], nxt[2][4];
+            int clen = load_group(cur);
+            Ring ring;
+            bool ok = true;
+            while (clen > 0 && ok) {
+                const int nlen = load_group(nxt);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (j < clen && ok) {
+                        if (!mbar_wait(&empty[ring.stage], ring.phase ^ 1u, abort_flag, ws.status,
+                                       kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
+                            ok = false;
+                        } else {
+                            uint4* dst = reinterpret_cast<uint4*>(sSFA + (ring.stage * 2) * 512) + lane;
+                            dst[0] = make_uint4(word(cur[0][0], j), word(cur[0][1], j), word(cur[0][2], j),
+                                                word(cur[0][3], j));
+                            dst[32] = make_uint4(word(cur[1][0], j), word(cur[1][1], j), word(cur[1][2], j),
+                                                 word(cur[1][3], j));
+                            fence_proxy_async_smem();
+                            mbar_arrive(&full[ring.stage]);
+                            ring.next();
+                        }
+                    }
+                }
+#pragma unroll
+                for (int a4 = 0; a4 < 2; ++a4)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) cur[a4][i] = nxt[a4][i];
+                clen = nlen;
             }
         } else if (warp < F_EPI_WARP0) {
             // -------------------------------------------------------- MMA issuers (one chain each)
             const int w = warp - F_MMA_WARP0;
-            int stage = 0, acc = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            Ring ring;
+            int acc = 0;
+            uint32_t acc_phase = 0;
             long job = 0;
-            bool ok = true;
             FCursor cur;
-            for (int ui = 0; ui < my_units && ok; ++ui) {
+            for (int ui = 0; ui < my_units; ++ui) {
                 const FUnit fu = fused_unit(blockIdx.x + ui * gridDim.x, U1, cur, pl, mt1, mt2);
                 const int N = (fu.u.n + 15) & ~15;
-                const int kt = fu.g2 ? kt2 : kt1;
-                const int kc = fu.g2 ? f.kc2 : 1;
-                // GEMM1: chain w = (operand w&1: gate/up, K-steps k%2 == w>>1); GEMM2: K-steps k%4 == w
-                const int op = fu.g2 ? 0 : (w & 1);
-                const int ks = fu.g2 ? 4 : 2, kq = fu.g2 ? w : (w >> 1);
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * F_ACC_COLS + w * F_NT);
                 if (!mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, ws.status,
-                               kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs)) {
-                    ok = false;
+                               kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs))
                     break;
-                }
                 tc_fence_after();
-                for (int kk = 0; kk < kt; ++kk) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, ws.status, kStTimeout | (1u << (kSiteShift + 3)),
-                                   kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t sfc =
-                            tmem + static_cast<uint32_t>(F_SF_BASE + (w * 2 + (job & 1)) * F_SF_SLOT);
-                        if (!fu.g2) {
-                            tc_cp_32x128b_x4(sfc, desc_sf_atom(smem_u32(sSFA + (stage * 2 + op) * 512)));
-                            tc_cp_32x128b_x4(sfc + 8, desc_sf_atom(smem_u32(sSFB + (stage * 2) * 512)));
-                        } else {
-                            for (int c = 0; c < kc; ++c) {
-                                tc_cp_32x128b_x4(sfc + 4 * c, desc_sf_atom(smem_u32(sSFA + (stage * 2 + c) * 512)));
-                                tc_cp_32x128b_x4(sfc + 8 + 4 * c,
-                                                 desc_sf_atom(smem_u32(sSFB + (stage * 2 + c) * 512)));
-                            }
-                        }
-                        for (int k = kq; k < 4 * kc; k += ks) {
-                            const int c = fu.g2 ? (k >> 2) : 0, k4 = k & 3;
-                            const int achunk = fu.g2 ? c : op;
-                            const uint64_t da = desc_kmajor_sw128(smem_u32(sA + (stage * 2 + achunk) * F_A_BYTES)) +
-                                                static_cast<uint64_t>((k4 * 32) >> 4);
-                            const uint64_t db = desc_kmajor_sw128(smem_u32(sB + (stage * 2 + c) * F_B_BYTES)) +
-                                                static_cast<uint64_t>((k4 * 32) >> 4);
-                            const uint32_t idesc = idesc_mx(128, N, 5, 0, k4, k4);
-                            tc_mma_mx(d_tmem, da, db, idesc, sfc + 4 * (fu.g2 ? c : 0), sfc + 8 + 4 * c,
-                                      (kk > 0 || k != kq) ? 1u : 0u);
-                        }
-                        tc_commit(&empty[stage]);
-                    }
-                    __syncwarp();
-                    ++job;
-                    if (++stage == F_STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
+                const bool ok = !fu.g2       ? mma_unit<false, 1>(p, ring, job, w, lane, d_tmem, N, kt1)
+                                : f.kc2 == 2 ? mma_unit<true, 2>(p, ring, job, w, lane, d_tmem, N, kt2)
+                                             : mma_unit<true, 1>(p, ring, job, w, lane, d_tmem, N, kt2);
                 if (!ok) break;
                 if (lane == 0) tc_commit(&accf[acc]);
                 __syncwarp();
@@ -495,6 +700,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 if (acc == 0) acc_phase ^= 1u;
             }
             if (lane == 0) tc_commit(drain);
+            if (lane == 0 && w == 0) FTRACE(6, (long long)globaltimer_ns());
             __syncwarp();
             volatile int never = 0;
             (void)mbar_wait(drain, 0, &never, ws.status, kStTimeout | (1u << (kSiteShift + 4)), kWaitLimitNs);
@@ -505,89 +711,36 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             uint32_t acc_phase = 0;
             const float L = f.swiglu_limit;
             FCursor cur;
+#ifdef BMOE_TRACE
+            bool fused_g2_prev = false;
+#endif
             for (int ui = 0; ui < my_units; ++ui) {
                 const FUnit fu = fused_unit(blockIdx.x + ui * gridDim.x, U1, cur, pl, mt1, mt2);
-                const UnitInfo& cu = fu.u;
                 if (!mbar_wait(&accf[acc], acc_phase, abort_flag, ws.status, kStTimeout | (1u << (kSiteShift + 5)),
                                kWaitLimitNs))
                     break;
                 tc_fence_after();
-                const uint32_t tb =
-                    tmem + (static_cast<uint32_t>(32 * qd) << 16) + static_cast<uint32_t>(acc * F_ACC_COLS);
-                const int feat = cu.m * 128 + 32 * qd + lane;
-                float v[F_NT];
-#pragma unroll
-                for (int j = 0; j < F_NT / 16; ++j) {
-                    const int c0 = 16 * j;
-                    if (c0 < cu.n) {
-                        uint32_t r[F_MW][16];
-#pragma unroll
-                        for (int w = 0; w < F_MW; ++w) tmem_ld16(tb + w * F_NT + c0, r[w]);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            // chains summed in the multi-kernel path's order, from +0 (same bits)
-                            float ga = 0.f, ub = 0.f;
-#pragma unroll
-                            for (int w = 0; w < F_MW; ++w) {
-                                if (!fu.g2 && (w & 1))
-                                    ub += __uint_as_float(r[w][i]);
-                                else
-                                    ga += __uint_as_float(r[w][i]);
-                            }
-                            if (!fu.g2) {
-                                if (ws.g && c0 + i < cu.n) {
-                                    const size_t prow = static_cast<size_t>(cu.row0 + c0 + i);
-                                    ws.g[prow * 2 * I + feat] = ga;
-                                    ws.g[prow * 2 * I + I + feat] = ub;
-                                }
-                                if (L > 0.f) {
-                                    ga = fminf(ga, L);
-                                    ub = fminf(fmaxf(ub, -L), L);
-                                }
-                                v[c0 + i] = ga * (1.0f / (1.0f + expf(-ga))) * ub;
-                            } else {
-                                v[c0 + i] = ga;
-                            }
-                        }
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(&acce[acc]);
+#ifdef BMOE_TRACE
+                if (qd == 0 && lane == 0 && fu.g2 && (ui == 0 || !fused_g2_prev)) FTRACE(8, (long long)globaltimer_ns());
+                fused_g2_prev = fu.g2;
+#endif
+                if (!fu.g2)
+                    epilogue_unit<false>(p, &acce[acc], ws, fu.u, acc, qd, lane, I, H, L);
+                else
+                    epilogue_unit<true>(p, &acce[acc], ws, fu.u, acc, qd, lane, I, H, L);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
-#pragma unroll
-                for (int c = 0; c < F_NT; ++c) {
-                    if (c < cu.n) {
-                        const size_t prow = static_cast<size_t>(cu.row0 + c);
-                        if (!fu.g2) {
-                            const float h = v[c];
-                            const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
-                            int code = static_cast<int>(amax >> 23) - 8;
-                            code = code < 0 ? 0 : code;
-                            const float mul = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
-                            ws.hq[prow * I + feat] = __nv_cvt_float_to_fp8(h * mul, __NV_SATFINITE, __NV_E4M3);
-                            if (lane == 0)
-                                ws.hs[((size_t)cu.g * (I >> 7) + cu.m) * 512 + 16 * (c & 31) + 4 * (c >> 5) + qd] =
-                                    static_cast<uint8_t>(code);
-                        } else {
-                            ws.y[prow * H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(v[c]));
-                        }
-                    }
-                }
-                if (!fu.g2) {
-                    // Release this warp's 32 features of tile g's h rows to the GEMM2 units (TMA reads
-                    // them from any CTA); warps release independently, nobody waits here.
-                    fence_proxy_async_all();
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0) {
-                        __threadfence();
-                        atom_add_release_u32(&ws.ready[cu.g], 1u);
-                    }
-                }
             }
         }
+        if (warp == F_EPI_WARP0 && lane == 0) FTRACE(7, (long long)globaltimer_ns());
+#ifdef BMOE_TRACE
+        if (threadIdx.x == 0) {
+            const int bx = static_cast<int>(blockIdx.x), gx = static_cast<int>(gridDim.x);
+            const int n1 = bx < U1 ? (U1 - 1 - bx) / gx + 1 : 0;
+            FTRACE(11, n1);
+            FTRACE(12, my_units - n1);
+        }
+#endif
         tc_fence_before();
         __syncthreads();
         if (warp == F_MMA_WARP0) {
@@ -596,6 +749,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         }
     }
     if (!grid_sync(bar_count, bar_gen, ws.status, abort_flag)) goto finish;
+    if (threadIdx.x == 0) FTRACE(9, (long long)globaltimer_ns());
 
     // ------------------------------------------------------------------ phase 2: combine
     {
@@ -607,11 +761,13 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         ca.T = T;
         ca.K = K;
         ca.H = H;
-        for (int t = blockIdx.x * (blockDim.x >> 5) + warp; t < T; t += gridDim.x * (blockDim.x >> 5))
-            rows::combine_row(ca, t, lane);
+        const int items = rows::combine_items(ca);
+        for (int it = blockIdx.x * (blockDim.x >> 5) + warp; it < items; it += gridDim.x * (blockDim.x >> 5))
+            rows::combine_item(ca, it, lane);
     }
 finish:
-    return;
+    __syncthreads();
+    if (threadIdx.x == 0) FTRACE(10, (long long)globaltimer_ns());
 }
 
 }  // namespace
@@ -663,3 +819,9 @@ cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaun
 }
 
 }  // namespace bmoe
+
+#ifdef BMOE_TRACE
+extern "C" int bmoe_fused_trace_copy(void* dst, size_t bytes) {
+    return static_cast<int>(cudaMemcpyFromSymbol(dst, g_fused_trace, bytes < sizeof(g_fused_trace) ? bytes : sizeof(g_fused_trace)));
+}
+#endif

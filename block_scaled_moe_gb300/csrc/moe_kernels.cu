@@ -196,9 +196,9 @@ __global__ void __launch_bounds__(256) k_quant_scatter(rows::QuantArgs a, const 
 // ---------------------------------------------------------------- combine
 // One warp per output row (rows::combine_row).
 __global__ void __launch_bounds__(256) k_combine(rows::CombineArgs a) {
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= a.T) return;
-    rows::combine_row(a, t, threadIdx.x & 31);
+    const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (item >= rows::combine_items(a)) return;
+    rows::combine_item(a, item, threadIdx.x & 31);
 }
 
 DispatchArgs dispatch_args(const Geometry& g, const Workspace& ws, const int32_t* ids, int T, const int32_t* nvr) {
@@ -301,7 +301,8 @@ cudaError_t launch_combine(const Geometry& g, const Workspace& ws, const float* 
     a.T = T;
     a.K = g.K;
     a.H = g.H;
-    k_combine<<<(T + 7) / 8, 256, 0, s>>>(a);
+    const int items = T * ((g.H / 8 + rows::kCombineVecs - 1) / rows::kCombineVecs);
+    k_combine<<<(items + 7) / 8, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 
