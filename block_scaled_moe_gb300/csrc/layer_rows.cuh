@@ -31,16 +31,25 @@ struct QuantArgs {
     Workspace ws;
 };
 
-// One warp quantises token row t to MXFP8 (E4M3 codes, one E8M0 scale per 32
-// along H, OCP MX rule: code = max(exponent(amax) - 8, 0), element =
-// RNE_satfinite(x * 2^(127-code))) and writes the codes once per valid slot into
-// the expert's packed rows, the scale into the route tile's 128x4 scale atom
-// (byte 16*(c%32) + 4*(c/32) + kblock%4 for row c of the tile); it also records
-// the packed row each slot combines (yrow, -1 for an invalid slot).
+// One warp quantises segment `seg` (kQuantBlocks 32-element blocks, one per
+// lane) of token row t to MXFP8 (E4M3 codes, one E8M0 scale per 32 along H, OCP
+// MX rule: code = max(exponent(amax) - 8, 0), element = RNE_satfinite(x *
+// 2^(127-code))) and writes the codes once per valid slot into the expert's
+// packed rows, the scale into the route tile's 128x4 scale atom (byte
+// 16*(c%32) + 4*(c/32) + kblock%4 for row c of the tile); segment 0 also
+// records the packed row each slot combines (yrow, -1 for an invalid slot).
 // `rowbase` / `tile_base` may point to global or shared memory.  Routing data
 // written earlier by other CTAs is read with L2-coherent loads.
-__device__ __forceinline__ void quant_scatter_row(const QuantArgs& a, const int32_t* rowbase,
-                                                  const int32_t* tile_base, int t, int nvr, int lane) {
+constexpr int kQuantBlocks = 32;
+
+__device__ __forceinline__ int quant_items(const QuantArgs& a) {
+    return a.T * ((a.H / 32 + kQuantBlocks - 1) / kQuantBlocks);
+}
+
+__device__ __forceinline__ void quant_scatter_seg(const QuantArgs& a, const int32_t* rowbase,
+                                                  const int32_t* tile_base, int item, int nvr, int lane) {
+    const int segs = (a.H / 32 + kQuantBlocks - 1) / kQuantBlocks;
+    const int t = item / segs, seg = item - t * segs;
     const int K = a.K;
     int p = -1, gt = 0, c = 0;
     bool valid = false;
@@ -63,7 +72,7 @@ __device__ __forceinline__ void quant_scatter_row(const QuantArgs& a, const int3
             gt = tile_base[e] + i / a.NT;
             c = i % a.NT;
         }
-        a.ws.yrow[(size_t)t * K + lane] = valid ? p : -1;
+        if (seg == 0) a.ws.yrow[(size_t)t * K + lane] = valid ? p : -1;
     }
     if (t >= nvr) return;  // warp-uniform
     const unsigned vmask = __ballot_sync(kFull, valid);
@@ -76,7 +85,7 @@ __device__ __forceinline__ void quant_scatter_row(const QuantArgs& a, const int3
     }
     const int H = a.H, nblk = H >> 5, ktiles = H >> 7;
     const uint16_t* xrow = a.x + (size_t)t * H;
-    for (int blk = lane; blk < nblk; blk += 32) {
+    for (int blk = seg * kQuantBlocks + lane; blk < min(nblk, (seg + 1) * kQuantBlocks); blk += 32) {
         const uint4* src = reinterpret_cast<const uint4*>(xrow + blk * 32);
         float f[32];
 #pragma unroll

@@ -29,12 +29,12 @@
 #include "ptx.cuh"
 
 #ifdef BMOE_TRACE
-// Phase trace (tracing builds only): per CTA 16 int64 slots of globaltimer ns
+// Phase trace (tracing builds only): per CTA 32 int64 slots of globaltimer ns
 // stamps and counters, read back with bmoe_fused_trace_copy.
-__device__ long long g_fused_trace[1024 * 16];
+__device__ long long g_fused_trace[1024 * 32];
 #define FTRACE(ev, val)                                              \
     do {                                                             \
-        if (blockIdx.x < 1024) g_fused_trace[blockIdx.x * 16 + (ev)] = (val); \
+        if (blockIdx.x < 1024) g_fused_trace[blockIdx.x * 32 + (ev)] = (val); \
     } while (0)
 #else
 #define FTRACE(ev, val) \
@@ -49,8 +49,8 @@ namespace {
 constexpr int F_NT = 32;                                    // route tile width
 constexpr int F_MW = 4;                                     // accumulator chains = MMA-issuing warps
 constexpr int F_EW = 4;                                     // epilogue warps (one per TMEM lane quadrant)
-constexpr int F_THREADS = 32 * (2 + F_MW + F_EW);
 constexpr int F_MMA_WARP0 = 2, F_EPI_WARP0 = 2 + F_MW;
+constexpr int F_THREADS = 32 * (2 + F_MW + F_EW);
 constexpr int F_A_BYTES = 128 * 128;                        // one 128x128 FP4 chunk in smem
 constexpr int F_A_TX = 128 * 128 / 2;                       // ... and its transaction bytes
 constexpr int F_B_BYTES = F_NT * 128;                       // one row chunk
@@ -60,8 +60,8 @@ constexpr int F_TAB_BYTES = 4 * (3 * F_TAB_E + 4);
 constexpr int F_SCR_INTS = 2 * F_TAB_E + 64;                // phase-0 scratch, inside the (idle) stage ring
 constexpr int F_STAGES = (220 * 1024 - F_TAB_BYTES) / F_STAGE_BYTES;
 constexpr int F_ACC_COLS = F_MW * F_NT;
-constexpr int F_SF_SLOT = 16;                               // [A atom 0|A atom 1|B atom 0|B atom 1]
-constexpr int F_SF_BASE = 512 - F_MW * 2 * F_SF_SLOT;
+constexpr int F_SF_SLOT = 8;                                // [weight atom | row atom] of the chain's chunk
+constexpr int F_SF_BASE = 512 - F_MW * 2 * F_SF_SLOT;       // two slots per chain (alternating stages)
 constexpr int F_NUM_ACC = 2;
 constexpr int F_BAR_BYTES = (2 * F_STAGES + 2 * 2 + 1) * 8 + 16;
 constexpr int F_SMEM = 1024 + F_STAGES * F_STAGE_BYTES + F_TAB_BYTES + F_BAR_BYTES;
@@ -190,11 +190,20 @@ struct Ring {
 template <bool G2, int KC>
 __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued, const CUtensorMap* tw,
                                              const CUtensorMap* tb, int wrow, int up_off, int row0,
-                                             const uint8_t* bsf, int kt, uint64_t pol_w, uint64_t pol_b) {
+                                             const uint8_t* bsf, int kt, uint64_t pol_w, uint64_t pol_b,
+                                             long long& wait_ns) {
     for (int kk = 0; kk < kt; ++kk) {
+#ifdef BMOE_TRACE
+        const long long tw0 = (long long)globaltimer_ns();
+#endif
         if (!mbar_wait(&p.empty[r.stage], r.phase ^ 1u, p.abort_flag, p.status, kStTimeout | (1u << (kSiteShift + 0)),
                        kWaitLimitNs))
             return false;
+#ifdef BMOE_TRACE
+        wait_ns += (long long)globaltimer_ns() - tw0;
+#else
+        (void)wait_ns;
+#endif
         uint64_t* fb = &p.full[r.stage];
         uint8_t* a0 = p.sA + (r.stage * 2) * F_A_BYTES;
         uint8_t* b0 = p.sB + (r.stage * 2) * F_B_BYTES;
@@ -222,38 +231,53 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
 }
 
 // MMA issue of one unit by chain w (its warp's lane 0).  GEMM1: chain w multiplies operand
-// w & 1 (gate / up) over the K-steps k with k % 2 == w >> 1; GEMM2: the K-steps k with
-// k % 4 == w of the stage's KC chunks.  Each chain copies its own scale atoms to TMEM
-// (two slots, alternating stages).
+// w & 1 (gate / up) over the K-steps k with k % 2 == w >> 1; GEMM2: chain w takes the KC
+// consecutive K-steps [w*KC, w*KC + KC) of the stage (k = 4 * chunk + step in chunk), all in
+// chunk w*KC/4.  Either way a chain reads one weight atom and one row atom per stage, which
+// it copies to its own TMEM slot (two slots, alternating stages).
 template <bool G2, int KC>
 __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w, int lane, uint32_t d_tmem, int N,
-                                         int kt) {
-    constexpr int KS = G2 ? F_MW : F_MW / 2;
-    constexpr int NCH = G2 ? KC : 1;
-    const int op = G2 ? 0 : (w & 1);
-    const int kq = G2 ? w : (w >> 1);
+                                         int kt, long long& wait_ns) {
+    static_assert(F_MW == 4 && (KC == 1 || KC == 2), "each chain's K-steps lie in one chunk");
+    const int ach = G2 ? (w * KC) >> 2 : (w & 1);  // weight chunk (GEMM1: operand) of this chain
+    const int bch = G2 ? (w * KC) >> 2 : 0;        // row chunk of this chain
     for (int kk = 0; kk < kt; ++kk) {
+#ifdef BMOE_TRACE
+        const long long tw0 = (long long)globaltimer_ns();
+#endif
         if (!mbar_wait(&p.full[r.stage], r.phase, p.abort_flag, p.status, kStTimeout | (1u << (kSiteShift + 3)),
                        kWaitLimitNs))
             return false;
+#ifdef BMOE_TRACE
+        wait_ns += (long long)globaltimer_ns() - tw0;
+#else
+        (void)wait_ns;
+#endif
         tc_fence_after();
         if (lane == 0) {
-            const uint32_t sfc = p.tmem + static_cast<uint32_t>(F_SF_BASE + (w * 2 + (job & 1)) * F_SF_SLOT);
+            const uint32_t sfa = p.tmem + static_cast<uint32_t>(F_SF_BASE + (w * 2 + (job & 1)) * F_SF_SLOT);
+            const uint32_t sfb = sfa + 4;
+            tc_cp_32x128b_x4(sfa, desc_sf_atom(smem_u32(p.sSFA + (r.stage * 2 + ach) * 512)));
+            tc_cp_32x128b_x4(sfb, desc_sf_atom(smem_u32(p.sSFB + (r.stage * 2 + bch) * 512)));
+            const uint64_t da0 = desc_kmajor_sw128(smem_u32(p.sA + (r.stage * 2 + ach) * F_A_BYTES));
+            const uint64_t db0 = desc_kmajor_sw128(smem_u32(p.sB + (r.stage * 2 + bch) * F_B_BYTES));
+            if constexpr (!G2) {
+                const int kq = w >> 1;
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                tc_cp_32x128b_x4(sfc + 4 * c, desc_sf_atom(smem_u32(p.sSFA + (r.stage * 2 + (G2 ? c : op)) * 512)));
-                tc_cp_32x128b_x4(sfc + 8 + 4 * c, desc_sf_atom(smem_u32(p.sSFB + (r.stage * 2 + c) * 512)));
-            }
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    if ((k4 & 1) != kq) continue;
+                    tc_mma_mx(d_tmem, da0 + static_cast<uint64_t>((k4 * 32) >> 4),
+                              db0 + static_cast<uint64_t>((k4 * 32) >> 4), idesc_mx(128, N, 5, 0, k4, k4), sfa, sfb,
+                              (kk > 0 || k4 != kq) ? 1u : 0u);
+                }
+            } else {
 #pragma unroll
-            for (int k = 0; k < 4 * NCH; ++k) {
-                if (k % KS != kq) continue;
-                const int c = k >> 2, k4 = k & 3;
-                const uint64_t da = desc_kmajor_sw128(smem_u32(p.sA + (r.stage * 2 + (G2 ? c : op)) * F_A_BYTES)) +
-                                    static_cast<uint64_t>((k4 * 32) >> 4);
-                const uint64_t db = desc_kmajor_sw128(smem_u32(p.sB + (r.stage * 2 + c) * F_B_BYTES)) +
-                                    static_cast<uint64_t>((k4 * 32) >> 4);
-                tc_mma_mx(d_tmem, da, db, idesc_mx(128, N, 5, 0, k4, k4), sfc + 4 * c, sfc + 8 + 4 * c,
-                          (kk > 0 || k != kq) ? 1u : 0u);
+                for (int j = 0; j < KC; ++j) {
+                    const int k4 = (w * KC + j) & 3;
+                    tc_mma_mx(d_tmem, da0 + static_cast<uint64_t>((k4 * 32) >> 4),
+                              db0 + static_cast<uint64_t>((k4 * 32) >> 4), idesc_mx(128, N, 5, 0, k4, k4), sfa, sfb,
+                              (kk > 0 || j > 0) ? 1u : 0u);
+                }
             }
             tc_commit(&p.empty[r.stage]);
         }
@@ -386,6 +410,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         // fixed-slot (vLLM PR #61262): slot (e, t), occupancy bits, no prepare step
         for (int i = gtid; i < E * q.words; i += gstride) ws.occ[i] = 0;
         if (!grid_sync(bar_count, bar_gen, ws.status, abort_flag)) goto finish;
+        if (threadIdx.x == 0) FTRACE(22, (long long)globaltimer_ns());
         for (int s = gtid; s < T * K; s += gstride) {
             const int t = s / K, e = q.ids[s];
             if (t < nvr && e >= E) atomicOr(ws.status, kStBadId);
@@ -397,6 +422,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             }
         }
         if (!grid_sync(bar_count, bar_gen, ws.status, abort_flag)) goto finish;
+        if (threadIdx.x == 0) FTRACE(23, (long long)globaltimer_ns());
         for (int e = threadIdx.x; e < E; e += blockDim.x) {
             int c = 0;
             for (int w = 0; w < q.words; ++w) c += __popc(__ldcg(&ws.occ[(size_t)e * q.words + w]));
@@ -478,10 +504,15 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             if (e < E) ws.counts[e] = t_cnt[e];
         }
     }
-    // quantise + scatter: one warp per row
-    for (int t = blockIdx.x * (blockDim.x >> 5) + warp; t < T; t += gridDim.x * (blockDim.x >> 5))
-        rows::quant_scatter_row(q, t_row, t_tile, t, nvr, lane);
+    if (threadIdx.x == 0) FTRACE(24, (long long)globaltimer_ns());
+    // quantise + scatter: one warp per row segment
+    {
+        const int items = rows::quant_items(q);
+        for (int it = blockIdx.x * (blockDim.x >> 5) + warp; it < items; it += gridDim.x * (blockDim.x >> 5))
+            rows::quant_scatter_seg(q, t_row, t_tile, it, nvr, lane);
+    }
     fence_proxy_async_all();  // the packed rows and scale atoms are read by TMA / bulk copies
+    if (threadIdx.x == 0) FTRACE(25, (long long)globaltimer_ns());
     if (!grid_sync(bar_count, bar_gen, ws.status, abort_flag)) goto finish;
 
     // ------------------------------------------------------------------ phase 1: GEMM1 + GEMM2
@@ -538,13 +569,14 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 long issued = 0;
                 bool ok = true;
                 FCursor cur;
+                long long ew1 = 0, ew2 = 0;  // empty-stage wait ns in GEMM1 / GEMM2 units (tracing builds)
                 fence_proxy_async_all();  // phase-0 rows and scale atoms are read through the async proxy
                 for (int ui = 0; ui < my_units && ok; ++ui) {
                     const FUnit fu = fused_unit(blockIdx.x + ui * gridDim.x, U1, cur, pl, mt1, mt2);
                     const UnitInfo& cu = fu.u;
                     if (!fu.g2) {
                         ok = produce_unit<false, 1>(p, ring, issued, &tm_w13, &tm_aq, cu.e * 2 * I + cu.m * 128, I,
-                                                    cu.row0, ws.as + (size_t)cu.g * kt1 * 512, kt1, pol_w, pol_b);
+                                                    cu.row0, ws.as + (size_t)cu.g * kt1 * 512, kt1, pol_w, pol_b, ew1);
                         continue;
                     }
                     // the h rows of tile g are complete once all epilogue warps of its I/128 GEMM1
@@ -575,13 +607,15 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                     const int wrow = cu.e * H + cu.m * 128;
                     const uint8_t* bsf = ws.hs + (size_t)cu.g * ktot2 * 512;
                     ok = f.kc2 == 2 ? produce_unit<true, 2>(p, ring, issued, &tm_w2, &tm_hq, wrow, 0, cu.row0, bsf,
-                                                            kt2, pol_w, pol_b)
+                                                            kt2, pol_w, pol_b, ew2)
                                     : produce_unit<true, 1>(p, ring, issued, &tm_w2, &tm_hq, wrow, 0, cu.row0, bsf,
-                                                            kt2, pol_w, pol_b);
+                                                            kt2, pol_w, pol_b, ew2);
                 }
 #ifdef BMOE_TRACE
                 FTRACE(4, wait_ns);
                 FTRACE(5, (long long)globaltimer_ns());
+                FTRACE(16, ew1);
+                FTRACE(17, ew2);
 #endif
                 drain_stages<F_STAGES>(full, ring.stage, ring.phase, issued, ws.status);
             }
@@ -682,17 +716,27 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             uint32_t acc_phase = 0;
             long job = 0;
             FCursor cur;
+            long long fw1 = 0, fw2 = 0;  // stage-ready wait ns (tracing builds)
+#ifdef BMOE_TRACE
+            long long aw1 = 0, aw2 = 0;  // accumulator wait ns
+#endif
             for (int ui = 0; ui < my_units; ++ui) {
                 const FUnit fu = fused_unit(blockIdx.x + ui * gridDim.x, U1, cur, pl, mt1, mt2);
                 const int N = (fu.u.n + 15) & ~15;
+#ifdef BMOE_TRACE
+                const long long ta0 = (long long)globaltimer_ns();
+#endif
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * F_ACC_COLS + w * F_NT);
                 if (!mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, ws.status,
                                kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs))
                     break;
+#ifdef BMOE_TRACE
+                (fu.g2 ? aw2 : aw1) += (long long)globaltimer_ns() - ta0;
+#endif
                 tc_fence_after();
-                const bool ok = !fu.g2       ? mma_unit<false, 1>(p, ring, job, w, lane, d_tmem, N, kt1)
-                                : f.kc2 == 2 ? mma_unit<true, 2>(p, ring, job, w, lane, d_tmem, N, kt2)
-                                             : mma_unit<true, 1>(p, ring, job, w, lane, d_tmem, N, kt2);
+                const bool ok = !fu.g2       ? mma_unit<false, 1>(p, ring, job, w, lane, d_tmem, N, kt1, fw1)
+                                : f.kc2 == 2 ? mma_unit<true, 2>(p, ring, job, w, lane, d_tmem, N, kt2, fw2)
+                                             : mma_unit<true, 1>(p, ring, job, w, lane, d_tmem, N, kt2, fw2);
                 if (!ok) break;
                 if (lane == 0) tc_commit(&accf[acc]);
                 __syncwarp();
@@ -700,7 +744,13 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 if (acc == 0) acc_phase ^= 1u;
             }
             if (lane == 0) tc_commit(drain);
-            if (lane == 0 && w == 0) FTRACE(6, (long long)globaltimer_ns());
+            if (lane == 0 && w == 0) {
+                FTRACE(6, (long long)globaltimer_ns());
+                FTRACE(18, fw1);
+                FTRACE(19, fw2);
+                FTRACE(20, aw1);
+                FTRACE(21, aw2);
+            }
             __syncwarp();
             volatile int never = 0;
             (void)mbar_wait(drain, 0, &never, ws.status, kStTimeout | (1u << (kSiteShift + 4)), kWaitLimitNs);

@@ -280,20 +280,26 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
                     if (wi == 0) trace(a, 2, job);
 #pragma unroll
                     for (int w = wi; w < MW; w += NI) {
-                        const int op = G1 ? (w & 1) : 0;   // GEMM1: 0 gate, 1 up
-                        const int kq = G1 ? (w >> 1) : w;  // chain w takes the K-steps k with k % KS == kq
+                        // GEMM1: chain w multiplies operand w & 1 (0 gate, 1 up) over the K-steps k with
+                        // k % KS == w >> 1; GEMM2: chain w takes the G2S consecutive K-steps from w * G2S
+                        // (k = 4 * chunk + step in chunk) and needs only the atoms of their chunks.
+                        constexpr int G2S = 4 * KC / MW;
+                        const int op = G1 ? (w & 1) : 0;
+                        const int kfirst = G1 ? (w >> 1) : w * G2S;
+                        const int c_lo = G1 ? 0 : (w * G2S) >> 2, c_hi = G1 ? KC - 1 : (w * G2S + G2S - 1) >> 2;
                         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * C::ACC_COLS + w * NT);
                         const uint32_t sfc = tmem + static_cast<uint32_t>(
                                                         C::SF_BASE + (w * C::SF_SLOTS + (job & 1)) * C::SF_SLOT_COLS);
 #pragma unroll
                         for (int c = 0; c < KC; ++c) {
+                            if (c < c_lo || c > c_hi) continue;
                             tc_cp_32x128b_x4(sfc + 4 * c,
                                              desc_sf_atom(smem_u32(sSFA + ((stage * NA + op) * KC + c) * 512)));
                             tc_cp_32x128b_x4(sfc + 4 * KC + 4 * c, desc_sf_atom(smem_u32(sSFB + (stage * KC + c) * 512)));
                         }
 #pragma unroll
                         for (int k = 0; k < 4 * KC; ++k) {
-                            if (k % KS != kq) continue;
+                            if (G1 ? (k % KS != kfirst) : (k / G2S != w)) continue;
                             const int c = k >> 2, k4 = k & 3;
                             const uint64_t da =
                                 desc_kmajor_sw128(smem_u32(sA + ((stage * NA + op) * KC + c) * C::A_BYTES)) +
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
                                                 static_cast<uint64_t>((k4 * 32) >> 4);
                             const uint32_t idesc = idesc_mx(128, N, 5, 0, k4, k4);
                             tc_mma_mx(d_tmem, da, db, idesc, sfc + 4 * c, sfc + 4 * KC + 4 * c,
-                                      (kk > 0 || k != kq) ? 1u : 0u);
+                                      (kk > 0 || k != kfirst) ? 1u : 0u);
                         }
                     }
                     tc_commit(&empty[stage]);

@@ -188,9 +188,9 @@ __global__ void __launch_bounds__(32) k_compact_rank(DispatchArgs a) {
 // One warp per token row (rows::quant_scatter_row).
 __global__ void __launch_bounds__(256) k_quant_scatter(rows::QuantArgs a, const int32_t* nvr_ptr) {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= a.T) return;
-    rows::quant_scatter_row(a, a.ws.rowbase, a.ws.tile_base, t, rows::read_nvr(nvr_ptr, a.T), lane);
+    const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (item >= rows::quant_items(a)) return;
+    rows::quant_scatter_seg(a, a.ws.rowbase, a.ws.tile_base, item, rows::read_nvr(nvr_ptr, a.T), lane);
 }
 
 // ---------------------------------------------------------------- combine
@@ -287,7 +287,8 @@ cudaError_t launch_quant_scatter(const Geometry& g, const Workspace& ws, const u
     a.NT = g.NT;
     a.scheme = g.scheme;
     a.ws = ws;
-    k_quant_scatter<<<(T + 7) / 8, 256, 0, s>>>(a, nvr);
+    const int items = T * ((g.H / 32 + rows::kQuantBlocks - 1) / rows::kQuantBlocks);
+    k_quant_scatter<<<(items + 7) / 8, 256, 0, s>>>(a, nvr);
     return cudaGetLastError();
 }
 
