@@ -184,14 +184,15 @@ struct Ring {
     }
 };
 
-// TMA producer, one unit of kt K stages.  GEMM1 (G2 false): gate and up chunks (rows wrow and
-// wrow + up_off), one row chunk and its scale atom per stage; GEMM2: KC (W2 chunk, h chunk)
-// pairs and KC h-scale atoms per stage.  The row-scale atoms of the unit start at bsf.
+// TMA producer, one unit of kt K stages.  GEMM1 (G2 false): the gate and up chunks of weight
+// tile m of expert e (one box of the W13 pair view, coordinates (k, m*128, 0, e)), one row
+// chunk and its scale atom per stage; GEMM2: KC (W2 chunk, h chunk) pairs and KC h-scale
+// atoms per stage (W2 rows from wrow).  The row-scale atoms of the unit start at bsf.
 template <bool G2, int KC>
 __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued, const CUtensorMap* tw,
-                                             const CUtensorMap* tb, int wrow, int up_off, int row0,
+                                             const CUtensorMap* tb, int wrow, int e, int row0,
                                              const uint8_t* bsf, int kt, uint64_t pol_w, uint64_t pol_b,
-                                             long long& wait_ns) {
+                                             long long& wait_ns, long long& issue_ns) {
     for (int kk = 0; kk < kt; ++kk) {
 #ifdef BMOE_TRACE
         const long long tw0 = (long long)globaltimer_ns();
@@ -200,17 +201,18 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
                        kWaitLimitNs))
             return false;
 #ifdef BMOE_TRACE
-        wait_ns += (long long)globaltimer_ns() - tw0;
+        const long long tw1 = (long long)globaltimer_ns();
+        wait_ns += tw1 - tw0;
 #else
         (void)wait_ns;
+        (void)issue_ns;
 #endif
         uint64_t* fb = &p.full[r.stage];
         uint8_t* a0 = p.sA + (r.stage * 2) * F_A_BYTES;
         uint8_t* b0 = p.sB + (r.stage * 2) * F_B_BYTES;
         if constexpr (!G2) {
             mbar_expect_tx(fb, 2 * F_A_TX + F_B_BYTES + 512);
-            tma_load_2d(a0, tw, fb, kk * 128, wrow, pol_w);
-            tma_load_2d(a0 + F_A_BYTES, tw, fb, kk * 128, wrow + up_off, pol_w);
+            tma_load_4d(a0, tw, fb, kk * 128, wrow, 0, e, pol_w);
             tma_load_2d(b0, tb, fb, kk * 128, row0, pol_b);
             bulk_load(p.sSFB + (r.stage * 2) * 512, bsf + static_cast<size_t>(kk) * 512, 512, fb);
         } else {
@@ -224,6 +226,9 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
             bulk_load(p.sSFB + (r.stage * 2) * 512, bsf + static_cast<size_t>(kk) * KC * 512, KC * 512, fb);
         }
         mbar_arrive(fb);
+#ifdef BMOE_TRACE
+        issue_ns += (long long)globaltimer_ns() - tw1;
+#endif
         ++issued;
         r.next();
     }
@@ -237,7 +242,7 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
 // it copies to its own TMEM slot (two slots, alternating stages).
 template <bool G2, int KC>
 __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w, int lane, uint32_t d_tmem, int N,
-                                         int kt, long long& wait_ns) {
+                                         int kt, long long& wait_ns, long long& issue_ns) {
     static_assert(F_MW == 4 && (KC == 1 || KC == 2), "each chain's K-steps lie in one chunk");
     const int ach = G2 ? (w * KC) >> 2 : (w & 1);  // weight chunk (GEMM1: operand) of this chain
     const int bch = G2 ? (w * KC) >> 2 : 0;        // row chunk of this chain
@@ -249,9 +254,11 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
                        kWaitLimitNs))
             return false;
 #ifdef BMOE_TRACE
-        wait_ns += (long long)globaltimer_ns() - tw0;
+        const long long tw1 = (long long)globaltimer_ns();
+        wait_ns += tw1 - tw0;
 #else
         (void)wait_ns;
+        (void)issue_ns;
 #endif
         tc_fence_after();
         if (lane == 0) {
@@ -280,6 +287,9 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
                 }
             }
             tc_commit(&p.empty[r.stage]);
+#ifdef BMOE_TRACE
+            issue_ns += (long long)globaltimer_ns() - tw1;
+#endif
         }
         __syncwarp();
         ++job;
@@ -369,7 +379,7 @@ __device__ __forceinline__ void epilogue_unit(const P1& p, uint64_t* acce_b, con
 }
 
 __global__ void __launch_bounds__(F_THREADS, 1)
-    k_fused(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_aq,
+    k_fused(const __grid_constant__ CUtensorMap tm_w13p, const __grid_constant__ CUtensorMap tm_aq,
             const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_hq, const FusedArgs f) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -570,13 +580,14 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 bool ok = true;
                 FCursor cur;
                 long long ew1 = 0, ew2 = 0;  // empty-stage wait ns in GEMM1 / GEMM2 units (tracing builds)
+                long long pi1 = 0, pi2 = 0;  // issue ns
                 fence_proxy_async_all();  // phase-0 rows and scale atoms are read through the async proxy
                 for (int ui = 0; ui < my_units && ok; ++ui) {
                     const FUnit fu = fused_unit(blockIdx.x + ui * gridDim.x, U1, cur, pl, mt1, mt2);
                     const UnitInfo& cu = fu.u;
                     if (!fu.g2) {
-                        ok = produce_unit<false, 1>(p, ring, issued, &tm_w13, &tm_aq, cu.e * 2 * I + cu.m * 128, I,
-                                                    cu.row0, ws.as + (size_t)cu.g * kt1 * 512, kt1, pol_w, pol_b, ew1);
+                        ok = produce_unit<false, 1>(p, ring, issued, &tm_w13p, &tm_aq, cu.m * 128, cu.e, cu.row0,
+                                                    ws.as + (size_t)cu.g * kt1 * 512, kt1, pol_w, pol_b, ew1, pi1);
                         continue;
                     }
                     // the h rows of tile g are complete once all epilogue warps of its I/128 GEMM1
@@ -607,15 +618,17 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                     const int wrow = cu.e * H + cu.m * 128;
                     const uint8_t* bsf = ws.hs + (size_t)cu.g * ktot2 * 512;
                     ok = f.kc2 == 2 ? produce_unit<true, 2>(p, ring, issued, &tm_w2, &tm_hq, wrow, 0, cu.row0, bsf,
-                                                            kt2, pol_w, pol_b, ew2)
+                                                            kt2, pol_w, pol_b, ew2, pi2)
                                     : produce_unit<true, 1>(p, ring, issued, &tm_w2, &tm_hq, wrow, 0, cu.row0, bsf,
-                                                            kt2, pol_w, pol_b, ew2);
+                                                            kt2, pol_w, pol_b, ew2, pi2);
                 }
 #ifdef BMOE_TRACE
                 FTRACE(4, wait_ns);
                 FTRACE(5, (long long)globaltimer_ns());
                 FTRACE(16, ew1);
                 FTRACE(17, ew2);
+                FTRACE(28, pi1);
+                FTRACE(29, pi2);
 #endif
                 drain_stages<F_STAGES>(full, ring.stage, ring.phase, issued, ws.status);
             }
@@ -717,6 +730,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             long job = 0;
             FCursor cur;
             long long fw1 = 0, fw2 = 0;  // stage-ready wait ns (tracing builds)
+            long long mi1 = 0, mi2 = 0;  // issue ns
 #ifdef BMOE_TRACE
             long long aw1 = 0, aw2 = 0;  // accumulator wait ns
 #endif
@@ -734,9 +748,9 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 (fu.g2 ? aw2 : aw1) += (long long)globaltimer_ns() - ta0;
 #endif
                 tc_fence_after();
-                const bool ok = !fu.g2       ? mma_unit<false, 1>(p, ring, job, w, lane, d_tmem, N, kt1, fw1)
-                                : f.kc2 == 2 ? mma_unit<true, 2>(p, ring, job, w, lane, d_tmem, N, kt2, fw2)
-                                             : mma_unit<true, 1>(p, ring, job, w, lane, d_tmem, N, kt2, fw2);
+                const bool ok = !fu.g2       ? mma_unit<false, 1>(p, ring, job, w, lane, d_tmem, N, kt1, fw1, mi1)
+                                : f.kc2 == 2 ? mma_unit<true, 2>(p, ring, job, w, lane, d_tmem, N, kt2, fw2, mi2)
+                                             : mma_unit<true, 1>(p, ring, job, w, lane, d_tmem, N, kt2, fw2, mi2);
                 if (!ok) break;
                 if (lane == 0) tc_commit(&accf[acc]);
                 __syncwarp();
@@ -750,6 +764,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 FTRACE(19, fw2);
                 FTRACE(20, aw1);
                 FTRACE(21, aw2);
+                FTRACE(30, mi1);
+                FTRACE(31, mi2);
             }
             __syncwarp();
             volatile int never = 0;
@@ -830,7 +846,7 @@ cudaError_t fused_set_attributes() {
     return cudaFuncSetAttribute(k_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
 }
 
-cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaunch& fl, const CUtensorMap* tm_w13,
+cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaunch& fl, const CUtensorMap* tm_w13p,
                          const CUtensorMap* tm_aq, const CUtensorMap* tm_w2, const CUtensorMap* tm_hq, int grid,
                          cudaStream_t s) {
     FusedArgs f{};
@@ -865,7 +881,7 @@ cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaun
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_fused, *tm_w13, *tm_aq, *tm_w2, *tm_hq, f);
+    return cudaLaunchKernelEx(&cfg, k_fused, *tm_w13p, *tm_aq, *tm_w2, *tm_hq, f);
 }
 
 }  // namespace bmoe

@@ -113,7 +113,8 @@ struct FusedLaunch {
     int T;
 };
 bool fused_supported(const Geometry& g);
-cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaunch& f, const CUtensorMap* tm_w13,
+// tm_w13p: the W13 gate/up pair view (K, row, half, expert), box {128, 128, 2, 1}.
+cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaunch& f, const CUtensorMap* tm_w13p,
                          const CUtensorMap* tm_aq, const CUtensorMap* tm_w2, const CUtensorMap* tm_hq, int grid,
                          cudaStream_t s);
 cudaError_t fused_set_attributes();
