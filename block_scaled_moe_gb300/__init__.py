@@ -80,6 +80,10 @@ def load(path: Optional[str] = None):
         lib.moe_profile_read.restype = i32
         lib.moe_last_path.argtypes = [vp]
         lib.moe_last_path.restype = i32
+        lib.moe_bind_layer.argtypes = [vp, i32, vp, vp, vp, vp]
+        lib.moe_bind_layer.restype = i32
+        lib.moe_select_layer.argtypes = [vp, i32]
+        lib.moe_select_layer.restype = i32
         lib.moe_dispatch_compact_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         lib.moe_dispatch_compact_noalloc.restype = i32
         _lib = lib
@@ -111,6 +115,14 @@ def moe_create(H: int, I: int, E: int, topk: int, capacity: int):
 
 def moe_bind_weights(h, w13_fp4: int, w13_sf: int, w2_fp4: int, w2_sf: int):
     _check(h, load().moe_bind_weights(h, w13_fp4, w13_sf, w2_fp4, w2_sf))
+
+
+def moe_bind_layer(h, slot: int, w13_fp4: int, w13_sf: int, w2_fp4: int, w2_sf: int):
+    _check(h, load().moe_bind_layer(h, slot, w13_fp4, w13_sf, w2_fp4, w2_sf))
+
+
+def moe_select_layer(h, slot: int):
+    _check(h, load().moe_select_layer(h, slot))
 
 
 def moe_forward(h, x: int, topk_ids: int, topk_weights: int, num_valid_rows: Optional[int], out: int, T: int,
@@ -184,7 +196,8 @@ class BlockScaledMoE:
 
     def __init__(self, H: int, I: int, E: int, topk: int, capacity: int, *, dispatch: Optional[str] = None,
                  swiglu_limit: float = 0.0, route_tile: int = 0, debug: bool = False,
-                 fixed_slot_max: Optional[int] = None, workspace=None, path: Optional[str] = None):
+                 fixed_slot_max: Optional[int] = None, workspace=None, path: Optional[str] = None,
+                 w13_layout: str = "concat", layer_slots: int = 1):
         self.H, self.I, self.E, self.topk, self.capacity = H, I, E, topk, capacity
         self.h = moe_create(H, I, E, topk, capacity)
         try:
@@ -199,6 +212,10 @@ class BlockScaledMoE:
             if debug:
                 moe_set_option(self.h, MOE_OPT_DEBUG_CAPTURE, 1)
             moe_set_option(self.h, MOE_OPT_SWIGLU_LIMIT, swiglu_limit)
+            moe_set_option(self.h, MOE_OPT_W13_LAYOUT,
+                           {"concat": MOE_W13_CONCAT, "interleaved": MOE_W13_INTERLEAVED}[w13_layout])
+            if layer_slots != 1:
+                moe_set_option(self.h, MOE_OPT_LAYER_SLOTS, layer_slots)
             if path is not None:
                 moe_set_option(self.h, MOE_OPT_PATH, {"auto": MOE_PATH_AUTO, "fused": MOE_PATH_FUSED,
                                                       "multi": MOE_PATH_MULTI}[path])
@@ -208,7 +225,7 @@ class BlockScaledMoE:
             moe_destroy(self.h)
             self.h = None
             raise
-        self._weights = None
+        self._weights = {}
 
     def close(self):
         if getattr(self, "h", None) is not None:
@@ -256,15 +273,34 @@ class BlockScaledMoE:
             raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
         return t.data_ptr()
 
-    def bind_weights(self, w13, w13_sf, w2, w2_sf):
+    def _weight_ptrs(self, w13, w13_sf, w2, w2_sf):
         import torch
         E, H, I = self.E, self.H, self.I
         fp4 = (torch.uint8,) + ((torch.float4_e2m1fn_x2,) if hasattr(torch, "float4_e2m1fn_x2") else ())
         sf = (torch.uint8,) + ((torch.float8_e8m0fnu,) if hasattr(torch, "float8_e8m0fnu") else ())
-        ptrs = (self._dev(w13, "w13", (E, 2 * I, H // 2), fp4), self._dev(w13_sf, "w13_sf", (E, 2 * I, H // 32), sf),
+        return (self._dev(w13, "w13", (E, 2 * I, H // 2), fp4), self._dev(w13_sf, "w13_sf", (E, 2 * I, H // 32), sf),
                 self._dev(w2, "w2", (E, H, I // 2), fp4), self._dev(w2_sf, "w2_sf", (E, H, I // 32), sf))
+
+    @property
+    def layer(self) -> int:
+        return int(moe_get_option(self.h, MOE_OPT_LAYER))
+
+    def set_w13_layout(self, layout: str):
+        """Row order assumed by the next bind: "concat" or "interleaved"."""
+        moe_set_option(self.h, MOE_OPT_W13_LAYOUT, {"concat": MOE_W13_CONCAT, "interleaved": MOE_W13_INTERLEAVED}[layout])
+
+    def bind_weights(self, w13, w13_sf, w2, w2_sf):
+        ptrs = self._weight_ptrs(w13, w13_sf, w2, w2_sf)
         moe_bind_weights(self.h, *ptrs)
-        self._weights = (w13, w13_sf, w2, w2_sf)  # keep caller tensors alive while bound
+        self._weights[self.layer] = (w13, w13_sf, w2, w2_sf)  # keep caller tensors alive while bound
+
+    def bind_layer(self, slot: int, w13, w13_sf, w2, w2_sf):
+        ptrs = self._weight_ptrs(w13, w13_sf, w2, w2_sf)
+        moe_bind_layer(self.h, slot, *ptrs)
+        self._weights[slot] = (w13, w13_sf, w2, w2_sf)
+
+    def select_layer(self, slot: int):
+        moe_select_layer(self.h, slot)
 
     def forward(self, x, topk_ids, topk_weights, num_valid_rows=None, out=None, stream=None):
         import torch

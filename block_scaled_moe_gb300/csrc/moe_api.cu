@@ -26,6 +26,18 @@ long long* bmoe_trace_buffer = nullptr;  // device pointer of the pipeline trace
 }
 #endif
 
+// One bound layer: the caller's weight buffers (not owned) and their tensor maps.
+struct Binding {
+    bool bound = false;
+    int w13_layout = MOE_W13_CONCAT;
+    const uint8_t* w13 = nullptr;
+    const uint8_t* w13s = nullptr;
+    const uint8_t* w2 = nullptr;
+    const uint8_t* w2s = nullptr;
+    CUtensorMap tm_w13p{};  // W13 gate/up pair view (K, feature, half, expert)
+    CUtensorMap tm_w2{};
+};
+
 struct moe_ctx {
     int device = -1;
     int num_sms = 0;
@@ -40,13 +52,10 @@ struct moe_ctx {
     size_t ws_bytes = 0;
     bool ws_owned = false;
     Workspace ws{};
-    bool bound = false;
-    const uint8_t* w13 = nullptr;
-    const uint8_t* w13s = nullptr;
-    const uint8_t* w2 = nullptr;
-    const uint8_t* w2s = nullptr;
-    CUtensorMap tm_w13{}, tm_w2{}, tm_aq{}, tm_hq{};
-    CUtensorMap tm_w13p{};  // W13 gate/up pair view (fused kernel)
+    std::vector<Binding> slots = std::vector<Binding>(1);  // layer slots; forwards use slots[cur]
+    int cur = 0;
+    int opt_w13_layout = MOE_W13_CONCAT;  // layout the next bind assumes
+    CUtensorMap tm_aq{}, tm_hq{};
     int last_T = 0;
     int profile = 0;
     bool profiled = false;
@@ -110,14 +119,18 @@ int make_map(moe_ctx* h, CUtensorMap* m, CUtensorMapDataType dt, const void* bas
     return MOE_OK;
 }
 
-// W13 as a 4D view (K, row in the gate or up half, half, expert) so that one box
+// W13 as a 4D view (K, output feature j, half: gate / up, expert) so that one box
 // {128, 128, 2, 1} brings the gate tile and the matching up tile of a unit's K
-// chunk: the fused kernel's GEMM1 stage is one TMA instead of two.
-int make_map_w13_pair(moe_ctx* h, CUtensorMap* m, const void* base, uint64_t H, uint64_t I, uint64_t E) {
+// chunk: a GEMM1 stage is one TMA.  Concatenated halves: feature stride one row,
+// half stride I rows; interleaved rows (gate j at 2j, up j at 2j + 1): feature
+// stride two rows, half stride one row.
+int make_map_w13_pair(moe_ctx* h, CUtensorMap* m, const void* base, uint64_t H, uint64_t I, uint64_t E,
+                      bool interleaved) {
     auto fn = encode_fn();
     if (!fn) return fail(h, MOE_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const uint64_t row = H / 2;
     cuuint64_t dims[4] = {H, I, 2, E};
-    cuuint64_t strides[3] = {H / 2, I * (H / 2), 2 * I * (H / 2)};
+    cuuint64_t strides[3] = {interleaved ? 2 * row : row, interleaved ? row : I * row, 2 * I * row};
     cuuint32_t box[4] = {128, 128, 2, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<void*>(base), dims, strides, box, estr,
@@ -289,31 +302,61 @@ void moe_destroy(moe_handle h) {
     delete h;
 }
 
-int moe_bind_weights(moe_handle h, const void* w13_fp4, const void* w13_sf, const void* w2_fp4, const void* w2_sf) {
-    if (!h) return MOE_EINVAL;
+namespace {
+
+// Validate the weights and build their tensor maps into *b; nothing of the handle changes.
+int prepare_binding(moe_handle h, Binding* b, const void* w13_fp4, const void* w13_sf, const void* w2_fp4,
+                    const void* w2_sf) {
     int rc;
     if ((rc = check_device_ptr(h, w13_fp4, "w13_fp4", 32))) return rc;
     if ((rc = check_device_ptr(h, w13_sf, "w13_sf", 16))) return rc;
     if ((rc = check_device_ptr(h, w2_fp4, "w2_fp4", 32))) return rc;
     if ((rc = check_device_ptr(h, w2_sf, "w2_sf", 16))) return rc;
     const Geometry& g = h->geo;
-    CUtensorMap m13, m2, m13p;
-    if ((rc = make_map(h, &m13, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13_fp4, g.H, (uint64_t)g.E * 2 * g.I, g.H / 2,
+    const bool inter = h->opt_w13_layout == MOE_W13_INTERLEAVED;
+    if ((rc = make_map_w13_pair(h, &b->tm_w13p, w13_fp4, g.H, g.I, g.E, inter))) return rc;
+    if ((rc = make_map(h, &b->tm_w2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2_fp4, g.I, (uint64_t)g.E * g.H, g.I / 2,
                        128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
         return rc;
-    if ((rc = make_map(h, &m2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2_fp4, g.I, (uint64_t)g.E * g.H, g.I / 2, 128,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
-        return rc;
-    if ((rc = make_map_w13_pair(h, &m13p, w13_fp4, g.H, g.I, g.E))) return rc;
-    // everything validated: switch the binding
-    h->tm_w13 = m13;
-    h->tm_w13p = m13p;
-    h->tm_w2 = m2;
-    h->w13 = static_cast<const uint8_t*>(w13_fp4);
-    h->w13s = static_cast<const uint8_t*>(w13_sf);
-    h->w2 = static_cast<const uint8_t*>(w2_fp4);
-    h->w2s = static_cast<const uint8_t*>(w2_sf);
-    h->bound = true;
+    b->w13_layout = h->opt_w13_layout;
+    b->w13 = static_cast<const uint8_t*>(w13_fp4);
+    b->w13s = static_cast<const uint8_t*>(w13_sf);
+    b->w2 = static_cast<const uint8_t*>(w2_fp4);
+    b->w2s = static_cast<const uint8_t*>(w2_sf);
+    b->bound = true;
+    return MOE_OK;
+}
+
+}  // namespace
+
+int moe_bind_weights(moe_handle h, const void* w13_fp4, const void* w13_sf, const void* w2_fp4, const void* w2_sf) {
+    if (!h) return MOE_EINVAL;
+    Binding b;
+    const int rc = prepare_binding(h, &b, w13_fp4, w13_sf, w2_fp4, w2_sf);
+    if (rc) return rc;
+    h->slots[h->cur] = b;  // everything validated: switch the binding
+    return MOE_OK;
+}
+
+int moe_bind_layer(moe_handle h, int slot, const void* w13_fp4, const void* w13_sf, const void* w2_fp4,
+                   const void* w2_sf) {
+    if (!h) return MOE_EINVAL;
+    if (slot < 0 || slot >= static_cast<int>(h->slots.size()))
+        return fail(h, MOE_EINVAL, "slot %d outside [0, %d)", slot, static_cast<int>(h->slots.size()));
+    Binding b;
+    const int rc = prepare_binding(h, &b, w13_fp4, w13_sf, w2_fp4, w2_sf);
+    if (rc) return rc;
+    h->slots[slot] = b;  // checked slot, then weights, then switch
+    h->cur = slot;
+    return MOE_OK;
+}
+
+int moe_select_layer(moe_handle h, int slot) {
+    if (!h) return MOE_EINVAL;
+    if (slot < 0 || slot >= static_cast<int>(h->slots.size()))
+        return fail(h, MOE_EINVAL, "slot %d outside [0, %d)", slot, static_cast<int>(h->slots.size()));
+    if (!h->slots[slot].bound) return fail(h, MOE_ENOTBOUND, "slot %d has no weights bound", slot);
+    h->cur = slot;
     return MOE_OK;
 }
 
@@ -323,7 +366,8 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     const Geometry& g = h->geo;
     if (T < 0) return fail(h, MOE_EINVAL, "T=%d is negative", T);
     if (T > g.cap) return fail(h, MOE_ECAPACITY, "T=%d exceeds the capacity %d", T, g.cap);
-    if (!h->bound) return fail(h, MOE_ENOTBOUND, "no weights bound");
+    const Binding& wb = h->slots[h->cur];
+    if (!wb.bound) return fail(h, MOE_ENOTBOUND, "no weights bound");
     if (!h->ws_mem) return fail(h, MOE_ENOMEM, "no workspace");
     if (T == 0) return MOE_OK;
     if (!x || !topk_ids || !topk_weights || !out) return fail(h, MOE_EINVAL, "x, topk_ids, topk_weights and out must be non-NULL");
@@ -349,13 +393,15 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
         fl.wts = topk_weights;
         fl.nvr = num_valid_rows;
         fl.out = static_cast<uint16_t*>(out);
-        fl.w13s = h->w13s;
-        fl.w2s = h->w2s;
+        fl.w13s = wb.w13s;
+        fl.w2s = wb.w2s;
+        fl.w13_rs = wb.w13_layout == MOE_W13_INTERLEAVED ? 2 : 1;
+        fl.w13_up = wb.w13_layout == MOE_W13_INTERLEAVED ? 1 : g.I;
         fl.swiglu_limit = static_cast<float>(h->swiglu_limit);
         fl.T = T;
         mark(1);
         mark(2);
-        e = bmoe::launch_fused(g, ws, fl, &h->tm_w13p, &h->tm_aq, &h->tm_w2, &h->tm_hq, h->num_sms, s);
+        e = bmoe::launch_fused(g, ws, fl, &wb.tm_w13p, &h->tm_aq, &wb.tm_w2, &h->tm_hq, h->num_sms, s);
         if (e != cudaSuccess) return cuda_fail(h, e, "fused launch");
         h->launches += 1;
         mark(3);
@@ -399,17 +445,18 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     a.I = g.I;
     a.H = g.H;
     // GEMM1: W13 (gate/up pairs) x dispatched rows, K = H
-    a.w_sf = h->w13s;
+    a.w_sf = wb.w13s;
     a.w_rows = 2 * g.I;
     a.ld_sf = g.H / 32;
-    a.up_off = g.I;
+    a.up_off = wb.w13_layout == MOE_W13_INTERLEAVED ? 1 : g.I;
+    a.w_rs = wb.w13_layout == MOE_W13_INTERLEAVED ? 2 : 1;
     a.ktiles = g.H / 128;
     a.mtiles = g.I / 128;
     a.b_sf = ws.as;
     a.hq = ws.hq;
     a.hs = ws.hs;
     a.g_dbg = g.debug ? ws.g : nullptr;
-    e = bmoe::launch_gemm1(a, &h->tm_w13, &h->tm_aq, g.NT, h->num_sms, s);
+    e = bmoe::launch_gemm1(a, &wb.tm_w13p, &h->tm_aq, g.NT, h->num_sms, s);
 #ifdef BMOE_TRACE
     a.trace = trace_buf + 2 * 6 * 512;
 #endif
@@ -417,16 +464,17 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     h->launches += 1;
     mark(3);
     // GEMM2: W2 x h rows, K = I
-    a.w_sf = h->w2s;
+    a.w_sf = wb.w2s;
     a.w_rows = g.H;
     a.ld_sf = g.I / 32;
     a.up_off = 0;
+    a.w_rs = 1;
     a.ktiles = g.I / 128;
     a.mtiles = g.H / 128;
     a.b_sf = ws.hs;
     a.y = ws.y;
     a.g_dbg = nullptr;
-    e = bmoe::launch_gemm2(a, &h->tm_w2, &h->tm_hq, g.NT, h->num_sms, s);
+    e = bmoe::launch_gemm2(a, &wb.tm_w2, &h->tm_hq, g.NT, h->num_sms, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "GEMM2 launch");
     h->launches += 1;
     mark(4);
@@ -461,7 +509,23 @@ int moe_set_option(moe_handle h, int key, double value) {
             return MOE_OK;
         }
         case MOE_OPT_LAUNCHES:
+        case MOE_OPT_LAYER:
             return fail(h, MOE_EINVAL, "option %d is read-only", key);
+        case MOE_OPT_W13_LAYOUT: {
+            const int v = static_cast<int>(value);
+            if (static_cast<double>(v) != value || (v != MOE_W13_CONCAT && v != MOE_W13_INTERLEAVED))
+                return fail(h, MOE_EINVAL, "bad W13 layout %g", value);
+            h->opt_w13_layout = v;
+            return MOE_OK;
+        }
+        case MOE_OPT_LAYER_SLOTS: {
+            const int v = static_cast<int>(value);
+            if (static_cast<double>(v) != value || v < 1 || v > 4096)
+                return fail(h, MOE_EINVAL, "layer slots must be an integer in [1, 4096]");
+            if (h->cur >= v) return fail(h, MOE_EINVAL, "slot %d is the current layer; keep at least %d slots", h->cur, h->cur + 1);
+            h->slots.resize(static_cast<size_t>(v));
+            return MOE_OK;
+        }
         case MOE_OPT_PATH: {
             const int v = static_cast<int>(value);
             if (static_cast<double>(v) != value || v < MOE_PATH_AUTO || v > MOE_PATH_MULTI)
@@ -527,6 +591,9 @@ int moe_get_option(moe_handle h, int key, double* value) {
         case MOE_OPT_PROFILE: *value = h->profile; return MOE_OK;
         case MOE_OPT_LAUNCHES: *value = static_cast<double>(h->launches); return MOE_OK;
         case MOE_OPT_PATH: *value = h->opt_path; return MOE_OK;
+        case MOE_OPT_W13_LAYOUT: *value = h->opt_w13_layout; return MOE_OK;
+        case MOE_OPT_LAYER_SLOTS: *value = static_cast<double>(h->slots.size()); return MOE_OK;
+        case MOE_OPT_LAYER: *value = h->cur; return MOE_OK;
         default: return fail(h, MOE_EINVAL, "unknown option %d", key);
     }
 }

@@ -77,6 +77,7 @@ struct FusedArgs {
     const uint8_t* w13s;
     const uint8_t* w2s;
     int I;
+    int w13_rs, w13_up;    // W13 scale rows: gate j at j * w13_rs, up j at j * w13_rs + w13_up
     int kc2;               // K chunks per GEMM2 stage (2 when I % 256 == 0)
     int nchunks;           // compact dispatch chunks
     int tiles_cap;
@@ -641,7 +642,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             // of 16 bytes take one 16-byte load per row and group: the weight-scale lines then need
             // not stay in L1, which this kernel's shared-memory footprint leaves small.
             const bool g1_vec = (H % 512) == 0;
-            int q_ui = 0, q_kk = 0, q_kt = 0, q_ld = 0;
+            int q_ui = 0, q_kk = 0, q_kt = 0, q_ld = 0, q_rs = 1;
             bool q_g2 = false;
             const uint8_t* q_base = nullptr;
             FCursor qcur;
@@ -652,8 +653,10 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                     q_g2 = fu.g2;
                     q_kt = fu.g2 ? kt2 : kt1;
                     q_ld = fu.g2 ? I / 32 : H / 32;
-                    const int wrow = fu.g2 ? fu.u.e * H + fu.u.m * 128 : fu.u.e * 2 * I + fu.u.m * 128;
-                    q_base = (fu.g2 ? f.w2s : f.w13s) + (static_cast<size_t>(wrow) + lane) * q_ld;
+                    q_rs = fu.g2 ? 1 : f.w13_rs;
+                    const int rrow = fu.g2 ? fu.u.e * H + fu.u.m * 128 + lane
+                                           : fu.u.e * 2 * I + (fu.u.m * 128 + lane) * f.w13_rs;
+                    q_base = (fu.g2 ? f.w2s : f.w13s) + static_cast<size_t>(rrow) * q_ld;
                 }
                 const int len = min(4, q_kt - q_kk);
                 if (!q_g2 && g1_vec) {
@@ -662,7 +665,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             g[a4][i] = __ldg(reinterpret_cast<const uint4*>(
-                                q_base + static_cast<size_t>(a4 * I + 32 * i) * q_ld + q_kk * 4));
+                                q_base + static_cast<size_t>(a4 * f.w13_up + 32 * i * q_rs) * q_ld + q_kk * 4));
                 } else {
 #pragma unroll
                     for (int a4 = 0; a4 < 2; ++a4) {
@@ -674,9 +677,9 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                             for (int j = 0; j < 4; ++j) {
                                 const int kk = q_kk + j;
                                 const uint8_t* src = q_g2 ? q_base + (kk * f.kc2 + a4) * 4
-                                                          : q_base + static_cast<size_t>(a4 * I) * q_ld + kk * 4;
+                                                          : q_base + static_cast<size_t>(a4 * f.w13_up) * q_ld + kk * 4;
                                 w4[j] = (use && j < len) ? __ldg(reinterpret_cast<const uint32_t*>(
-                                                               src + static_cast<size_t>(32 * i) * q_ld))
+                                                               src + static_cast<size_t>(32 * i * q_rs) * q_ld))
                                                          : 0u;
                             }
                             g[a4][i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -867,6 +870,8 @@ cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaun
     f.w13s = fl.w13s;
     f.w2s = fl.w2s;
     f.I = g.I;
+    f.w13_rs = fl.w13_rs;
+    f.w13_up = fl.w13_up;
     f.kc2 = g.I % 256 == 0 ? 2 : 1;
     f.nchunks = (fl.T * g.K + kChunk - 1) / kChunk;
     f.tiles_cap = static_cast<int>(g.tiles_cap);

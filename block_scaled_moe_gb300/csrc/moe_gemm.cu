@@ -81,6 +81,7 @@ struct Cfg {
     static_assert(NUM_ACC * ACC_COLS <= SF_BASE, "TMEM columns");
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(4 % KS == 0, "K-steps per stage must split evenly");
+    static_assert(!G1 || KC == 1, "GEMM1 stages hold one K chunk (the W13 pair box)");
     static_assert(CW % 16 == 0, "epilogue column split");
 };
 
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
             bool ok = true;
             for (int ui = 0; ui < my_units && ok; ++ui) {
                 const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
-                const int wrow = cu.e * a.w_rows + cu.m * 128;
+                const int wrow = cu.e * a.w_rows + cu.m * 128;  // GEMM2 (GEMM1 reads the W13 pair view)
                 const uint8_t* b_sf = a.b_sf + static_cast<size_t>(cu.g) * a.ktiles * 512;
                 for (int kk = 0; kk < KT; ++kk) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
@@ -169,10 +170,11 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < KC; ++c) {
                         const int k0 = (kk * KC + c) * 128;
-                        tma_load_2d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0, wrow, pol_w);
-                        if constexpr (G1)
-                            tma_load_2d(sA + ((stage * NA + 1) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0,
-                                        wrow + a.up_off, pol_w);
+                        if constexpr (G1)  // gate and up tiles of feature tile m: one box {128, 128, 2, 1}
+                            tma_load_4d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0, cu.m * 128,
+                                        0, cu.e, pol_w);
+                        else
+                            tma_load_2d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0, wrow, pol_w);
                         tma_load_2d(sB + (stage * KC + c) * C::B_BYTES, &tm_b, &full[stage], k0, cu.row0, pol_b);
                     }
                     bulk_load(sSFB + stage * KC * 512, b_sf + kk * KC * 512, KC * 512, &full[stage]);
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
             if (p_ui >= my_units) return;
             if (p_kk == 0) {
                 const UnitInfo pu = decode_unit(blockIdx.x + p_ui * gridDim.x, p_ecur, pl, a.mtiles, NT);
-                p_src = a.w_sf + (static_cast<size_t>(pu.e) * a.w_rows + pu.m * 128 + lane) * a.ld_sf;
+                p_src = a.w_sf + (static_cast<size_t>(pu.e) * a.w_rows + (pu.m * 128 + lane) * a.w_rs) * a.ld_sf;
             }
 #pragma unroll
             for (int op = 0; op < NA; ++op)
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         dst[(op * KC + c) * 4 + i] =
-                            __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(32 * i) * a.ld_sf));
+                            __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(32 * i * a.w_rs) * a.ld_sf));
                 }
             if (++p_kk == KT) {
                 p_kk = 0;

@@ -80,7 +80,8 @@ struct GemmArgs {
     const uint8_t* w_sf;   // natural [E*rows_per_expert][K/32]
     int w_rows;            // weight rows per expert (2I for GEMM1, H for GEMM2)
     int ld_sf;             // K/32
-    int up_off;            // GEMM1: row offset of the up half (= I)
+    int up_off;            // GEMM1: row offset of up row j from gate row j (I concatenated, 1 interleaved)
+    int w_rs;              // row stride of consecutive output features (1, or 2 for interleaved W13)
     int ktiles;            // K/128
     int mtiles;            // weight tiles (of 128 rows, or row pairs for GEMM1) per expert
     // activations: codes through the tensor map, scale atoms
@@ -111,9 +112,11 @@ struct FusedLaunch {
     const uint8_t* w2s;
     float swiglu_limit;
     int T;
+    int w13_rs;  // W13 scale rows: gate row j of an expert at j * w13_rs, up row j at j * w13_rs + w13_up
+    int w13_up;
 };
 bool fused_supported(const Geometry& g);
-// tm_w13p: the W13 gate/up pair view (K, row, half, expert), box {128, 128, 2, 1}.
+// tm_w13p: the W13 gate/up pair view (K, feature, half, expert), box {128, 128, 2, 1}.
 cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaunch& f, const CUtensorMap* tm_w13p,
                          const CUtensorMap* tm_aq, const CUtensorMap* tm_w2, const CUtensorMap* tm_hq, int grid,
                          cudaStream_t s);

@@ -92,6 +92,19 @@ typedef void* moe_stream_t;
 #define MOE_PATH_FUSED 1
 #define MOE_PATH_MULTI 2
 
+#define MOE_OPT_W13_LAYOUT 9      /* MOE_W13_*: row order of W13 assumed by the next bind */
+#define MOE_OPT_LAYER_SLOTS 10    /* number of layer slots (>= 1, default 1); see moe_bind_layer */
+#define MOE_OPT_LAYER 11          /* read-only: the current layer slot */
+
+/* W13 row order.  CONCAT: rows [0,I) gate, rows [I,2I) up.  INTERLEAVED
+ * (the gate-up-interleaved experts of the mega_moe reference in ROCm/aiter
+ * PR #6881's linked AKLR commit): row 2j is gate row j and row 2j+1 up row j;
+ * the reading that gate and up alternate row by row is ours (the pages name
+ * the layout without defining its granularity).  Codes and scales follow the
+ * same order.  Both layouts give the same bits. */
+#define MOE_W13_CONCAT 0
+#define MOE_W13_INTERLEAVED 1
+
 #define MOE_DISPATCH_AUTO 0       /* fixed-slot iff capacity <= fixed-slot max */
 #define MOE_DISPATCH_FIXED 1
 #define MOE_DISPATCH_COMPACT 2
@@ -108,20 +121,36 @@ typedef void* moe_stream_t;
 int moe_create(moe_handle* out, int H, int I, int E, int topk, int capacity);
 
 /* Bind expert weights without copying (ROCm/aiter PR #6154, Changes and
- * tuning: "a shared workspace bind[s] the current layer's prepared weights
- * without copying them"):
+ * tuning: one shared workspace takes each layer's prepared weights in place)
+ * into the current layer slot:
  *   w13_fp4 u8 [E, 2I, H/2]  E2M1 codes, element 2j in the low nibble of byte j;
- *                            rows [0,I) gate, rows [I,2I) up
+ *                            row order per MOE_OPT_W13_LAYOUT (default: rows
+ *                            [0,I) gate, rows [I,2I) up)
  *   w13_sf  u8 [E, 2I, H/32] E8M0 scales (uint8 or float8_e8m0fnu bytes)
  *   w2_fp4  u8 [E, H, I/2]
  *   w2_sf   u8 [E, H, I/32]
  * The caller keeps ownership; the memory must outlive the binding and every
  * CUDA graph that captured a forward using it.  Everything is validated
  * before any state changes, so a refused bind leaves the previous binding
- * intact (aiter #6881, commit note: bind checks "everything that can refuse
- * ... before changing any binding").  Rebinding is allowed between forwards. */
+ * intact (aiter #6881, commit notes: every check that can refuse runs before a
+ * binding changes).  Rebinding is allowed between forwards. */
 int moe_bind_weights(moe_handle h, const void* w13_fp4, const void* w13_sf,
                      const void* w2_fp4, const void* w2_sf);
+
+/* Layer slots (ROCm/aiter PR #6881, commit notes on LargeMRuntime.bind_layer:
+ * each MoE layer has its own slot on one shared operator; the slot is checked
+ * first, then the weights, and only then does the current slot switch).
+ * moe_bind_layer binds the weights (as moe_bind_weights) into `slot`, in
+ * [0, MOE_OPT_LAYER_SLOTS), and makes it current; MOE_EINVAL for a bad slot,
+ * and a refusal leaves both the slot and the current slot unchanged.
+ * moe_select_layer makes an already bound slot current without rebuilding its
+ * tensor maps (MOE_ENOTBOUND if the slot is empty).  Forwards use the current
+ * slot's weights; a captured CUDA graph keeps the slot that was current at
+ * capture.  Slots share the handle's workspace, so forwards of different
+ * layers on one handle must be stream-ordered. */
+int moe_bind_layer(moe_handle h, int slot, const void* w13_fp4, const void* w13_sf,
+                   const void* w2_fp4, const void* w2_sf);
+int moe_select_layer(moe_handle h, int slot);
 
 /* One forward on `stream`:
  *   x              bf16 [T, H]

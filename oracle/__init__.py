@@ -173,10 +173,25 @@ def dispatch_fixed(ids, E: int, mtpr: int, num_valid_rows=None) -> dict:
 
 # ------------------------------------------------------------------ forward
 
+def w13_rows_concat(w13_rows, layout: str):
+    """W13 codes or scales [E, 2I, n] in the concatenated order (gate rows [0,I), up rows [I,2I)).
+
+    layout "interleaved": gate row j is row 2j and up row j is row 2j+1 (the gate-up-interleaved
+    experts of the mega_moe reference linked from ROCm/aiter PR #6881; the row-by-row reading is
+    ours)."""
+    a = _np(w13_rows, np.uint8)
+    if layout == "concat":
+        return a
+    if layout != "interleaved":
+        raise ValueError(layout)
+    return np.ascontiguousarray(np.concatenate([a[:, 0::2, :], a[:, 1::2, :]], axis=1))
+
+
 def moe_forward(x_bf16, ids, wts, weights, num_valid_rows=None, swiglu_limit: float = 0.0,
-                y_fp32: bool = False, rows=None, nthreads: int = 0):
+                y_fp32: bool = False, rows=None, nthreads: int = 0, w13_layout: str = "concat"):
     """Returns BF16 bits (uint16) [T or len(rows), H]."""
     w13, w13s, w2, w2s = (_np(a, np.uint8) for a in weights)
+    w13, w13s = w13_rows_concat(w13, w13_layout), w13_rows_concat(w13s, w13_layout)
     E, I2, Hh = w13.shape
     H, I = Hh * 2, I2 // 2
     xb = _bf16_bits(x_bf16)

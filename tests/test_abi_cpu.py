@@ -21,7 +21,7 @@ def test_every_declared_symbol_is_exported(lib):
     expected = {"moe_create", "moe_bind_weights", "moe_forward", "moe_destroy", "moe_set_option",
                 "moe_get_option", "moe_workspace_bytes", "moe_set_workspace", "moe_read_status",
                 "moe_last_error", "moe_dispatch_scheme", "moe_debug_copy", "moe_profile_read",
-                "moe_last_path", "moe_dispatch_compact_noalloc"}
+                "moe_last_path", "moe_dispatch_compact_noalloc", "moe_bind_layer", "moe_select_layer"}
     assert expected <= set(names)
     for n in names:
         assert hasattr(lib, n), n

@@ -344,3 +344,26 @@ def test_swiglu_helper_sanity():
     g = np.array([[1.0, 1.0]], np.float32)
     assert abs(swiglu(g, 1, 0.0)[0, 0] - 1 / (1 + math.exp(-1))) < 1e-7
     assert bf16_bits(np.array([1.0], np.float32))[0] == 0x3F80
+
+
+def test_w13_interleaved_layout_is_row_alternation(oracle_lib):
+    """Interleaved W13 (gate row j at 2j, up row j at 2j+1), built here row by row, gives the
+    oracle's concatenated rows back exactly, and the same layer output."""
+    import oracle
+    w = synth.micro(6, 128, 128, 3, 2, nvr=6, invalid_frac=0.0, seed=4)
+    x = synth.make_x(w)
+    ids, wts = synth.make_routing(w)
+    W = [t.cpu().numpy() for t in synth.make_weights(w, "cpu")]
+    E, I2, _ = W[0].shape
+    I = I2 // 2
+    inter = [np.empty_like(W[0]), np.empty_like(W[1])]
+    for src, dst in zip(W[:2], inter):
+        for e in range(E):
+            for j in range(I):
+                dst[e, 2 * j] = src[e, j]
+                dst[e, 2 * j + 1] = src[e, I + j]
+    assert np.array_equal(oracle.w13_rows_concat(inter[0], "interleaved"), W[0])
+    assert np.array_equal(oracle.w13_rows_concat(inter[1], "interleaved"), W[1])
+    a = oracle.moe_forward(x, ids, wts, W)
+    b = oracle.moe_forward(x, ids, wts, [inter[0], inter[1], W[2], W[3]], w13_layout="interleaved")
+    assert np.array_equal(a, b)
