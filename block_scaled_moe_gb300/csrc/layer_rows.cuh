@@ -130,8 +130,8 @@ __device__ __forceinline__ void quant_scatter_seg(const QuantArgs& a, const int3
 }
 
 // out[t] = BF16( sum over valid slots, k ascending, of w[t,k] * y[row(t,k)] ),
-// float accumulation rounded once (ROCm/ATOM PR #2725: the MoE sum "in f32 and
-// rounds once"); -1 slots are skipped (ROCm/aiter PR #6881, Technical
+// float accumulation rounded once (ROCm/ATOM PR #2725: the routed terms are
+// added in single precision and rounded one time); -1 slots are skipped (ROCm/aiter PR #6881, Technical
 // Details: both paths leave out top-k slots marked -1); rows with no valid slot
 // are +0.  Work item = one segment of kCombineVecs 16-byte vectors of one row,
 // one warp per item; y is read with L2-coherent loads (the fused kernel

@@ -70,8 +70,9 @@ struct DispatchArgs {
 };
 
 // ---------------------------------------------------------------- fixed-slot
-// vLLM PR #61262 "second fixed-slot MegaMoEV2 runtime": each token writes
-// straight into a per-expert slot (e, t) of capacity MTPR; no prepare kernel.
+// vLLM PR #61262 (the second, fixed-slot MegaMoEV2 runtime): a token goes
+// directly to the slot (e, t) of its expert, capacity MTPR, with no prepare
+// step.
 // Occupancy bits are ORed atomically (order-independent, so deterministic);
 // the last block turns them into per-expert row counts and the route-tile plan.
 __global__ void __launch_bounds__(256) k_fixed_mark(DispatchArgs a) {

@@ -9,7 +9,7 @@
  *   1. quantise the BF16 row to MXFP8: E4M3 codes, one E8M0 scale per 32
  *      elements along H;
  *   2. dispatch the row to each valid top-k expert (fixed-slot or compact
- *      scheme, vLLM PR #61262 "second fixed-slot MegaMoEV2 runtime");
+ *      scheme, vLLM PR #61262 (a second, fixed-slot MegaMoEV2 runtime));
  *   3. GEMM1 against the expert's MXFP4 W13 [2I,H] (E2M1 codes, one E8M0 scale
  *      per 32 along H), SwiGLU epilogue (optional clamp), MXFP8 1x32
  *      re-quantisation of the I intermediate values;
@@ -156,8 +156,8 @@ int moe_select_layer(moe_handle h, int slot);
  *   x              bf16 [T, H]
  *   topk_ids       int32 [T, topk]; -1 (or any id outside [0,E)) marks an
  *                  invalid slot that claims no slot and adds nothing (ROCm/ATOM
- *                  PR #2725 linked fix: "a route with a negative id now claims
- *                  no slot"); ids >= E also set MOE_ST_BAD_ID
+ *                  PR #2725 linked fix: a negative id takes no slot); ids >= E
+ *                  also set MOE_ST_BAD_ID
  *   topk_weights   float32 [T, topk]
  *   num_valid_rows device int32, first element = rows to compute, clamped to
  *                  [0,T]; NULL means T.  Read on the device, so a replayed CUDA

@@ -17,8 +17,8 @@
  *
  * The formulation is the plainest one: a dense loop over the token's k slots,
  * every dot product accumulated in double (the aiter #6881 commit that adds the
- * mega_moe op: "The reference sums over the group's experts in float64") and
- * rounded to float.  No blocking, no fusion, no reordering.
+ * mega_moe op: its reference accumulates the experts' sum in double precision)
+ * and rounded to float.  No blocking, no fusion, no reordering.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *   Q8  MXFP8 block quantisation (E4M3 codes, one E8M0 scale per 32): OCP MX
@@ -31,10 +31,10 @@
  *       path's BF16 rows, aiter #6881 Technical Details); `y_fp32` keeps them float.
  *   out Sum over valid slots in ascending k in float, rounded to BF16 once
  *       (ROCm/ATOM PR #2725 "route before the rows move", last commit note:
- *       "sums the routed contributions in f32 and rounds once").
+ *       the routed terms are added in single precision and rounded one time).
  *   A slot is valid iff its row t < num_valid_rows and 0 <= id < E
- *       (ATOM #2725 "Per-pass real row counts"; the aiter fix commit "a route
- *       with a negative id now claims no slot").  Invalid rows give +0.
+ *       (ATOM #2725 "Per-pass real row counts"; the linked aiter fix commit:
+ *       a negative id takes no slot).  Invalid rows give +0.
  */
 #include <math.h>
 #include <stdint.h>
@@ -157,7 +157,7 @@ static int slot_valid(const int32_t* ids, int t, int k, int K, int E, int nvr) {
     return t < nvr && e >= 0 && e < E;
 }
 
-/* Compact dispatch (vLLM PR #61262 "second fixed-slot MegaMoEV2 runtime": the compact
+/* Compact dispatch (vLLM PR #61262 (a second, fixed-slot MegaMoEV2 runtime): the compact
  * scheme packs tokens before dispatch).  counts[e] = valid slots with id e;
  * offsets = exclusive scan (E+1 entries); perm lists the valid flat slot ids
  * t*K+k grouped by expert, ascending flat id inside an expert;
@@ -191,8 +191,9 @@ int orc_dispatch_compact(const int32_t* ids, int T, int K, int E, const int32_t*
     return ORC_OK;
 }
 
-/* Fixed-slot dispatch (vLLM PR #61262: "each token writes straight into a per-rank
- * slot, with no prepare kernel"; on one GPU the slot belongs to the expert).
+/* Fixed-slot dispatch (vLLM PR #61262: a token goes directly to a slot reserved
+ * per rank, without a separate prepare step; on one GPU the slot belongs to the
+ * expert).
  * Slot of (t,k) = e*mtpr + t; occ holds one bit per (e,t) in words of 32 tokens
  * ([E][ceil(mtpr/32)]); counts[e] = occupied slots of expert e (a row that names
  * the same expert twice occupies one slot); route_slot = -1 for invalid slots. */
