@@ -84,6 +84,10 @@ def load(path: Optional[str] = None):
         lib.moe_bind_layer.restype = i32
         lib.moe_select_layer.argtypes = [vp, i32]
         lib.moe_select_layer.restype = i32
+        lib.moe_topk_softmax.argtypes = [vp, i32, i32, i32, i32, vp, i32, vp, vp, vp]
+        lib.moe_topk_softmax.restype = i32
+        lib.moe_forward_routed.argtypes = [vp, vp, vp, i32, i32, vp, vp, i32, vp]
+        lib.moe_forward_routed.restype = i32
         lib.moe_dispatch_compact_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         lib.moe_dispatch_compact_noalloc.restype = i32
         _lib = lib
@@ -128,6 +132,44 @@ def moe_select_layer(h, slot: int):
 def moe_forward(h, x: int, topk_ids: int, topk_weights: int, num_valid_rows: Optional[int], out: int, T: int,
                 stream: int = 0):
     _check(h, load().moe_forward(h, x, topk_ids, topk_weights, num_valid_rows, out, T, stream))
+
+
+def moe_topk_softmax(logits: int, logits_dtype: int, T: int, E: int, topk: int, num_valid_rows: Optional[int],
+                     renormalize: bool, topk_ids: int, topk_weights: int, stream: int = 0):
+    _check(None, load().moe_topk_softmax(logits, logits_dtype, T, E, topk, num_valid_rows, int(bool(renormalize)),
+                                         topk_ids, topk_weights, stream))
+
+
+def moe_forward_routed(h, x: int, router_logits: int, logits_dtype: int, renormalize: bool,
+                       num_valid_rows: Optional[int], out: int, T: int, stream: int = 0):
+    _check(h, load().moe_forward_routed(h, x, router_logits, logits_dtype, int(bool(renormalize)), num_valid_rows,
+                                        out, T, stream))
+
+
+def _logits_dtype(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return MOE_DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return MOE_DTYPE_BF16
+    raise ValueError(f"router logits must be float32 or bfloat16, not {t.dtype}")
+
+
+def topk_softmax(router_logits, topk: int, num_valid_rows=None, renormalize: bool = True, stream=None):
+    """Router top-k with softmax weights on the GPU: logits [T, E] -> (ids int32 [T, topk], weights float32)."""
+    import torch
+    if not (isinstance(router_logits, torch.Tensor) and router_logits.is_cuda and router_logits.is_contiguous()
+            and router_logits.dim() == 2):
+        raise ValueError("router_logits must be a contiguous 2-D CUDA tensor")
+    T, E = router_logits.shape
+    dev = router_logits.device
+    ids = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    w = torch.empty((T, topk), dtype=torch.float32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    moe_topk_softmax(router_logits.data_ptr(), _logits_dtype(router_logits), T, E, topk,
+                     None if num_valid_rows is None else num_valid_rows.data_ptr(), renormalize, ids.data_ptr(),
+                     w.data_ptr(), s.cuda_stream)
+    return ids, w
 
 
 def moe_destroy(h):
@@ -323,6 +365,24 @@ class BlockScaledMoE:
 
     __call__ = forward
 
+    def forward_routed(self, x, router_logits, num_valid_rows=None, out=None, stream=None, renormalize=True):
+        """Router top-k from `router_logits` [T, E] (float32 or bf16), then the layer."""
+        import torch
+        T = x.shape[0]
+        self._dev(x, "x", (T, self.H), (torch.bfloat16,))
+        self._dev(router_logits, "router_logits", (T, self.E), (torch.float32, torch.bfloat16))
+        if num_valid_rows is not None:
+            self._dev(num_valid_rows, "num_valid_rows", (1,), (torch.int32,))
+        if out is None:
+            out = torch.empty((T, self.H), dtype=torch.bfloat16, device=x.device)
+        else:
+            self._dev(out, "out", (T, self.H), (torch.bfloat16,))
+        s = stream if stream is not None else torch.cuda.current_stream(x.device)
+        moe_forward_routed(self.h, x.data_ptr(), router_logits.data_ptr(), _logits_dtype(router_logits), renormalize,
+                           None if num_valid_rows is None else num_valid_rows.data_ptr(), out.data_ptr(), T,
+                           s.cuda_stream)
+        return out
+
     def read_status(self, stream=None) -> int:
         import torch
         s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
@@ -336,7 +396,8 @@ class BlockScaledMoE:
                "route_slot": (MOE_DBG_ROUTE_SLOT, np.int32), "occ": (MOE_DBG_OCC, np.uint32),
                "xq": (MOE_DBG_XQ, np.uint8), "xs": (MOE_DBG_XS, np.uint8), "yrow": (MOE_DBG_YROW, np.int32),
                "hq": (MOE_DBG_HQ, np.uint8), "g": (MOE_DBG_G, np.float32), "y": (MOE_DBG_Y, np.uint16),
-               "tiles": (MOE_DBG_TILES, np.int32)}
+               "tiles": (MOE_DBG_TILES, np.int32), "topk_ids": (MOE_DBG_TOPK_IDS, np.int32),
+               "topk_weights": (MOE_DBG_TOPK_WEIGHTS, np.float32)}
         code, dt = ids[which]
         raw = moe_debug_copy(self.h, code, torch.cuda.current_stream().cuda_stream)
         return np.frombuffer(raw, dtype=dt).copy()

@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "lib", "libblockmoe.so")
-SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_gemm.cu", "moe_fused.cu", "moe_noalloc.cu"]
+SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_gemm.cu", "moe_fused.cu", "moe_noalloc.cu", "moe_route.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC,-Wall", "-I", INCLUDE, "-I", CSRC,
                 "--expt-relaxed-constexpr", "-Werror", "all-warnings"]

@@ -631,6 +631,53 @@ const char* moe_last_error(moe_handle h) {
     return h ? h->err.c_str() : g_create_err.c_str();
 }
 
+namespace {
+
+int check_topk_args(moe_ctx* h, const void* logits, int dtype, int T, int E, int K, const void* ids,
+                    const void* wts) {
+    if (dtype != MOE_DTYPE_F32 && dtype != MOE_DTYPE_BF16) return fail(h, MOE_EINVAL, "bad logits dtype %d", dtype);
+    if (T < 0) return fail(h, MOE_EINVAL, "T=%d is negative", T);
+    if (E < 1 || E > bmoe::kMaxExperts) return fail(h, MOE_EINVAL, "E=%d outside [1, %d]", E, bmoe::kMaxExperts);
+    if (K < 1 || K > bmoe::kMaxTopk || K > E) return fail(h, MOE_EINVAL, "topk=%d outside [1, min(16, E)]", K);
+    if (T == 0) return MOE_OK;
+    if (!logits || !ids || !wts) return fail(h, MOE_EINVAL, "logits, ids and weights must be non-NULL");
+    const uintptr_t a = reinterpret_cast<uintptr_t>(logits);
+    if ((dtype == MOE_DTYPE_F32 && (a & 3)) || (a & 1)) return fail(h, MOE_EINVAL, "logits are misaligned for their dtype");
+    if ((reinterpret_cast<uintptr_t>(ids) | reinterpret_cast<uintptr_t>(wts)) & 3)
+        return fail(h, MOE_EINVAL, "ids and weights must be 4-byte aligned");
+    return MOE_OK;
+}
+
+}  // namespace
+
+int moe_topk_softmax(const void* logits, int logits_dtype, int T, int E, int topk, const int32_t* num_valid_rows,
+                     int renormalize, int32_t* topk_ids, float* topk_weights, moe_stream_t stream) {
+    int rc = check_topk_args(nullptr, logits, logits_dtype, T, E, topk, topk_ids, topk_weights);
+    if (rc) return rc;
+    const cudaError_t e = bmoe::launch_topk_softmax(logits, logits_dtype == MOE_DTYPE_BF16, T, E, topk, num_valid_rows,
+                                                    renormalize != 0, topk_ids, topk_weights,
+                                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(nullptr, e, "top-k softmax launch");
+}
+
+int moe_forward_routed(moe_handle h, const void* x, const void* router_logits, int logits_dtype, int renormalize,
+                       const int32_t* num_valid_rows, void* out, int T, moe_stream_t stream) {
+    if (!h) return MOE_EINVAL;
+    const Geometry& g = h->geo;
+    if (T > g.cap) return fail(h, MOE_ECAPACITY, "T=%d exceeds the capacity %d", T, g.cap);
+    int rc = check_topk_args(h, router_logits, logits_dtype, T, g.E, g.K, h->ws.rids, h->ws.rw);
+    if (rc) return rc;
+    if (!h->slots[h->cur].bound) return fail(h, MOE_ENOTBOUND, "no weights bound");
+    if (T > 0) {
+        const cudaError_t e = bmoe::launch_topk_softmax(router_logits, logits_dtype == MOE_DTYPE_BF16, T, g.E, g.K,
+                                                        num_valid_rows, renormalize != 0, h->ws.rids, h->ws.rw,
+                                                        static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(h, e, "top-k softmax launch");
+        h->launches += 1;
+    }
+    return moe_forward(h, x, h->ws.rids, h->ws.rw, num_valid_rows, out, T, stream);
+}
+
 int moe_last_path(moe_handle h) {
     if (!h) return MOE_EINVAL;
     return h->last_path;
@@ -673,6 +720,8 @@ int moe_debug_copy(moe_handle h, int which, void* host_dst, size_t* bytes, moe_s
         case MOE_DBG_HQ: src = w.hq; n = (size_t)g.rows_cap * g.I; break;
         case MOE_DBG_G: src = w.g; n = (size_t)g.rows_cap * 2 * g.I * sizeof(float); break;
         case MOE_DBG_Y: src = w.y; n = (size_t)g.rows_cap * g.H * 2; break;
+        case MOE_DBG_TOPK_IDS: src = w.rids; n = sizeof(int32_t) * (size_t)h->last_T * g.K; break;
+        case MOE_DBG_TOPK_WEIGHTS: src = w.rw; n = sizeof(float) * (size_t)h->last_T * g.K; break;
         case MOE_DBG_TILES: {
             std::vector<int32_t> cnt(g.E), rb(g.E + 1), tb(g.E + 1);
             cudaStream_t s = static_cast<cudaStream_t>(stream);

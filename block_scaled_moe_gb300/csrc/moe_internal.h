@@ -43,6 +43,8 @@ struct Workspace {
     uint8_t* xs;           // [cap][H/32] canonical scales (debug capture only)
     float* g;              // [rows_cap][2I] raw GEMM1 outputs (debug capture only)
     uint32_t* ready;       // [tiles_cap] fused path: GEMM1 units finished per route tile
+    int32_t* rids;         // [cap*K] router top-k ids (moe_forward_routed)
+    float* rw;             // [cap*K] router top-k weights (moe_forward_routed)
 };
 
 struct Geometry {
@@ -120,6 +122,9 @@ bool fused_supported(const Geometry& g);
 cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaunch& f, const CUtensorMap* tm_w13p,
                          const CUtensorMap* tm_aq, const CUtensorMap* tm_w2, const CUtensorMap* tm_hq, int grid,
                          cudaStream_t s);
+// Router top-k softmax (moe_route.cu): one warp per row; bf16 != 0 reads BF16 logits.
+cudaError_t launch_topk_softmax(const void* logits, int bf16, int T, int E, int K, const int32_t* nvr, int renorm,
+                                int32_t* ids, float* w, cudaStream_t s);
 cudaError_t fused_set_attributes();
 
 // Error text of a failed call made without a handle (read by moe_last_error(NULL)).

@@ -246,6 +246,8 @@ size_t workspace_layout(const Geometry& g, char* base, Workspace* ws) {
     w.hs = reinterpret_cast<uint8_t*>(carve((size_t)g.tiles_cap * (g.I / 128) * 512));
     w.y = reinterpret_cast<uint16_t*>(carve((size_t)g.rows_cap * g.H * 2));
     w.ready = reinterpret_cast<uint32_t*>(carve(sizeof(uint32_t) * (size_t)g.tiles_cap));
+    w.rids = reinterpret_cast<int32_t*>(carve(sizeof(int32_t) * slots));
+    w.rw = reinterpret_cast<float*>(carve(sizeof(float) * slots));
     if (g.debug) {
         w.xq = reinterpret_cast<uint8_t*>(carve((size_t)g.cap * g.H));
         w.xs = reinterpret_cast<uint8_t*>(carve((size_t)g.cap * (g.H / 32)));

@@ -204,6 +204,36 @@ int moe_dispatch_scheme(moe_handle h);
 /* Path the last forward took: MOE_PATH_FUSED or MOE_PATH_MULTI (0 before any forward). */
 int moe_last_path(moe_handle h);
 
+/* ------------------------------------------------ router top-k in front of dispatch */
+#define MOE_DTYPE_F32 0
+#define MOE_DTYPE_BF16 1
+
+/* Router top-k with softmax weights (ROCm/ATOM PR #2725, linked commits on
+ * the Triton softmax top-k routing that follows the device row count):
+ *   router_logits  [T, E] float32 or bf16 (logits_dtype), device memory
+ *   num_valid_rows device int32 (first element) or NULL (= T); rows at or
+ *                  past it get ids -1 and weights 0 (read on the device, so a
+ *                  replayed CUDA graph follows the value at replay)
+ *   topk_ids       out int32 [T, topk]; topk_weights out float32 [T, topk]
+ * Per row: pick topk times the expert with the largest remaining logit (ties:
+ * lowest id) and clear it to -inf, so a row with fewer finite logits than topk
+ * picks expert 0 again with weight 0; weight = exp(logit - row max) divided by
+ * the sum over the picked experts (renormalize != 0) or over the whole row.  A
+ * row of -inf logits gets NaN weights.  1 <= E <= 4096, 1 <= topk <= min(16, E).
+ * One kernel launch on `stream`; errors are readable with moe_last_error(NULL). */
+int moe_topk_softmax(const void* router_logits, int logits_dtype, int T, int E, int topk,
+                     const int32_t* num_valid_rows, int renormalize, int32_t* topk_ids,
+                     float* topk_weights, moe_stream_t stream);
+
+/* moe_topk_softmax into the handle's workspace (E and topk of the handle),
+ * then moe_forward with those ids and weights: the router output feeds the
+ * dispatch directly, with no buffer of the caller's in between.  Same
+ * arguments, errors and stream semantics as the two calls; the ids and weights
+ * of the last call are readable with MOE_DBG_TOPK_IDS / MOE_DBG_TOPK_WEIGHTS. */
+int moe_forward_routed(moe_handle h, const void* x, const void* router_logits, int logits_dtype,
+                       int renormalize, const int32_t* num_valid_rows, void* out, int T,
+                       moe_stream_t stream);
+
 /* Stage times in milliseconds of the last forward run with MOE_OPT_PROFILE=1,
  * measured by CUDA events recorded on the forward's stream:
  *   ms[0] dispatch, ms[1] quantisation + scatter, ms[2] GEMM1, ms[3] GEMM2,
@@ -254,6 +284,8 @@ int moe_dispatch_compact_noalloc(const int32_t* topk_ids, int T, int topk, int E
 #define MOE_DBG_G 11            /* float [rows][2I]: raw GEMM1 outputs (needs DEBUG_CAPTURE) */
 #define MOE_DBG_Y 12            /* bf16 [rows][H]: GEMM2 outputs per packed row */
 #define MOE_DBG_TILES 13        /* int32 [1 + 3*tiles]: tile count, then (expert, row0, n) per tile */
+#define MOE_DBG_TOPK_IDS 14     /* int32 [T][topk]: router ids of the last moe_forward_routed */
+#define MOE_DBG_TOPK_WEIGHTS 15 /* float [T][topk]: router weights of the last moe_forward_routed */
 int moe_debug_copy(moe_handle h, int which, void* host_dst, size_t* bytes, moe_stream_t stream);
 
 #ifdef __cplusplus

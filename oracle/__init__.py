@@ -60,6 +60,7 @@ def _load():
             lib.orc_moe_forward.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, P,
                                             f32, i32, P, i32, P, i32]
             lib.orc_route_intermediates.argtypes = [P, i32, i32, i32, i32, P, P, P, P, f32, P, P, P, P]
+            lib.orc_topk_softmax.argtypes = [P, i32, i32, i32, P, i32, P, P]
             lib.orc_max_threads.restype = i32
             _lib = lib
     return _lib
@@ -232,6 +233,22 @@ def route_intermediates(x_row_bf16, e: int, weights, swiglu_limit: float = 0.0) 
     if rc:
         raise ValueError(f"orc_route_intermediates: {rc}")
     return {"g": g, "hq": hq, "hs": hs, "y": y}
+
+
+def topk_softmax(logits, K: int, num_valid_rows=None, renormalize: bool = True) -> dict:
+    """Router top-k: logits float32 [T, E] (BF16 logits: pass them widened) -> ids int32 [T, K],
+    weights float32 [T, K]."""
+    lg = np.ascontiguousarray(_np(logits, np.float32))
+    T, E = lg.shape
+    ids = np.zeros((max(T, 1), K), np.int32)
+    w = np.zeros((max(T, 1), K), np.float32)
+    nvr = None if num_valid_rows is None else np.array([num_valid_rows], np.int32)
+    if T == 0:
+        lg = np.zeros((1, E), np.float32)
+    rc = _load().orc_topk_softmax(_p(lg), T, E, K, _p(nvr), int(bool(renormalize)), _p(ids), _p(w))
+    if rc:
+        raise ValueError(f"orc_topk_softmax: {rc}")
+    return {"ids": ids[:T], "weights": w[:T]}
 
 
 def max_threads() -> int:

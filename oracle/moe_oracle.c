@@ -398,3 +398,67 @@ int orc_max_threads(void) {
     return 1;
 #endif
 }
+
+/* Router top-k with softmax weights, the step in front of dispatch (ROCm/ATOM
+ * PR #2725, linked commits on the Triton softmax top-k routing: an optional
+ * device count of real rows sends rows at or past it to ids -1 with weight 0;
+ * an expert once picked is cleared to -inf and picks use a strict greater-than
+ * scan, so ties go to the lowest id and, once a row's finite logits run out,
+ * expert 0 is picked again with weight 0; weights are renormalised over the
+ * picked experts unless `renormalize` is 0).
+ *
+ * Per row t < nvr, with m = max_e logit[t,e]:
+ *   p_e = exp(l_e - m) / sum_e' exp(l_e' - m)             (double)
+ *   pick k = 0..K-1: the first e with the largest remaining logit; its logit
+ *   becomes -inf; weight_k = exp(l_pick - m) of the value before clearing
+ *   (0 if it was already -inf), divided by sum_e' exp(l_e' - m), or by the sum
+ *   of the K picked numerators when renormalising.
+ * A row whose logits are all -inf has m = -inf and NaN weights (the formula as
+ * written; out of the layer's contract).  Logits are float32 here; BF16 logits
+ * are widened exactly by the caller. */
+int orc_topk_softmax(const float* logits, int T, int E, int K, const int32_t* num_valid_rows, int renormalize,
+                     int32_t* ids, float* weights) {
+    int t, e, k;
+    int nvr;
+    double* v;
+    double* num;
+    if (T < 0 || E < 1 || K < 1 || K > E) return ORC_EINVAL;
+    nvr = clamp_nvr(num_valid_rows, T);
+    v = (double*)malloc(sizeof(double) * (size_t)E);
+    num = (double*)malloc(sizeof(double) * (size_t)K);
+    if (!v || !num) {
+        free(v);
+        free(num);
+        return ORC_ENOMEM;
+    }
+    for (t = 0; t < T; ++t) {
+        const float* l = logits + (int64_t)t * E;
+        double m = -INFINITY, all = 0.0, picked = 0.0;
+        if (t >= nvr) {
+            for (k = 0; k < K; ++k) {
+                ids[(int64_t)t * K + k] = -1;
+                weights[(int64_t)t * K + k] = 0.0f;
+            }
+            continue;
+        }
+        for (e = 0; e < E; ++e) {
+            v[e] = (double)l[e];
+            if (v[e] > m) m = v[e];
+        }
+        for (e = 0; e < E; ++e) all += exp((double)l[e] - m);
+        for (k = 0; k < K; ++k) {
+            int best = 0;
+            for (e = 1; e < E; ++e)
+                if (v[e] > v[best]) best = e;
+            num[k] = v[best] == -INFINITY ? 0.0 : exp(v[best] - m);
+            picked += num[k];
+            ids[(int64_t)t * K + k] = best;
+            v[best] = -INFINITY;
+        }
+        for (k = 0; k < K; ++k)
+            weights[(int64_t)t * K + k] = (float)(num[k] / (renormalize ? picked : all));
+    }
+    free(v);
+    free(num);
+    return ORC_OK;
+}

@@ -21,7 +21,8 @@ def test_every_declared_symbol_is_exported(lib):
     expected = {"moe_create", "moe_bind_weights", "moe_forward", "moe_destroy", "moe_set_option",
                 "moe_get_option", "moe_workspace_bytes", "moe_set_workspace", "moe_read_status",
                 "moe_last_error", "moe_dispatch_scheme", "moe_debug_copy", "moe_profile_read",
-                "moe_last_path", "moe_dispatch_compact_noalloc", "moe_bind_layer", "moe_select_layer"}
+                "moe_last_path", "moe_dispatch_compact_noalloc", "moe_bind_layer", "moe_select_layer", "moe_topk_softmax",
+                "moe_forward_routed"}
     assert expected <= set(names)
     for n in names:
         assert hasattr(lib, n), n
@@ -63,3 +64,18 @@ def test_create_without_gpu_fails_cleanly(lib):
     rc = lib.moe_create(ctypes.byref(h), 256, 128, 8, 2, 64)
     assert rc in (bm.MOE_ECUDA, bm.MOE_EDEVICE)
     assert not h.value
+
+
+@pytest.mark.parametrize("dtype,T,E,K", [(7, 4, 8, 2), (0, -1, 8, 2), (0, 4, 0, 1), (0, 4, 4097, 1),
+                                         (0, 4, 8, 0), (0, 4, 8, 17), (1, 4, 3, 4), (0, 4, 8, 2)])
+def test_topk_softmax_refuses_bad_arguments_before_cuda(lib, dtype, T, E, K):
+    """Argument checks run on the host before any CUDA call (the last case: NULL buffers)."""
+    import block_scaled_moe_gb300 as bm
+    rc = lib.moe_topk_softmax(None, dtype, T, E, K, None, 1, None, None, None)
+    assert rc == bm.MOE_EINVAL
+    assert bm.moe_last_error(None)
+
+
+def test_topk_softmax_empty_batch_is_a_no_op(lib):
+    import block_scaled_moe_gb300 as bm
+    assert lib.moe_topk_softmax(None, bm.MOE_DTYPE_BF16, 0, 384, 6, None, 1, None, None, None) == bm.MOE_OK

@@ -367,3 +367,52 @@ def test_w13_interleaved_layout_is_row_alternation(oracle_lib):
     a = oracle.moe_forward(x, ids, wts, W)
     b = oracle.moe_forward(x, ids, wts, [inter[0], inter[1], W[2], W[3]], w13_layout="interleaved")
     assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ router top-k softmax
+
+def _topk_ref_sorted(lg, K, renorm):
+    """Independent formulation for finite logits: a stable descending sort (ties: lowest id first)
+    and a float64 softmax."""
+    ids = np.argsort(-lg.astype(np.float64), axis=1, kind="stable")[:, :K]
+    z = lg.astype(np.float64) - lg.max(axis=1, keepdims=True)
+    p = np.exp(z) / np.exp(z).sum(axis=1, keepdims=True)
+    w = np.take_along_axis(p, ids, axis=1)
+    if renorm:
+        w = w / w.sum(axis=1, keepdims=True)
+    return ids.astype(np.int32), w.astype(np.float32)
+
+
+@pytest.mark.parametrize("renorm", [True, False])
+def test_topk_softmax_equals_stable_sort(oracle_lib, renorm):
+    import oracle
+    rng = np.random.default_rng(7)
+    for T, E, K in [(9, 8, 2), (33, 384, 6), (5, 64, 16), (4, 3, 3)]:
+        lg = rng.standard_normal((T, E)).astype(np.float32)
+        lg[:, ::5] = np.round(lg[:, ::5])          # repeated values: ties must go to the lowest id
+        got = oracle.topk_softmax(lg, K, renormalize=renorm)
+        ids, w = _topk_ref_sorted(lg, K, renorm)
+        assert np.array_equal(got["ids"], ids)
+        np.testing.assert_allclose(got["weights"], w, rtol=2e-7, atol=0)
+
+
+def test_topk_softmax_special_cases(oracle_lib):
+    import oracle
+    inf = np.inf
+    lg = np.array([[-inf, 1.0, -inf, 2.0, -inf, -inf],       # 2 finite logits, K = 4
+                   [0.5, 0.5, 0.5, 0.5, 0.5, 0.5],            # all equal: ids 0, 1, 2, 3
+                   [-inf] * 6,                                 # no finite logit: NaN weights
+                   [3.0, 1.0, 2.0, 0.0, -1.0, 5.0]], np.float32)
+    r = oracle.topk_softmax(lg, 4, num_valid_rows=3)
+    a, b = 1.0, np.exp(-1.0)
+    assert r["ids"][0].tolist() == [3, 1, 0, 0]
+    np.testing.assert_allclose(r["weights"][0], [a / (a + b), b / (a + b), 0, 0], rtol=1e-7)
+    assert r["ids"][1].tolist() == [0, 1, 2, 3]
+    np.testing.assert_allclose(r["weights"][1], [0.25] * 4, rtol=1e-7)
+    assert r["ids"][2].tolist() == [0, 0, 0, 0] and np.all(np.isnan(r["weights"][2]))
+    assert r["ids"][3].tolist() == [-1] * 4 and np.all(r["weights"][3] == 0)   # row 3 >= count 3
+    full = oracle.topk_softmax(lg[3:], 4)
+    assert full["ids"][0].tolist() == [5, 0, 2, 1]
+    nr = oracle.topk_softmax(lg[3:], 4, renormalize=False)["weights"][0]
+    p = np.exp(lg[3].astype(np.float64) - 5.0)
+    np.testing.assert_allclose(nr, p[[5, 0, 2, 1]] / p.sum(), rtol=1e-7)
