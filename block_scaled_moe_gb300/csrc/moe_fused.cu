@@ -338,7 +338,7 @@ __device__ __forceinline__ void epilogue_unit(const P1& p, uint64_t* acce_b, con
                         ga = fminf(ga, L);
                         ub = fminf(fmaxf(ub, -L), L);
                     }
-                    v[c0 + i] = ga * (1.0f / (1.0f + expf(-ga))) * ub;
+                    v[c0 + i] = __fdividef(ga, 1.0f + __expf(-ga)) * ub;  // SwiGLU, fast exp / divide intrinsics
                 } else {
                     v[c0 + i] = ga;
                 }

@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
                                 ga = fminf(ga, L);
                                 ub = fminf(fmaxf(ub, -L), L);
                             }
-                            v[16 * j + i] = ga * (1.0f / (1.0f + expf(-ga))) * ub;
+                            v[16 * j + i] = __fdividef(ga, 1.0f + __expf(-ga)) * ub;  // SwiGLU, fast exp / divide intrinsics
                         } else {
                             v[16 * j + i] = ga;
                         }
