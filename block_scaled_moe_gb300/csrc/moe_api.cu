@@ -36,6 +36,7 @@ struct Binding {
     const uint8_t* w2s = nullptr;
     CUtensorMap tm_w13p{};  // W13 gate/up pair view (K, feature, half, expert)
     CUtensorMap tm_w2{};
+    CUtensorMap tm_w2w{};   // W2 with 256-row boxes (paired tiles of prefill GEMM2)
 };
 
 struct moe_ctx {
@@ -318,6 +319,9 @@ int prepare_binding(moe_handle h, Binding* b, const void* w13_fp4, const void* w
     if ((rc = make_map(h, &b->tm_w2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2_fp4, g.I, (uint64_t)g.E * g.H, g.I / 2,
                        128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
         return rc;
+    if ((rc = make_map(h, &b->tm_w2w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2_fp4, g.I, (uint64_t)g.E * g.H, g.I / 2,
+                       256, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
+        return rc;
     b->w13_layout = h->opt_w13_layout;
     b->w13 = static_cast<const uint8_t*>(w13_fp4);
     b->w13s = static_cast<const uint8_t*>(w13_sf);
@@ -450,6 +454,7 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     a.ld_sf = g.H / 32;
     a.up_off = wb.w13_layout == MOE_W13_INTERLEAVED ? 1 : g.I;
     a.w_rs = wb.w13_layout == MOE_W13_INTERLEAVED ? 2 : 1;
+    a.m_rows = 128;
     a.ktiles = g.H / 128;
     a.mtiles = g.I / 128;
     a.b_sf = ws.as;
@@ -464,17 +469,20 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     h->launches += 1;
     mark(3);
     // GEMM2: W2 x h rows, K = I
+    // 128-row route tiles take W2 tiles in pairs (one 256-row box, two accumulator chains)
+    const bool w2_pairs = g.NT == 128 && g.H % 256 == 0;
     a.w_sf = wb.w2s;
     a.w_rows = g.H;
     a.ld_sf = g.I / 32;
-    a.up_off = 0;
+    a.up_off = w2_pairs ? 128 : 0;
     a.w_rs = 1;
+    a.m_rows = w2_pairs ? 256 : 128;
     a.ktiles = g.I / 128;
-    a.mtiles = g.H / 128;
+    a.mtiles = g.H / a.m_rows;
     a.b_sf = ws.hs;
     a.y = ws.y;
     a.g_dbg = nullptr;
-    e = bmoe::launch_gemm2(a, &wb.tm_w2, &h->tm_hq, g.NT, h->num_sms, s);
+    e = bmoe::launch_gemm2(a, &wb.tm_w2, &wb.tm_w2w, &h->tm_hq, g.NT, h->num_sms, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "GEMM2 launch");
     h->launches += 1;
     mark(4);

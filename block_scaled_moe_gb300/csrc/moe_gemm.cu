@@ -45,10 +45,14 @@ namespace bmoe {
 
 namespace {
 
-template <bool G1, int NT, int KC>
+template <bool G1, int NT, int KC, bool WIDE>
 struct Cfg {
     // A K stage is KC chunks of 128 K-elements (one 128-byte swizzle atom each).
-    static constexpr int NA = G1 ? 2 : 1;                  // weight operands per stage (gate/up or W2)
+    // WIDE (GEMM2, 128-row route tiles): a unit takes two adjacent 128-row W2 tiles
+    // against one route tile, like GEMM1's gate/up pair, so that a stage streams
+    // 16 KB of weights per 16 KB row chunk instead of 8 KB.
+    static constexpr bool PAIR = G1 || WIDE;                // two weight operands per stage
+    static constexpr int NA = PAIR ? 2 : 1;                 // weight operands per stage (gate/up, W2 pair or W2)
     static constexpr int A_BYTES = 128 * 128;              // one 128x128 weight chunk in smem (1 byte per code)
     // Transaction bytes of one 128x128 FP4 box: the TMA counts the packed bytes it
     // reads (two codes per byte), not the 16-byte-aligned footprint it writes.
@@ -62,9 +66,9 @@ struct Cfg {
     // MMA issuers and their accumulator chains: 4 for the decode tile width (issue
     // bound); for 128-wide tiles GEMM1 keeps its gate/up pair and GEMM2 one chain,
     // so that GEMM2's accumulator can be double-buffered in TMEM.
-    static constexpr int MW = NT <= 64 ? 4 : (G1 ? 2 : 1);
+    static constexpr int MW = NT <= 64 ? 4 : (PAIR ? 2 : 1);
     static constexpr int NI = MW;                          // MMA-issuing warps (chain w is issued by warp w % NI)
-    static constexpr int KS = G1 ? MW / 2 : MW;            // K-steps of a stage split over KS chains per operand
+    static constexpr int KS = PAIR ? MW / 2 : MW;          // K-steps of a stage split over KS chains per operand
     static constexpr int EW = NT <= 64 ? 4 : 8;            // epilogue warps (EW/4 per TMEM lane quadrant)
     static constexpr int CW = NT / (EW / 4);               // accumulator columns per epilogue warp
     static constexpr int ACC_COLS = MW * NT;               // one accumulator set: MW chains of NT columns
@@ -76,20 +80,26 @@ struct Cfg {
     static constexpr int MMA_WARP0 = 2;
     static constexpr int EPI_WARP0 = 2 + NI;
     static constexpr int THREADS = 32 * (2 + NI + EW);
-    static constexpr int BAR_BYTES = (2 * STAGES + 2 * 2 + 1) * 8 + 16;
+    // WIDE units release their two single-buffered accumulator chains one at a time
+    static constexpr bool PER_CHAIN = WIDE;
+    static constexpr int BAR_BYTES = (2 * STAGES + 2 + 4 + 1) * 8 + 16;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + TAB_BYTES + BAR_BYTES;
     static_assert(NUM_ACC * ACC_COLS <= SF_BASE, "TMEM columns");
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(4 % KS == 0, "K-steps per stage must split evenly");
     static_assert(!G1 || KC == 1, "GEMM1 stages hold one K chunk (the W13 pair box)");
+    static_assert(!WIDE || (!G1 && NT == 128 && KC == 1), "wide units: GEMM2, 128-row route tiles");
+    static_assert(!PER_CHAIN || NUM_ACC == 1, "per-chain release of a single-buffered accumulator");
+    static_assert(MW <= 4, "barrier slots");
     static_assert(CW % 16 == 0, "epilogue column split");
 };
 
-template <bool G1, int NT, int KC>
-__global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
+template <bool G1, int NT, int KC, bool WIDE>
+__global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b, const GemmArgs a) {
-    using C = Cfg<G1, NT, KC>;
+    using C = Cfg<G1, NT, KC, WIDE>;
     constexpr int STAGES = C::STAGES, NA = C::NA, MW = C::MW, KS = C::KS, NI = C::NI;
+    constexpr bool PAIR = C::PAIR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = sm;
@@ -100,8 +110,8 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * KC * 512);
     uint64_t* empty = full + STAGES;
     uint64_t* accf = empty + STAGES;
-    uint64_t* acce = accf + 2;
-    uint64_t* drain = acce + 2;
+    uint64_t* acce = accf + 2;  // [2] accumulator sets, or [MW] chains when PER_CHAIN
+    uint64_t* drain = acce + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int32_t* tab = reinterpret_cast<int32_t*>(sSFB + STAGES * KC * 512 + C::BAR_BYTES);
@@ -127,10 +137,8 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
             mbar_init(&full[s], 1 + 32);  // TMA issuer + the 32 scale-copying lanes
             mbar_init(&empty[s], NI);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&accf[b], NI);
-            mbar_init(&acce[b], 32 * C::EW);
-        }
+        for (int b = 0; b < 2; ++b) mbar_init(&accf[b], NI);
+        for (int b = 0; b < 4; ++b) mbar_init(&acce[b], 32 * C::EW);
         mbar_init(drain, NI);
         *abort_flag = 0;
         fence_mbar_init();
@@ -157,7 +165,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
             bool ok = true;
             for (int ui = 0; ui < my_units && ok; ++ui) {
                 const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
-                const int wrow = cu.e * a.w_rows + cu.m * 128;  // GEMM2 (GEMM1 reads the W13 pair view)
+                const int wrow = cu.e * a.w_rows + cu.m * a.m_rows;  // GEMM2 (GEMM1 reads the W13 pair view)
                 const uint8_t* b_sf = a.b_sf + static_cast<size_t>(cu.g) * a.ktiles * 512;
                 for (int kk = 0; kk < KT; ++kk) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
@@ -173,7 +181,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
                         if constexpr (G1)  // gate and up tiles of feature tile m: one box {128, 128, 2, 1}
                             tma_load_4d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0, cu.m * 128,
                                         0, cu.e, pol_w);
-                        else
+                        else  // W2 tile (WIDE: a 256-row box, the unit's two tiles back to back)
                             tma_load_2d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0, wrow, pol_w);
                         tma_load_2d(sB + (stage * KC + c) * C::B_BYTES, &tm_b, &full[stage], k0, cu.row0, pol_b);
                     }
@@ -205,7 +213,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
             if (p_ui >= my_units) return;
             if (p_kk == 0) {
                 const UnitInfo pu = decode_unit(blockIdx.x + p_ui * gridDim.x, p_ecur, pl, a.mtiles, NT);
-                p_src = a.w_sf + (static_cast<size_t>(pu.e) * a.w_rows + (pu.m * 128 + lane) * a.w_rs) * a.ld_sf;
+                p_src = a.w_sf + (static_cast<size_t>(pu.e) * a.w_rows + (pu.m * a.m_rows + lane) * a.w_rs) * a.ld_sf;
             }
 #pragma unroll
             for (int op = 0; op < NA; ++op)
@@ -265,8 +273,13 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
         for (int ui = 0; ui < my_units && ok; ++ui) {
             const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
             const int N = (cu.n + 15) & ~15;
-            if (!mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 2)),
-                           kWaitLimitNs)) {
+            if constexpr (C::PER_CHAIN) {
+                for (int w = wi; w < MW && ok; w += NI)
+                    ok = mbar_wait(&acce[w], acc_phase ^ 1u, abort_flag, a.status,
+                                   kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs);
+                if (!ok) break;
+            } else if (!mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, a.status,
+                                  kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs)) {
                 ok = false;
                 break;
             }
@@ -286,9 +299,10 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
                         // k % KS == w >> 1; GEMM2: chain w takes the G2S consecutive K-steps from w * G2S
                         // (k = 4 * chunk + step in chunk) and needs only the atoms of their chunks.
                         constexpr int G2S = 4 * KC / MW;
-                        const int op = G1 ? (w & 1) : 0;
-                        const int kfirst = G1 ? (w >> 1) : w * G2S;
-                        const int c_lo = G1 ? 0 : (w * G2S) >> 2, c_hi = G1 ? KC - 1 : (w * G2S + G2S - 1) >> 2;
+                        // (WIDE: chain w multiplies W2 tile w over every K-step, like an operand of the pair.)
+                        const int op = PAIR ? (w & 1) : 0;
+                        const int kfirst = PAIR ? (w >> 1) : w * G2S;
+                        const int c_lo = PAIR ? 0 : (w * G2S) >> 2, c_hi = PAIR ? KC - 1 : (w * G2S + G2S - 1) >> 2;
                         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * C::ACC_COLS + w * NT);
                         const uint32_t sfc = tmem + static_cast<uint32_t>(
                                                         C::SF_BASE + (w * C::SF_SLOTS + (job & 1)) * C::SF_SLOT_COLS);
@@ -301,7 +315,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
                         }
 #pragma unroll
                         for (int k = 0; k < 4 * KC; ++k) {
-                            if (G1 ? (k % KS != kfirst) : (k / G2S != w)) continue;
+                            if (PAIR ? (k % KS != kfirst) : (k / G2S != w)) continue;
                             const int c = k >> 2, k4 = k & 3;
                             const uint64_t da =
                                 desc_kmajor_sw128(smem_u32(sA + ((stage * NA + op) * KC + c) * C::A_BYTES)) +
@@ -361,6 +375,38 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
             if (tracer) trace(a, 4, ui);
             const uint32_t tb =
                 tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * C::ACC_COLS);
+            if constexpr (WIDE) {
+                // chain w = W2 tile w of the pair: drain it, release it, store its BF16 rows
+#pragma unroll
+                for (int w = 0; w < MW; ++w) {
+                    float v[CW];
+#pragma unroll
+                    for (int h2 = 0; h2 < CW / 32; ++h2) {
+                        uint32_t r[2][16];
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+                            if (cbase + 32 * h2 + 16 * j < cu.n) tmem_ld16(tb + w * NT + cbase + 32 * h2 + 16 * j, r[j]);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[32 * h2 + 16 * j + i] = __uint_as_float(r[j][i]);
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&acce[w]);
+                    const int featw = cu.m * a.m_rows + w * 128 + 32 * q + lane;
+#pragma unroll
+                    for (int j = 0; j < CW; ++j) {
+                        const int c = cbase + j;
+                        if (c < cu.n)
+                            a.y[static_cast<size_t>(cu.row0 + c) * a.H + featw] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+                    }
+                }
+                if (tracer) trace(a, 5, ui);
+                acc_phase ^= 1u;
+                continue;
+            }
             const int feat = cu.m * 128 + 32 * q + lane;
             float v[CW];  // GEMM1: h = SwiGLU(gate, up); GEMM2: y
 #pragma unroll
@@ -438,15 +484,15 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC>::THREADS, 1)
     }
 }
 
-template <bool G1, int NT, int KC>
+template <bool G1, int NT, int KC, bool WIDE>
 cudaError_t set_attr() {
-    return cudaFuncSetAttribute(k_gemm<G1, NT, KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Cfg<G1, NT, KC>::SMEM);
+    return cudaFuncSetAttribute(k_gemm<G1, NT, KC, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<G1, NT, KC, WIDE>::SMEM);
 }
 
-template <bool G1, int NT, int KC>
+template <bool G1, int NT, int KC, bool WIDE>
 cudaError_t launch(const GemmArgs& a, const CUtensorMap* tw, const CUtensorMap* tb, int grid, cudaStream_t s) {
-    k_gemm<G1, NT, KC><<<grid, Cfg<G1, NT, KC>::THREADS, Cfg<G1, NT, KC>::SMEM, s>>>(*tw, *tb, a);
+    k_gemm<G1, NT, KC, WIDE><<<grid, Cfg<G1, NT, KC, WIDE>::THREADS, Cfg<G1, NT, KC, WIDE>::SMEM, s>>>(*tw, *tb, a);
     return cudaGetLastError();
 }
 
@@ -454,24 +500,28 @@ cudaError_t launch(const GemmArgs& a, const CUtensorMap* tw, const CUtensorMap* 
 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
-    if ((e = set_attr<true, 128, 1>()) != cudaSuccess) return e;
-    if ((e = set_attr<true, 32, 1>()) != cudaSuccess) return e;
-    if ((e = set_attr<false, 128, 1>()) != cudaSuccess) return e;
-    if ((e = set_attr<false, 32, 1>()) != cudaSuccess) return e;
-    return set_attr<false, 32, 2>();
+    if ((e = set_attr<true, 128, 1, false>()) != cudaSuccess) return e;
+    if ((e = set_attr<true, 32, 1, false>()) != cudaSuccess) return e;
+    if ((e = set_attr<false, 128, 1, false>()) != cudaSuccess) return e;
+    if ((e = set_attr<false, 32, 1, false>()) != cudaSuccess) return e;
+    if ((e = set_attr<false, 128, 1, true>()) != cudaSuccess) return e;
+    return set_attr<false, 32, 2, false>();
 }
 
 cudaError_t launch_gemm1(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_x, int NT, int grid,
                          cudaStream_t s) {
-    return NT == 32 ? launch<true, 32, 1>(a, tm_w, tm_x, grid, s) : launch<true, 128, 1>(a, tm_w, tm_x, grid, s);
+    return NT == 32 ? launch<true, 32, 1, false>(a, tm_w, tm_x, grid, s)
+                    : launch<true, 128, 1, false>(a, tm_w, tm_x, grid, s);
 }
 
-cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_h, int NT, int grid,
-                         cudaStream_t s) {
+cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_w_wide,
+                         const CUtensorMap* tm_h, int NT, int grid, cudaStream_t s) {
     // decode tiles stream W2 in 256-wide K stages when I allows it (halves the per-stage cost per byte)
-    if (NT == 32) return a.ktiles % 2 == 0 ? launch<false, 32, 2>(a, tm_w, tm_h, grid, s)
-                                           : launch<false, 32, 1>(a, tm_w, tm_h, grid, s);
-    return launch<false, 128, 1>(a, tm_w, tm_h, grid, s);
+    if (NT == 32) return a.ktiles % 2 == 0 ? launch<false, 32, 2, false>(a, tm_w, tm_h, grid, s)
+                                           : launch<false, 32, 1, false>(a, tm_w, tm_h, grid, s);
+    // 128-row route tiles: pairs of W2 tiles (a.m_rows == 256) when H allows it
+    return a.m_rows == 256 ? launch<false, 128, 1, true>(a, tm_w_wide, tm_h, grid, s)
+                           : launch<false, 128, 1, false>(a, tm_w, tm_h, grid, s);
 }
 
 }  // namespace bmoe

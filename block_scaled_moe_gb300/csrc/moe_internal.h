@@ -84,6 +84,7 @@ struct GemmArgs {
     int ld_sf;             // K/32
     int up_off;            // GEMM1: row offset of up row j from gate row j (I concatenated, 1 interleaved)
     int w_rs;              // row stride of consecutive output features (1, or 2 for interleaved W13)
+    int m_rows;            // weight rows per unit and operand tile index step: 128, or 256 for paired W2 tiles
     int ktiles;            // K/128
     int mtiles;            // weight tiles (of 128 rows, or row pairs for GEMM1) per expert
     // activations: codes through the tensor map, scale atoms
@@ -99,8 +100,9 @@ struct GemmArgs {
 
 cudaError_t launch_gemm1(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_x, int NT, int grid,
                          cudaStream_t s);
-cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_h, int NT, int grid,
-                         cudaStream_t s);
+// tm_w_wide: W2 with 256-row boxes, used when a.m_rows == 256 (128-row route tiles, H % 256 == 0)
+cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_w_wide,
+                         const CUtensorMap* tm_h, int NT, int grid, cudaStream_t s);
 cudaError_t gemm_set_attributes();
 
 // ------------------------------------------------------------------ single-launch fused path (moe_fused.cu)
