@@ -189,8 +189,11 @@ def w13_rows_concat(w13_rows, layout: str):
 
 
 def moe_forward(x_bf16, ids, wts, weights, num_valid_rows=None, swiglu_limit: float = 0.0,
-                y_fp32: bool = False, rows=None, nthreads: int = 0, w13_layout: str = "concat"):
-    """Returns BF16 bits (uint16) [T or len(rows), H]."""
+                y_fp32: bool = False, rows=None, nthreads: int = 0, w13_layout: str = "concat",
+                y_format: str = None):
+    """Returns BF16 bits (uint16) [T or len(rows), H].  y_format: GEMM2 rows handed to the combine as
+    "bf16" (default), "fp32" (same as y_fp32=True) or "mxfp8" (1x32 E4M3 + E8M0 along H)."""
+    y_mode = {"bf16": 0, "fp32": 1, "mxfp8": 2}[y_format or ("fp32" if y_fp32 else "bf16")]
     w13, w13s, w2, w2s = (_np(a, np.uint8) for a in weights)
     w13, w13s = w13_rows_concat(w13, w13_layout), w13_rows_concat(w13s, w13_layout)
     E, I2, Hh = w13.shape
@@ -212,7 +215,7 @@ def moe_forward(x_bf16, ids, wts, weights, num_valid_rows=None, swiglu_limit: fl
         ids = np.zeros((1, K), np.int32)
         wts = np.zeros((1, K), np.float32)
     rc = _load().orc_moe_forward(_p(xb), _p(ids), _p(wts), T, H, I, E, K, _p(nvr), _p(w13), _p(w13s),
-                                 _p(w2), _p(w2s), float(swiglu_limit), int(y_fp32), _p(rws), n, _p(out),
+                                 _p(w2), _p(w2s), float(swiglu_limit), y_mode, _p(rws), n, _p(out),
                                  int(nthreads))
     if rc:
         raise ValueError(f"orc_moe_forward: {rc}")

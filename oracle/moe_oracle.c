@@ -28,7 +28,11 @@
  *   SwiGLU a = G[0:I) (gate), b = G[I:2I) (up); with clamp L > 0:
  *       a = min(a, L), b = clamp(b, -L, L); h = a * (1/(1+exp(-a))) * b in float.
  *   y   GEMM2 rows are rounded to BF16 per route before the combine (the main
- *       path's BF16 rows, aiter #6881 Technical Details); `y_fp32` keeps them float.
+ *       path's BF16 rows, aiter #6881 Technical Details); `y_mode` 1 keeps them
+ *       float; `y_mode` 2 sends them as MXFP8 in the main path's 1x32 format
+ *       (aiter #6881 Technical Details, small input: GEMM2 rows go to the
+ *       combine as FP8 instead of BF16), quantised from the float value with
+ *       rule Q8 along H and dequantised for the combine.
  *   out Sum over valid slots in ascending k in float, rounded to BF16 once
  *       (ROCm/ATOM PR #2725 "route before the rows move", last commit note:
  *       the routed terms are added in single precision and rounded one time).
@@ -282,7 +286,7 @@ static void expert_route(const orc_weights* W, int e, const double* xdq, float s
 
 typedef struct {
     float *g, *h, *y, *acc;
-    uint8_t *hq, *hs, *xq, *xs;
+    uint8_t *hq, *hs, *xq, *xs, *yq, *ys;
     double *xdq, *hdq;
 } orc_scratch;
 
@@ -295,20 +299,22 @@ static int scratch_alloc(orc_scratch* s, int H, int I) {
     s->hs = (uint8_t*)malloc((size_t)I / 32);
     s->xq = (uint8_t*)malloc((size_t)H);
     s->xs = (uint8_t*)malloc((size_t)H / 32);
+    s->yq = (uint8_t*)malloc((size_t)H);
+    s->ys = (uint8_t*)malloc((size_t)H / 32);
     s->xdq = (double*)malloc(sizeof(double) * H);
     s->hdq = (double*)malloc(sizeof(double) * I);
-    return (s->g && s->h && s->y && s->acc && s->hq && s->hs && s->xq && s->xs && s->xdq && s->hdq)
+    return (s->g && s->h && s->y && s->acc && s->hq && s->hs && s->xq && s->xs && s->yq && s->ys && s->xdq && s->hdq)
                ? ORC_OK : ORC_ENOMEM;
 }
 
 static void scratch_free(orc_scratch* s) {
     free(s->g); free(s->h); free(s->y); free(s->acc); free(s->hq); free(s->hs);
-    free(s->xq); free(s->xs); free(s->xdq); free(s->hdq);
+    free(s->xq); free(s->xs); free(s->yq); free(s->ys); free(s->xdq); free(s->hdq);
 }
 
 /* One output row. */
 static void forward_row(const orc_weights* W, const uint16_t* x, const int32_t* ids, const float* wts,
-                        int t, int K, int nvr, float swiglu_limit, int y_fp32, uint16_t* out_row,
+                        int t, int K, int nvr, float swiglu_limit, int y_mode, uint16_t* out_row,
                         orc_scratch* s) {
     const int H = W->H;
     int k, j, hh, any = 0;
@@ -323,8 +329,12 @@ static void forward_row(const orc_weights* W, const uint16_t* x, const int32_t* 
             if (e < 0 || e >= W->E) continue;
             any = 1;
             expert_route(W, e, s->xdq, swiglu_limit, s->y, NULL, NULL, NULL, s->g, s->h, s->hq, s->hs, s->hdq);
+            if (y_mode == 2)
+                for (j = 0; j < H / 32; ++j) orc_quant_mxfp8_block(s->y + 32 * j, s->yq + 32 * j, s->ys + j);
             for (j = 0; j < H; ++j) {
-                float yv = y_fp32 ? s->y[j] : orc_bf16_to_float(orc_float_to_bf16(s->y[j]));
+                float yv = y_mode == 1   ? s->y[j]
+                           : y_mode == 2 ? (float)(orc_e4m3_value(s->yq[j]) * orc_e8m0_value(s->ys[j / 32]))
+                                         : orc_bf16_to_float(orc_float_to_bf16(s->y[j]));
                 float prod = wk * yv;
                 s->acc[j] = s->acc[j] + prod;
             }
@@ -335,12 +345,13 @@ static void forward_row(const orc_weights* W, const uint16_t* x, const int32_t* 
 
 /* Full forward, or a subset of rows.
  *   x [T,H] bf16; ids [T,K] int32; wts [T,K] float; num_valid_rows: NULL = T.
+ *   y_mode: 0 BF16 GEMM2 rows, 1 float, 2 MXFP8 (see the file comment).
  *   rows/nrows: the token rows to compute (NULL = all T, in order); out is
  *   [nrows, H] bf16 in the order of `rows`.
  *   nthreads <= 0: the OpenMP default. */
 int orc_moe_forward(const uint16_t* x, const int32_t* ids, const float* wts, int T, int H, int I, int E, int K,
                     const int32_t* num_valid_rows, const uint8_t* w13, const uint8_t* w13s,
-                    const uint8_t* w2, const uint8_t* w2s, float swiglu_limit, int y_fp32,
+                    const uint8_t* w2, const uint8_t* w2s, float swiglu_limit, int y_mode,
                     const int32_t* rows, int nrows, uint16_t* out, int nthreads) {
     orc_weights W;
     int nvr = clamp_nvr(num_valid_rows, T), n = rows ? nrows : T, r, err = ORC_OK;
@@ -366,7 +377,7 @@ int orc_moe_forward(const uint16_t* x, const int32_t* ids, const float* wts, int
             int t = rows ? rows[r] : r;
             if (!ok) continue;
             if (t < 0 || t >= T) { memset(out + (int64_t)r * H, 0, sizeof(uint16_t) * H); continue; }
-            forward_row(&W, x, ids, wts, t, K, nvr, swiglu_limit, y_fp32, out + (int64_t)r * H, &s);
+            forward_row(&W, x, ids, wts, t, K, nvr, swiglu_limit, y_mode, out + (int64_t)r * H, &s);
         }
         scratch_free(&s);
     }

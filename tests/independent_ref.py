@@ -79,7 +79,7 @@ def swiglu(g: np.ndarray, I: int, limit: float) -> np.ndarray:
 
 
 def grouped_forward(x_bf16: torch.Tensor, ids: np.ndarray, wts: np.ndarray, weights, nvr=None,
-                    swiglu_limit: float = 0.0, y_fp32: bool = False) -> np.ndarray:
+                    swiglu_limit: float = 0.0, y_fp32: bool = False, y_mxfp8: bool = False) -> np.ndarray:
     """Per-expert grouped formulation.  Returns BF16 bits [T,H]."""
     w13, w13s, w2, w2s = (np.asarray(a.cpu().numpy() if isinstance(a, torch.Tensor) else a) for a in weights)
     E, I2, _ = w13.shape
@@ -101,7 +101,11 @@ def grouped_forward(x_bf16: torch.Tensor, ids: np.ndarray, wts: np.ndarray, weig
         h = swiglu(G, I, swiglu_limit)
         hq, hs = q8(h)
         Yv = (q8_dequant(hq, hs) @ fp4_dequant(w2[e], w2s[e]).T).astype(np.float32)
-        Y[t_idx, k_idx] = Yv if y_fp32 else bf16_round(Yv)
+        if y_mxfp8:
+            yq, ys = q8(Yv)
+            Y[t_idx, k_idx] = q8_dequant(yq, ys).astype(np.float32)
+        else:
+            Y[t_idx, k_idx] = Yv if y_fp32 else bf16_round(Yv)
     acc = np.zeros((T, H), np.float32)
     for k in range(K):
         contrib = (wts[:, k:k + 1].astype(np.float32) * Y[:, k]).astype(np.float32)

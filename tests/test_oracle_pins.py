@@ -416,3 +416,20 @@ def test_topk_softmax_special_cases(oracle_lib):
     nr = oracle.topk_softmax(lg[3:], 4, renormalize=False)["weights"][0]
     p = np.exp(lg[3].astype(np.float64) - 5.0)
     np.testing.assert_allclose(nr, p[[5, 0, 2, 1]] / p.sum(), rtol=1e-7)
+
+
+def test_mxfp8_gemm2_rows_equal_grouped_formulation(oracle_lib):
+    """GEMM2 rows handed to the combine as MXFP8 (1x32 along H): the oracle equals the grouped
+    formulation with its own torch/numpy Q8 of y, bit for bit; and it differs from the BF16-row
+    output by about the FP8 step (the mode does change the result)."""
+    import oracle
+    w = synth.get("tiny")
+    x, ids, wts, W = synth.make_all(w)
+    got = oracle.moe_forward(x, ids, wts, [t.cpu() for t in W], num_valid_rows=w.nvr, y_format="mxfp8")
+    ref = grouped_forward(x, ids, wts, W, nvr=w.nvr, swiglu_limit=w.swiglu_limit, y_mxfp8=True)
+    assert np.array_equal(got, ref)
+    bf = oracle.moe_forward(x, ids, wts, [t.cpu() for t in W], num_valid_rows=w.nvr)
+    a = oracle.bf16_bits_to_float(got).astype(np.float64)
+    b = oracle.bf16_bits_to_float(bf).astype(np.float64)
+    rel = np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert 1e-3 < rel < 5e-2, rel
