@@ -239,7 +239,7 @@ class BlockScaledMoE:
     def __init__(self, H: int, I: int, E: int, topk: int, capacity: int, *, dispatch: Optional[str] = None,
                  swiglu_limit: float = 0.0, route_tile: int = 0, debug: bool = False,
                  fixed_slot_max: Optional[int] = None, workspace=None, path: Optional[str] = None,
-                 w13_layout: str = "concat", layer_slots: int = 1):
+                 w13_layout: str = "concat", layer_slots: int = 1, y_format: str = "bf16"):
         self.H, self.I, self.E, self.topk, self.capacity = H, I, E, topk, capacity
         self.h = moe_create(H, I, E, topk, capacity)
         try:
@@ -258,6 +258,7 @@ class BlockScaledMoE:
                            {"concat": MOE_W13_CONCAT, "interleaved": MOE_W13_INTERLEAVED}[w13_layout])
             if layer_slots != 1:
                 moe_set_option(self.h, MOE_OPT_LAYER_SLOTS, layer_slots)
+            moe_set_option(self.h, MOE_OPT_Y_FORMAT, {"bf16": MOE_Y_BF16, "mxfp8": MOE_Y_MXFP8}[y_format])
             if path is not None:
                 moe_set_option(self.h, MOE_OPT_PATH, {"auto": MOE_PATH_AUTO, "fused": MOE_PATH_FUSED,
                                                       "multi": MOE_PATH_MULTI}[path])

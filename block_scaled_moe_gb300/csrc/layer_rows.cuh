@@ -4,6 +4,7 @@
 // rows, and the top-k weighted combine of one output row.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "moe_internal.h"
@@ -143,7 +144,25 @@ struct CombineArgs {
     const float* w;
     uint16_t* out;
     int T, K, H;
+    const uint8_t* y8;  // non-null: GEMM2 rows are MXFP8 codes [rows][H] ...
+    const uint8_t* ys;  // ... with E8M0 scales [rows][H/32]
 };
+
+// One MXFP8 1x32 block held by a warp, one element per lane (OCP MX rule as for
+// the input rows): returns the lane's E4M3 code; *scale receives the E8M0 code.
+__device__ __forceinline__ uint8_t quant_block_warp(float v, uint8_t* scale) {
+    const uint32_t amax = __reduce_max_sync(kFull, __float_as_uint(fabsf(v)));
+    int code = static_cast<int>(amax >> 23) - 8;
+    code = code < 0 ? 0 : code;
+    *scale = static_cast<uint8_t>(code);
+    const float mul = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
+    return __nv_cvt_float_to_fp8(v * mul, __NV_SATFINITE, __NV_E4M3);
+}
+
+// 2^(code - 127) for an E8M0 code in [0, 254] (code 0 is the subnormal 2^-127).
+__device__ __forceinline__ float e8m0_value(uint32_t code) {
+    return code ? __uint_as_float(code << 23) : __uint_as_float(1u << 22);
+}
 
 __device__ __forceinline__ int combine_items(const CombineArgs& a) {
     return a.T * ((a.H / 8 + kCombineVecs - 1) / kCombineVecs);
@@ -175,14 +194,31 @@ __device__ __forceinline__ void combine_item(const CombineArgs& a, int item, int
         for (int k = 0; k < kMaxTopk; ++k) {
             if (k >= a.K || rows[k] < 0) continue;
             any = true;
-            const uint4 q = __ldcg(reinterpret_cast<const uint4*>(a.y + (size_t)rows[k] * a.H) + v);
-            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
             const float wv = wk[k];
+            float yv[8];
+            if (a.y8) {  // MXFP8 row: 8 codes and the scale of their 32-block (exact dequantisation)
+                const uint2 q = __ldcg(reinterpret_cast<const uint2*>(a.y8 + (size_t)rows[k] * a.H) + v);
+                const float sc = e8m0_value(__ldcg(a.ys + (size_t)rows[k] * (a.H >> 5) + (v >> 2)));
+                const uint32_t w2[2] = {q.x, q.y};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                acc[2 * j] = __fadd_rn(acc[2 * j], __fmul_rn(wv, __uint_as_float(w4[j] << 16)));
-                acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __fmul_rn(wv, __uint_as_float(w4[j] & 0xffff0000u)));
+                for (int j = 0; j < 4; ++j) {
+                    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+                        static_cast<__nv_fp8x2_storage_t>((w2[j >> 1] >> (16 * (j & 1))) & 0xffffu), __NV_E4M3);
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+                    yv[2 * j] = f.x * sc;
+                    yv[2 * j + 1] = f.y * sc;
+                }
+            } else {
+                const uint4 q = __ldcg(reinterpret_cast<const uint4*>(a.y + (size_t)rows[k] * a.H) + v);
+                const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    yv[2 * j] = __uint_as_float(w4[j] << 16);
+                    yv[2 * j + 1] = __uint_as_float(w4[j] & 0xffff0000u);
+                }
             }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], __fmul_rn(wv, yv[j]));
         }
         uint4 o = make_uint4(0, 0, 0, 0);
         if (any) {

@@ -56,6 +56,7 @@ struct moe_ctx {
     std::vector<Binding> slots = std::vector<Binding>(1);  // layer slots; forwards use slots[cur]
     int cur = 0;
     int opt_w13_layout = MOE_W13_CONCAT;  // layout the next bind assumes
+    int y_format = MOE_Y_BF16;            // GEMM2 rows handed to the combine
     CUtensorMap tm_aq{}, tm_hq{};
     int last_T = 0;
     int profile = 0;
@@ -387,6 +388,9 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     auto mark = [&](int i) {
         if (prof) cudaEventRecord(h->ev[i], s);
     };
+    // MXFP8 GEMM2 rows live in the y region: codes [rows_cap][H], then scales [rows_cap][H/32]
+    uint8_t* y8 = h->y_format == MOE_Y_MXFP8 ? reinterpret_cast<uint8_t*>(ws.y) : nullptr;
+    uint8_t* ys = y8 ? y8 + (size_t)g.rows_cap * g.H : nullptr;
     mark(0);
     const bool fused = h->opt_path != MOE_PATH_MULTI && h->coop && bmoe::fused_supported(g) &&
                        (h->opt_path == MOE_PATH_FUSED || T <= 512);
@@ -401,6 +405,8 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
         fl.w2s = wb.w2s;
         fl.w13_rs = wb.w13_layout == MOE_W13_INTERLEAVED ? 2 : 1;
         fl.w13_up = wb.w13_layout == MOE_W13_INTERLEAVED ? 1 : g.I;
+        fl.y8 = y8;
+        fl.ys = ys;
         fl.swiglu_limit = static_cast<float>(h->swiglu_limit);
         fl.T = T;
         mark(1);
@@ -439,6 +445,8 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     a.E = g.E;
     a.swiglu_limit = static_cast<float>(h->swiglu_limit);
     a.status = ws.status;
+    a.y8 = y8;
+    a.ys = ys;
     a.trace = nullptr;
 #ifdef BMOE_TRACE
     static long long* trace_buf = nullptr;  // [2 GEMMs][2 CTAs][6][512] clock64 stamps
@@ -486,7 +494,7 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     if (e != cudaSuccess) return cuda_fail(h, e, "GEMM2 launch");
     h->launches += 1;
     mark(4);
-    e = bmoe::launch_combine(g, ws, topk_weights, T, num_valid_rows, static_cast<uint16_t*>(out), s);
+    e = bmoe::launch_combine(g, ws, topk_weights, T, num_valid_rows, static_cast<uint16_t*>(out), y8, ys, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
     h->launches += 1;
     mark(5);
@@ -524,6 +532,13 @@ int moe_set_option(moe_handle h, int key, double value) {
             if (static_cast<double>(v) != value || (v != MOE_W13_CONCAT && v != MOE_W13_INTERLEAVED))
                 return fail(h, MOE_EINVAL, "bad W13 layout %g", value);
             h->opt_w13_layout = v;
+            return MOE_OK;
+        }
+        case MOE_OPT_Y_FORMAT: {
+            const int v = static_cast<int>(value);
+            if (static_cast<double>(v) != value || (v != MOE_Y_BF16 && v != MOE_Y_MXFP8))
+                return fail(h, MOE_EINVAL, "bad GEMM2 row format %g", value);
+            h->y_format = v;
             return MOE_OK;
         }
         case MOE_OPT_LAYER_SLOTS: {
@@ -600,6 +615,7 @@ int moe_get_option(moe_handle h, int key, double* value) {
         case MOE_OPT_LAUNCHES: *value = static_cast<double>(h->launches); return MOE_OK;
         case MOE_OPT_PATH: *value = h->opt_path; return MOE_OK;
         case MOE_OPT_W13_LAYOUT: *value = h->opt_w13_layout; return MOE_OK;
+        case MOE_OPT_Y_FORMAT: *value = h->y_format; return MOE_OK;
         case MOE_OPT_LAYER_SLOTS: *value = static_cast<double>(h->slots.size()); return MOE_OK;
         case MOE_OPT_LAYER: *value = h->cur; return MOE_OK;
         default: return fail(h, MOE_EINVAL, "unknown option %d", key);

@@ -79,6 +79,8 @@ struct FusedArgs {
     int I;
     int w13_rs, w13_up;    // W13 scale rows: gate j at j * w13_rs, up j at j * w13_rs + w13_up
     int kc2;               // K chunks per GEMM2 stage (2 when I % 256 == 0)
+    uint8_t* y8;           // GEMM2 rows as MXFP8 codes / scales (nullptr: BF16 rows in ws.y)
+    uint8_t* ys;
     int nchunks;           // compact dispatch chunks
     int tiles_cap;
     float swiglu_limit;
@@ -306,7 +308,8 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
 // GEMM2 units; GEMM2: BF16 rows of y.  The accumulator is handed back before the stores.
 template <bool G2>
 __device__ __forceinline__ void epilogue_unit(const P1& p, uint64_t* acce_b, const Workspace& ws, const UnitInfo& cu,
-                                              int acc, int qd, int lane, int I, int H, float L) {
+                                              int acc, int qd, int lane, int I, int H, float L, uint8_t* y8,
+                                              uint8_t* ys) {
     const uint32_t tb = p.tmem + (static_cast<uint32_t>(32 * qd) << 16) + static_cast<uint32_t>(acc * F_ACC_COLS);
     const int feat = cu.m * 128 + 32 * qd + lane;
     float v[F_NT];
@@ -361,6 +364,10 @@ __device__ __forceinline__ void epilogue_unit(const P1& p, uint64_t* acce_b, con
                 if (lane == 0)
                     ws.hs[((size_t)cu.g * (I >> 7) + cu.m) * 512 + 16 * (c & 31) + 4 * (c >> 5) + qd] =
                         static_cast<uint8_t>(code);
+            } else if (y8) {  // MXFP8 row: this warp's 32 features are one 1x32 block
+                uint8_t sc;
+                y8[prow * H + feat] = rows::quant_block_warp(v[c], &sc);
+                if (lane == 0) ys[prow * (H >> 5) + (feat >> 5)] = sc;
             } else {
                 ws.y[prow * H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(v[c]));
             }
@@ -794,9 +801,9 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 fused_g2_prev = fu.g2;
 #endif
                 if (!fu.g2)
-                    epilogue_unit<false>(p, &acce[acc], ws, fu.u, acc, qd, lane, I, H, L);
+                    epilogue_unit<false>(p, &acce[acc], ws, fu.u, acc, qd, lane, I, H, L, f.y8, f.ys);
                 else
-                    epilogue_unit<true>(p, &acce[acc], ws, fu.u, acc, qd, lane, I, H, L);
+                    epilogue_unit<true>(p, &acce[acc], ws, fu.u, acc, qd, lane, I, H, L, f.y8, f.ys);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
@@ -830,6 +837,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         ca.T = T;
         ca.K = K;
         ca.H = H;
+        ca.y8 = f.y8;
+        ca.ys = f.ys;
         const int items = rows::combine_items(ca);
         for (int it = blockIdx.x * (blockDim.x >> 5) + warp; it < items; it += gridDim.x * (blockDim.x >> 5))
             rows::combine_item(ca, it, lane);
@@ -872,6 +881,8 @@ cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaun
     f.I = g.I;
     f.w13_rs = fl.w13_rs;
     f.w13_up = fl.w13_up;
+    f.y8 = fl.y8;
+    f.ys = fl.ys;
     f.kc2 = g.I % 256 == 0 ? 2 : 1;
     f.nchunks = (fl.T * g.K + kChunk - 1) / kChunk;
     f.tiles_cap = static_cast<int>(g.tiles_cap);

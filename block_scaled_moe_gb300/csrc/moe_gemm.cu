@@ -38,6 +38,7 @@
 #include <cuda_fp8.h>
 
 #include "gemm_common.cuh"
+#include "layer_rows.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -398,9 +399,16 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < CW; ++j) {
                         const int c = cbase + j;
-                        if (c < cu.n)
-                            a.y[static_cast<size_t>(cu.row0 + c) * a.H + featw] =
-                                __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+                        if (c < cu.n) {
+                            const size_t prow = static_cast<size_t>(cu.row0 + c);
+                            if (a.y8) {  // MXFP8 row: this warp's 32 features are one 1x32 block
+                                uint8_t sc;
+                                a.y8[prow * a.H + featw] = rows::quant_block_warp(v[j], &sc);
+                                if (lane == 0) a.ys[prow * (a.H >> 5) + (featw >> 5)] = sc;
+                            } else {
+                                a.y[prow * a.H + featw] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+                            }
+                        }
                     }
                 }
                 if (tracer) trace(a, 5, ui);
@@ -468,6 +476,10 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                         if (lane == 0)
                             a.hs[(static_cast<size_t>(cu.g) * (a.I >> 7) + cu.m) * 512 + 16 * (c & 31) +
                                  4 * (c >> 5) + q] = static_cast<uint8_t>(code);
+                    } else if (a.y8) {  // MXFP8 row: this warp's 32 features are one 1x32 block
+                        uint8_t sc;
+                        a.y8[prow * a.H + feat] = rows::quant_block_warp(v[j], &sc);
+                        if (lane == 0) a.ys[prow * (a.H >> 5) + (feat >> 5)] = sc;
                     } else {
                         a.y[prow * a.H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
                     }

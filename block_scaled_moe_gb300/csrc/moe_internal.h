@@ -68,8 +68,9 @@ cudaError_t launch_compact_dispatch(const Geometry& g, const Workspace& ws, cons
                                     const int32_t* nvr, cudaStream_t s);
 cudaError_t launch_quant_scatter(const Geometry& g, const Workspace& ws, const uint16_t* x, const int32_t* ids,
                                  int T, const int32_t* nvr, cudaStream_t s);
+// y8/ys non-null: the GEMM2 rows are MXFP8 codes and scales instead of BF16 y.
 cudaError_t launch_combine(const Geometry& g, const Workspace& ws, const float* wts, int T,
-                           const int32_t* nvr, uint16_t* out, cudaStream_t s);
+                           const int32_t* nvr, uint16_t* out, const uint8_t* y8, const uint8_t* ys, cudaStream_t s);
 
 // ------------------------------------------------------------------ GEMMs (moe_gemm.cu)
 struct GemmArgs {
@@ -85,6 +86,8 @@ struct GemmArgs {
     int up_off;            // GEMM1: row offset of up row j from gate row j (I concatenated, 1 interleaved)
     int w_rs;              // row stride of consecutive output features (1, or 2 for interleaved W13)
     int m_rows;            // weight rows per unit and operand tile index step: 128, or 256 for paired W2 tiles
+    uint8_t* y8;           // GEMM2 rows as MXFP8 codes [rows][H] (nullptr: BF16 rows in y)
+    uint8_t* ys;           // ... and their E8M0 scales [rows][H/32]
     int ktiles;            // K/128
     int mtiles;            // weight tiles (of 128 rows, or row pairs for GEMM1) per expert
     // activations: codes through the tensor map, scale atoms
@@ -118,6 +121,8 @@ struct FusedLaunch {
     int T;
     int w13_rs;  // W13 scale rows: gate row j of an expert at j * w13_rs, up row j at j * w13_rs + w13_up
     int w13_up;
+    uint8_t* y8;  // GEMM2 rows as MXFP8 (nullptr: BF16)
+    uint8_t* ys;
 };
 bool fused_supported(const Geometry& g);
 // tm_w13p: the W13 gate/up pair view (K, feature, half, expert), box {128, 128, 2, 1}.

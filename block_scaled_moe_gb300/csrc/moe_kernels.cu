@@ -296,7 +296,7 @@ cudaError_t launch_quant_scatter(const Geometry& g, const Workspace& ws, const u
 }
 
 cudaError_t launch_combine(const Geometry& g, const Workspace& ws, const float* wts, int T,
-                           const int32_t* /*nvr*/, uint16_t* out, cudaStream_t s) {
+                           const int32_t* /*nvr*/, uint16_t* out, const uint8_t* y8, const uint8_t* ys, cudaStream_t s) {
     rows::CombineArgs a;
     a.y = ws.y;
     a.yrow = ws.yrow;
@@ -305,6 +305,8 @@ cudaError_t launch_combine(const Geometry& g, const Workspace& ws, const float* 
     a.T = T;
     a.K = g.K;
     a.H = g.H;
+    a.y8 = y8;
+    a.ys = ys;
     const int items = T * ((g.H / 8 + rows::kCombineVecs - 1) / rows::kCombineVecs);
     k_combine<<<(items + 7) / 8, 256, 0, s>>>(a);
     return cudaGetLastError();

@@ -95,6 +95,17 @@ typedef void* moe_stream_t;
 #define MOE_OPT_W13_LAYOUT 9      /* MOE_W13_*: row order of W13 assumed by the next bind */
 #define MOE_OPT_LAYER_SLOTS 10    /* number of layer slots (>= 1, default 1); see moe_bind_layer */
 #define MOE_OPT_LAYER 11          /* read-only: the current layer slot */
+#define MOE_OPT_Y_FORMAT 12       /* MOE_Y_*: GEMM2 rows handed to the combine */
+
+/* GEMM2 rows.  BF16: one BF16 row per route (default).  MXFP8: the rows go to
+ * the combine as 1x32 E4M3 codes with one E8M0 scale per 32 along H (ROCm/aiter
+ * PR #6881, Technical Details, small-input path: GEMM2 rows in the main path's
+ * 1x32 FP8 format instead of BF16), quantised from the float accumulator with
+ * the rule of the input rows and dequantised exactly by the combine.  Takes
+ * effect at the next forward; a captured graph keeps the format of capture.
+ * MOE_DBG_Y then holds the codes [rows][H] followed by the scales [rows][H/32]. */
+#define MOE_Y_BF16 0
+#define MOE_Y_MXFP8 1
 
 /* W13 row order.  CONCAT: rows [0,I) gate, rows [I,2I) up.  INTERLEAVED
  * (the gate-up-interleaved experts of the mega_moe reference in ROCm/aiter
