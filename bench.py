@@ -162,6 +162,21 @@ def traffic_for(kernel, workload):
     return None
 
 
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """The largest of every rank's `v` (the slowest rank's time); `v` itself on one rank."""
+    if world <= 1:
+        return float(v)
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(valid_rows_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job tokens/s: the valid rows of every rank's steps over the slowest rank's time."""
+    return valid_rows_per_step * steps * world / (max_ms / 1e3)
+
+
 def cpu_baseline(w, x, ids, wts, Wh, rows_n):
     import numpy as np
     import oracle
@@ -277,13 +292,9 @@ def main():
         torch.distributed.barrier()
     launches = layer.launches - launches0
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     tokens = w.nvr * args.steps * world
-    value = tokens / (total_ms / 1e3)
+    value = job_throughput(w.nvr, args.steps, world, total_ms)
 
     # ---- end to end: pinned host buffers, H2D inputs + forward + D2H output per step
     xh = x.pin_memory()
@@ -315,12 +326,8 @@ def main():
         e2e_step()
         ee[i].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee))
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = tokens / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(es, ee)), world, dev)
+    e2e_value = job_throughput(w.nvr, args.steps, world, e2e_ms)
 
     # ---- roofline of the dominant kernel from its live CUDA-event durations (stage slot 2 holds GEMM1, or
     # the whole fused kernel on the single-launch path)

@@ -1,0 +1,102 @@
+"""Expert-parallel host logic on two gloo ranks (CPU processes, no GPU).
+
+Each rank owns half of the experts and a shard of the tokens.  Dispatch, a local layer over the
+rank's own experts (the CPU oracle stands in for the GPU layer), and combine must give, for every
+token, the single-process oracle output within the layer tolerance (the partial rows are rounded to
+BF16 before the owner adds them).  The runtime choice follows the largest token count over the ranks.
+"""
+
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import synth
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, result_q):
+    import torch.distributed as dist
+    try:
+        os.environ["MASTER_ADDR"] = "127.0.0.1"
+        os.environ["MASTER_PORT"] = str(port)
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+        import oracle
+        from block_scaled_moe_gb300 import ep
+        from parity_util import compare
+
+        w = synth.micro(40, 256, 128, 8, 3, nvr=38, routing="uniform", invalid_frac=0.1, seed=77)
+        x, ids, wts, W = synth.make_all(w)
+        Wh = [t.cpu() for t in W]
+        per = ep.experts_per_rank(w.E, world)
+        # this rank's token shard (uneven on purpose) and its experts' weights
+        cut = 17
+        lo, hi = (0, cut) if rank == 0 else (cut, w.T)
+        nv_local = max(0, min(hi, w.nvr) - lo)
+        xl, idsl, wtsl = x[lo:hi], torch.from_numpy(ids[lo:hi]), torch.from_numpy(wts[lo:hi])
+        plan = ep.make_plan(idsl, wtsl, w.E, world, rank, num_valid_rows=nv_local)
+        rcv = ep.dispatch(plan, xl)
+        mine = [t[rank * per:(rank + 1) * per].contiguous() for t in Wh]
+        if rcv.x.shape[0]:
+            part = oracle.moe_forward(rcv.x, rcv.ids.numpy(), rcv.weights.numpy(), mine)
+            partial = torch.from_numpy(part.view(np.int16)).view(torch.bfloat16)
+        else:
+            partial = torch.zeros((0, w.H), dtype=torch.bfloat16)
+        out = ep.combine(plan, rcv, partial, hi - lo)
+        ref = oracle.moe_forward(x, ids, wts, Wh, num_valid_rows=w.nvr)[lo:hi]
+        got = out.view(torch.int16).numpy().view(np.uint16)
+        c = compare(got, ref)
+        zero_rows_ok = bool(np.all(got[nv_local:] == 0))
+        # runtime choice: the same answer on every rank, from the largest local count
+        choice_small = ep.select_runtime(hi - lo, small_max=25)    # max(17, 23) = 23 <= 25
+        choice_large = ep.select_runtime(hi - lo, small_max=20)    # 23 > 20
+        result_q.put((rank, c, zero_rows_ok, choice_small, choice_large, plan.send_counts, rcv.recv_counts))
+        dist.destroy_process_group()
+    except Exception as exc:  # pragma: no cover - reported to the parent
+        result_q.put((rank, repr(exc), None, None, None, None, None))
+
+
+def test_ep_dispatch_combine_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = {}
+    for _ in range(2):
+        r = q.get(timeout=300)
+        res[r[0]] = r
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank in range(2):
+        _, c, zero_ok, small, large, sent, recv = res[rank]
+        assert isinstance(c, dict), c
+        assert c["nan"] == 0 and c["rel_l2"] <= 1e-2 and c["bad"] == 0, (rank, c)
+        assert zero_ok
+        assert small == "decode" and large == "large"
+    # what rank a sends to rank b is what b receives from a
+    assert res[0][5][1] == res[1][6][0] and res[1][5][0] == res[0][6][1]
+
+
+def test_plan_routes_each_row_once_per_owner():
+    from block_scaled_moe_gb300 import ep
+    ids = torch.tensor([[0, 5], [1, 2], [7, 6], [-1, 3], [4, 4]], dtype=torch.int32)
+    w = torch.tensor([[0.6, 0.4], [0.5, 0.5], [0.9, 0.1], [0.0, 1.0], [0.3, 0.7]])
+    plan = ep.make_plan(ids, w, E=8, world=2, rank=0, num_valid_rows=4)
+    # experts 0-3 on rank 0, 4-7 on rank 1; row 4 is past the row count
+    assert plan.send_counts == [3, 2]
+    assert plan.send_rows.tolist() == [0, 1, 3, 0, 2]
+    assert plan.ids.tolist() == [[0, -1], [1, 2], [-1, 3], [-1, 1], [3, 2]]
+    assert torch.allclose(plan.weights, torch.tensor([[0.6, 0], [0.5, 0.5], [0, 1.0], [0, 0.4], [0.9, 0.1]]))
+    with pytest.raises(ValueError):
+        ep.make_plan(ids, w, E=8, world=3, rank=0)
