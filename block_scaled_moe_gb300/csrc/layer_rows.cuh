@@ -168,7 +168,7 @@ __device__ __forceinline__ int combine_items(const CombineArgs& a) {
     return a.T * ((a.H / 8 + kCombineVecs - 1) / kCombineVecs);
 }
 
-__device__ __forceinline__ void combine_item(const CombineArgs& a, int item, int lane) {
+__device__ __forceinline__ void combine_item_bf16(const CombineArgs& a, int item, int lane) {
     const int segs = (a.H / 8 + kCombineVecs - 1) / kCombineVecs;
     const int t = item / segs, seg = item - t * segs;
     int r_l = -1;
@@ -194,31 +194,14 @@ __device__ __forceinline__ void combine_item(const CombineArgs& a, int item, int
         for (int k = 0; k < kMaxTopk; ++k) {
             if (k >= a.K || rows[k] < 0) continue;
             any = true;
+            const uint4 q = __ldcg(reinterpret_cast<const uint4*>(a.y + (size_t)rows[k] * a.H) + v);
+            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
             const float wv = wk[k];
-            float yv[8];
-            if (a.y8) {  // MXFP8 row: 8 codes and the scale of their 32-block (exact dequantisation)
-                const uint2 q = __ldcg(reinterpret_cast<const uint2*>(a.y8 + (size_t)rows[k] * a.H) + v);
-                const float sc = e8m0_value(__ldcg(a.ys + (size_t)rows[k] * (a.H >> 5) + (v >> 2)));
-                const uint32_t w2[2] = {q.x, q.y};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
-                        static_cast<__nv_fp8x2_storage_t>((w2[j >> 1] >> (16 * (j & 1))) & 0xffffu), __NV_E4M3);
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-                    yv[2 * j] = f.x * sc;
-                    yv[2 * j + 1] = f.y * sc;
-                }
-            } else {
-                const uint4 q = __ldcg(reinterpret_cast<const uint4*>(a.y + (size_t)rows[k] * a.H) + v);
-                const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    yv[2 * j] = __uint_as_float(w4[j] << 16);
-                    yv[2 * j + 1] = __uint_as_float(w4[j] & 0xffff0000u);
-                }
+            for (int j = 0; j < 4; ++j) {
+                acc[2 * j] = __fadd_rn(acc[2 * j], __fmul_rn(wv, __uint_as_float(w4[j] << 16)));
+                acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __fmul_rn(wv, __uint_as_float(w4[j] & 0xffff0000u)));
             }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], __fmul_rn(wv, yv[j]));
         }
         uint4 o = make_uint4(0, 0, 0, 0);
         if (any) {
@@ -232,6 +215,78 @@ __device__ __forceinline__ void combine_item(const CombineArgs& a, int item, int
         }
         reinterpret_cast<uint4*>(a.out + (size_t)t * a.H)[v] = o;
     }
+}
+
+// MXFP8 GEMM2 rows: slots taken one at a time (row and weight shuffled from lane k), so that the
+// dequantisation's registers do not add to a per-slot table.
+__device__ __forceinline__ void combine_item_fp8(const CombineArgs& a, int item, int lane) {
+    constexpr int kPer = kCombineVecs / 32;  // vectors per lane in one item
+    const int segs = (a.H / 8 + kCombineVecs - 1) / kCombineVecs;
+    const int t = item / segs, seg = item - t * segs;
+    int r_l = -1;
+    float w_l = 0.f;
+    if (lane < a.K) {
+        r_l = __ldcg(a.yrow + (size_t)t * a.K + lane);
+        w_l = a.w[(size_t)t * a.K + lane];
+    }
+    const int v1 = min(a.H >> 3, (seg + 1) * kCombineVecs);
+    float acc[kPer][8];
+#pragma unroll
+    for (int it = 0; it < kPer; ++it)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[it][j] = 0.f;
+    bool any = false;
+    for (int k = 0; k < a.K; ++k) {  // slots in ascending k: each element's sum keeps that order
+        const int rk = __shfl_sync(kFull, r_l, k);
+        const float wv = __shfl_sync(kFull, w_l, k);
+        if (rk < 0) continue;
+        any = true;
+#pragma unroll
+        for (int it = 0; it < kPer; ++it) {
+            const int v = seg * kCombineVecs + lane + 32 * it;
+            if (v >= v1) continue;
+            float yv[8];
+            {  // MXFP8 row: 8 codes and the scale of their 32-block (exact dequantisation)
+                const uint2 q = __ldcg(reinterpret_cast<const uint2*>(a.y8 + (size_t)rk * a.H) + v);
+                const float sc = e8m0_value(__ldcg(a.ys + (size_t)rk * (a.H >> 5) + (v >> 2)));
+                const uint32_t w2[2] = {q.x, q.y};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+                        static_cast<__nv_fp8x2_storage_t>((w2[j >> 1] >> (16 * (j & 1))) & 0xffffu), __NV_E4M3);
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+                    yv[2 * j] = f.x * sc;
+                    yv[2 * j + 1] = f.y * sc;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[it][j] = __fadd_rn(acc[it][j], __fmul_rn(wv, yv[j]));
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < kPer; ++it) {
+        const int v = seg * kCombineVecs + lane + 32 * it;
+        if (v >= v1) continue;
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (any) {
+            uint32_t ow[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __nv_bfloat162 b = __floats2bfloat162_rn(acc[it][2 * j], acc[it][2 * j + 1]);
+                ow[j] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+        reinterpret_cast<uint4*>(a.out + (size_t)t * a.H)[v] = o;
+    }
+}
+
+// Work item -> the combine of one row segment, from BF16 or MXFP8 GEMM2 rows.
+__device__ __forceinline__ void combine_item(const CombineArgs& a, int item, int lane) {
+    if (a.y8)
+        combine_item_fp8(a, item, lane);
+    else
+        combine_item_bf16(a, item, lane);
 }
 
 }  // namespace rows

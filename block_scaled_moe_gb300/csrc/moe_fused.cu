@@ -350,6 +350,18 @@ __device__ __forceinline__ void epilogue_unit(const P1& p, uint64_t* acce_b, con
     }
     tc_fence_before();
     mbar_arrive(acce_b);
+    if (G2 && y8) {  // MXFP8 GEMM2 rows: this warp's 32 features are one 1x32 block
+#pragma unroll
+        for (int c = 0; c < F_NT; ++c) {
+            if (c < cu.n) {
+                const size_t prow = static_cast<size_t>(cu.row0 + c);
+                uint8_t sc;
+                y8[prow * H + feat] = rows::quant_block_warp(v[c], &sc);
+                if (lane == 0) ys[prow * (H >> 5) + (feat >> 5)] = sc;
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int c = 0; c < F_NT; ++c) {
         if (c < cu.n) {
@@ -364,10 +376,6 @@ __device__ __forceinline__ void epilogue_unit(const P1& p, uint64_t* acce_b, con
                 if (lane == 0)
                     ws.hs[((size_t)cu.g * (I >> 7) + cu.m) * 512 + 16 * (c & 31) + 4 * (c >> 5) + qd] =
                         static_cast<uint8_t>(code);
-            } else if (y8) {  // MXFP8 row: this warp's 32 features are one 1x32 block
-                uint8_t sc;
-                y8[prow * H + feat] = rows::quant_block_warp(v[c], &sc);
-                if (lane == 0) ys[prow * (H >> 5) + (feat >> 5)] = sc;
             } else {
                 ws.y[prow * H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(v[c]));
             }

@@ -396,18 +396,24 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                     tc_fence_before();
                     mbar_arrive(&acce[w]);
                     const int featw = cu.m * a.m_rows + w * 128 + 32 * q + lane;
+                    if (a.y8) {  // MXFP8 rows: this warp's 32 features are one 1x32 block
 #pragma unroll
-                    for (int j = 0; j < CW; ++j) {
-                        const int c = cbase + j;
-                        if (c < cu.n) {
-                            const size_t prow = static_cast<size_t>(cu.row0 + c);
-                            if (a.y8) {  // MXFP8 row: this warp's 32 features are one 1x32 block
+                        for (int j = 0; j < CW; ++j) {
+                            const int c = cbase + j;
+                            if (c < cu.n) {
+                                const size_t prow = static_cast<size_t>(cu.row0 + c);
                                 uint8_t sc;
                                 a.y8[prow * a.H + featw] = rows::quant_block_warp(v[j], &sc);
                                 if (lane == 0) a.ys[prow * (a.H >> 5) + (featw >> 5)] = sc;
-                            } else {
-                                a.y[prow * a.H + featw] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
                             }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < CW; ++j) {
+                            const int c = cbase + j;
+                            if (c < cu.n)
+                                a.y[static_cast<size_t>(cu.row0 + c) * a.H + featw] =
+                                    __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
                         }
                     }
                 }
@@ -461,6 +467,19 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
             } else {
                 acc_phase ^= 1u;
             }
+            if (!G1 && a.y8) {  // MXFP8 GEMM2 rows: this warp's 32 features are one 1x32 block
+#pragma unroll
+                for (int j = 0; j < CW; ++j) {
+                    const int c = cbase + j;
+                    if (c < cu.n) {
+                        const size_t prow = static_cast<size_t>(cu.row0 + c);
+                        uint8_t sc;
+                        a.y8[prow * a.H + feat] = rows::quant_block_warp(v[j], &sc);
+                        if (lane == 0) a.ys[prow * (a.H >> 5) + (feat >> 5)] = sc;
+                    }
+                }
+                continue;
+            }
 #pragma unroll
             for (int j = 0; j < CW; ++j) {
                 const int c = cbase + j;
@@ -476,10 +495,6 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                         if (lane == 0)
                             a.hs[(static_cast<size_t>(cu.g) * (a.I >> 7) + cu.m) * 512 + 16 * (c & 31) +
                                  4 * (c >> 5) + q] = static_cast<uint8_t>(code);
-                    } else if (a.y8) {  // MXFP8 row: this warp's 32 features are one 1x32 block
-                        uint8_t sc;
-                        a.y8[prow * a.H + feat] = rows::quant_block_warp(v[j], &sc);
-                        if (lane == 0) a.ys[prow * (a.H >> 5) + (feat >> 5)] = sc;
                     } else {
                         a.y[prow * a.H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
                     }

@@ -196,10 +196,16 @@ __global__ void __launch_bounds__(256) k_quant_scatter(rows::QuantArgs a, const 
 
 // ---------------------------------------------------------------- combine
 // One warp per output row (rows::combine_row).
+// Two instances so that the BF16 one keeps its small register footprint (occupancy: the combine
+// is bound by memory latency).
+template <bool FP8>
 __global__ void __launch_bounds__(256) k_combine(rows::CombineArgs a) {
     const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (item >= rows::combine_items(a)) return;
-    rows::combine_item(a, item, threadIdx.x & 31);
+    if constexpr (FP8)
+        rows::combine_item_fp8(a, item, threadIdx.x & 31);
+    else
+        rows::combine_item_bf16(a, item, threadIdx.x & 31);
 }
 
 DispatchArgs dispatch_args(const Geometry& g, const Workspace& ws, const int32_t* ids, int T, const int32_t* nvr) {
@@ -308,7 +314,10 @@ cudaError_t launch_combine(const Geometry& g, const Workspace& ws, const float* 
     a.y8 = y8;
     a.ys = ys;
     const int items = T * ((g.H / 8 + rows::kCombineVecs - 1) / rows::kCombineVecs);
-    k_combine<<<(items + 7) / 8, 256, 0, s>>>(a);
+    if (y8)
+        k_combine<true><<<(items + 7) / 8, 256, 0, s>>>(a);
+    else
+        k_combine<false><<<(items + 7) / 8, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 
