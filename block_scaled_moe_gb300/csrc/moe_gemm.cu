@@ -76,21 +76,24 @@ struct Cfg {
     static constexpr int SF_SLOTS = 2;                     // scale slots per chain (alternating stages)
     static constexpr int SF_SLOT_COLS = 8 * KC;            // KC weight atoms then KC row atoms, 4 columns each
     static constexpr int SF_BASE = 512 - MW * SF_SLOTS * SF_SLOT_COLS;
-    static constexpr int NUM_ACC = (2 * ACC_COLS <= SF_BASE) ? 2 : 1;
+    // 128-row tiles with two chains (GEMM1 gate/up, paired W2 tiles) cannot double-buffer 2 x 256
+    // columns next to the scale columns; they rotate three single-chain slots instead: unit u's chain w
+    // accumulates in slot (2u + w) % 3, each slot with its own full / free barriers, so the next unit's
+    // first chain always finds a free slot and its second waits only for one drained slot.
+    static constexpr bool ROT3 = PAIR && NT == 128;
+    static constexpr int NUM_ACC = ROT3 ? 1 : ((2 * ACC_COLS <= SF_BASE) ? 2 : 1);
     // warps: 0 TMA producer, 1 scale producer, 2..1+NI MMA issuers, then EW epilogue warps
     static constexpr int MMA_WARP0 = 2;
     static constexpr int EPI_WARP0 = 2 + NI;
     static constexpr int THREADS = 32 * (2 + NI + EW);
-    // WIDE units release their two single-buffered accumulator chains one at a time
-    static constexpr bool PER_CHAIN = WIDE;
-    static constexpr int BAR_BYTES = (2 * STAGES + 2 + 4 + 1) * 8 + 16;
+    static constexpr int BAR_BYTES = (2 * STAGES + 4 + 4 + 1) * 8 + 16;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + TAB_BYTES + BAR_BYTES;
     static_assert(NUM_ACC * ACC_COLS <= SF_BASE, "TMEM columns");
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(4 % KS == 0, "K-steps per stage must split evenly");
     static_assert(!G1 || KC == 1, "GEMM1 stages hold one K chunk (the W13 pair box)");
     static_assert(!WIDE || (!G1 && NT == 128 && KC == 1), "wide units: GEMM2, 128-row route tiles");
-    static_assert(!PER_CHAIN || NUM_ACC == 1, "per-chain release of a single-buffered accumulator");
+    static_assert(!ROT3 || (MW == 2 && NI == 2 && 3 * NT <= SF_BASE), "three rotating slots");
     static_assert(MW <= 4, "barrier slots");
     static_assert(CW % 16 == 0, "epilogue column split");
 };
@@ -110,8 +113,8 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
     uint8_t* sSFB = sSFA + STAGES * NA * KC * 512;
     uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * KC * 512);
     uint64_t* empty = full + STAGES;
-    uint64_t* accf = empty + STAGES;
-    uint64_t* acce = accf + 2;  // [2] accumulator sets, or [MW] chains when PER_CHAIN
+    uint64_t* accf = empty + STAGES;  // accumulator full: [2] sets, or [3] rotating slots (ROT3)
+    uint64_t* acce = accf + 4;        // accumulator free, same indexing
     uint64_t* drain = acce + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -138,8 +141,10 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
             mbar_init(&full[s], 1 + 32);  // TMA issuer + the 32 scale-copying lanes
             mbar_init(&empty[s], NI);
         }
-        for (int b = 0; b < 2; ++b) mbar_init(&accf[b], NI);
-        for (int b = 0; b < 4; ++b) mbar_init(&acce[b], 32 * C::EW);
+        for (int b = 0; b < 4; ++b) {
+            mbar_init(&accf[b], C::ROT3 ? 1 : NI);  // ROT3: one chain (one issuing warp) per slot use
+            mbar_init(&acce[b], 32 * C::EW);
+        }
         mbar_init(drain, NI);
         *abort_flag = 0;
         fence_mbar_init();
@@ -274,11 +279,14 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
         for (int ui = 0; ui < my_units && ok; ++ui) {
             const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
             const int N = (cu.n + 15) & ~15;
-            if constexpr (C::PER_CHAIN) {
-                for (int w = wi; w < MW && ok; w += NI)
-                    ok = mbar_wait(&acce[w], acc_phase ^ 1u, abort_flag, a.status,
-                                   kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs);
-                if (!ok) break;
+            // ROT3: this warp's one chain (w = wi) uses slot (2 ui + wi) % 3, its (2 ui + wi) / 3-th use
+            const int rq = 2 * ui + wi, rslot = rq % 3;
+            if constexpr (C::ROT3) {
+                if (!mbar_wait(&acce[rslot], ((rq / 3) & 1u) ^ 1u, abort_flag, a.status,
+                               kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
             } else if (!mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, a.status,
                                   kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs)) {
                 ok = false;
@@ -304,7 +312,8 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                         const int op = PAIR ? (w & 1) : 0;
                         const int kfirst = PAIR ? (w >> 1) : w * G2S;
                         const int c_lo = PAIR ? 0 : (w * G2S) >> 2, c_hi = PAIR ? KC - 1 : (w * G2S + G2S - 1) >> 2;
-                        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * C::ACC_COLS + w * NT);
+                        const uint32_t d_tmem =
+                            tmem + static_cast<uint32_t>(C::ROT3 ? rslot * NT : acc * C::ACC_COLS + w * NT);
                         const uint32_t sfc = tmem + static_cast<uint32_t>(
                                                         C::SF_BASE + (w * C::SF_SLOTS + (job & 1)) * C::SF_SLOT_COLS);
 #pragma unroll
@@ -339,7 +348,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                 }
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(&accf[acc]);
+            if (lane == 0) tc_commit(&accf[C::ROT3 ? rslot : acc]);
             __syncwarp();
             if (C::NUM_ACC == 2) {
                 acc ^= 1;
@@ -369,103 +378,135 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
         const bool tracer = warp == C::EPI_WARP0 && lane == 0;
         for (int ui = 0; ui < my_units; ++ui) {
             const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
-            if (!mbar_wait(&accf[acc], acc_phase, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 5)),
-                           kWaitLimitNs))
-                break;
-            tc_fence_after();
-            if (tracer) trace(a, 4, ui);
-            const uint32_t tb =
-                tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * C::ACC_COLS);
-            if constexpr (WIDE) {
-                // chain w = W2 tile w of the pair: drain it, release it, store its BF16 rows
-#pragma unroll
-                for (int w = 0; w < MW; ++w) {
-                    float v[CW];
-#pragma unroll
-                    for (int h2 = 0; h2 < CW / 32; ++h2) {
-                        uint32_t r[2][16];
-#pragma unroll
-                        for (int j = 0; j < 2; ++j)
-                            if (cbase + 32 * h2 + 16 * j < cu.n) tmem_ld16(tb + w * NT + cbase + 32 * h2 + 16 * j, r[j]);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 2; ++j)
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) v[32 * h2 + 16 * j + i] = __uint_as_float(r[j][i]);
-                    }
-                    tc_fence_before();
-                    mbar_arrive(&acce[w]);
-                    const int featw = cu.m * a.m_rows + w * 128 + 32 * q + lane;
-                    if (a.y8) {  // MXFP8 rows: this warp's 32 features are one 1x32 block
-#pragma unroll
-                        for (int j = 0; j < CW; ++j) {
-                            const int c = cbase + j;
-                            if (c < cu.n) {
-                                const size_t prow = static_cast<size_t>(cu.row0 + c);
-                                uint8_t sc;
-                                a.y8[prow * a.H + featw] = rows::quant_block_warp(v[j], &sc);
-                                if (lane == 0) a.ys[prow * (a.H >> 5) + (featw >> 5)] = sc;
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < CW; ++j) {
-                            const int c = cbase + j;
-                            if (c < cu.n)
-                                a.y[static_cast<size_t>(cu.row0 + c) * a.H + featw] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
-                        }
-                    }
-                }
-                if (tracer) trace(a, 5, ui);
-                acc_phase ^= 1u;
-                continue;
-            }
             const int feat = cu.m * 128 + 32 * q + lane;
             float v[CW];  // GEMM1: h = SwiGLU(gate, up); GEMM2: y
+            if constexpr (C::ROT3) {
+                // chain by chain from its rotating slot; each slot is freed as soon as it is drained
+                bool ok = true;
 #pragma unroll
-            for (int j = 0; j < CW / 16; ++j) {
-                const int c0 = cbase + 16 * j;
-                if (c0 < cu.n) {
-                    uint32_t r[MW][16];
+                for (int w = 0; w < 2; ++w) {
+                    const int rq = 2 * ui + w, rslot = rq % 3;
+                    if (!mbar_wait(&accf[rslot], (rq / 3) & 1u, abort_flag, a.status,
+                                   kStTimeout | (1u << (kSiteShift + 5)), kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (tracer && w == 0) trace(a, 4, ui);
+                    const uint32_t tbs = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(rslot * NT);
 #pragma unroll
-                    for (int w = 0; w < MW; ++w) tmem_ld16(tb + w * NT + c0, r[w]);
-                    tmem_ld_wait();
+                    for (int j = 0; j < CW / 16; ++j) {  // 16 columns per load: the gate values stay live
+                        const int c0 = cbase + 16 * j;
+                        if (c0 < cu.n) {
+                            uint32_t r[16];
+                            tmem_ld16(tbs + c0, r);
+                            tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float ga = 0.f, ub = 0.f;
-#pragma unroll
-                        for (int w = 0; w < MW; ++w) {
-                            if (G1 && (w & 1))
-                                ub += __uint_as_float(r[w][i]);
-                            else
-                                ga += __uint_as_float(r[w][i]);
+                            for (int i = 0; i < 16; ++i) {
+                                const int vi = 16 * j + i;
+                                if constexpr (G1) {
+                                    if (w == 0) {
+                                        v[vi] = 0.f + __uint_as_float(r[i]);  // gate (+0 like the chain sums)
+                                    } else {
+                                        float ga = v[vi], ub = 0.f + __uint_as_float(r[i]);
+                                        if (a.g_dbg && c0 + i < cu.n) {
+                                            const size_t prow = static_cast<size_t>(cu.row0 + c0 + i);
+                                            a.g_dbg[prow * 2 * a.I + feat] = ga;
+                                            a.g_dbg[prow * 2 * a.I + a.I + feat] = ub;
+                                        }
+                                        if (L > 0.f) {
+                                            ga = fminf(ga, L);
+                                            ub = fminf(fmaxf(ub, -L), L);
+                                        }
+                                        v[vi] = __fdividef(ga, 1.0f + __expf(-ga)) * ub;  // SwiGLU, fast intrinsics
+                                    }
+                                } else {
+                                    v[vi] = __uint_as_float(r[i]);
+                                }
+                            }
                         }
-                        if constexpr (G1) {
-                            if (a.g_dbg && c0 + i < cu.n) {
-                                const size_t prow = static_cast<size_t>(cu.row0 + c0 + i);
-                                a.g_dbg[prow * 2 * a.I + feat] = ga;
-                                a.g_dbg[prow * 2 * a.I + a.I + feat] = ub;
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&acce[rslot]);
+                    if constexpr (WIDE) {  // chain w = W2 tile w of the pair: store its rows now
+                        const int featw = cu.m * a.m_rows + w * 128 + 32 * q + lane;
+                        if (a.y8) {  // MXFP8 rows: this warp's 32 features are one 1x32 block
+#pragma unroll
+                            for (int j = 0; j < CW; ++j) {
+                                const int c = cbase + j;
+                                if (c < cu.n) {
+                                    const size_t prow = static_cast<size_t>(cu.row0 + c);
+                                    uint8_t sc;
+                                    a.y8[prow * a.H + featw] = rows::quant_block_warp(v[j], &sc);
+                                    if (lane == 0) a.ys[prow * (a.H >> 5) + (featw >> 5)] = sc;
+                                }
                             }
-                            if (L > 0.f) {
-                                ga = fminf(ga, L);
-                                ub = fminf(fmaxf(ub, -L), L);
-                            }
-                            v[16 * j + i] = __fdividef(ga, 1.0f + __expf(-ga)) * ub;  // SwiGLU, fast exp / divide intrinsics
                         } else {
-                            v[16 * j + i] = ga;
+#pragma unroll
+                            for (int j = 0; j < CW; ++j) {
+                                const int c = cbase + j;
+                                if (c < cu.n)
+                                    a.y[static_cast<size_t>(cu.row0 + c) * a.H + featw] =
+                                        __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+                            }
                         }
                     }
                 }
-            }
-            tc_fence_before();
-            if (tracer) trace(a, 5, ui);
-            mbar_arrive(&acce[acc]);
-            if (C::NUM_ACC == 2) {
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
+                if (!ok) break;
+                if (tracer) trace(a, 5, ui);
+                if constexpr (WIDE) continue;
             } else {
-                acc_phase ^= 1u;
+                if (!mbar_wait(&accf[acc], acc_phase, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 5)),
+                               kWaitLimitNs))
+                    break;
+                tc_fence_after();
+                if (tracer) trace(a, 4, ui);
+                const uint32_t tb =
+                    tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * C::ACC_COLS);
+#pragma unroll
+                for (int j = 0; j < CW / 16; ++j) {
+                    const int c0 = cbase + 16 * j;
+                    if (c0 < cu.n) {
+                        uint32_t r[MW][16];
+#pragma unroll
+                        for (int w = 0; w < MW; ++w) tmem_ld16(tb + w * NT + c0, r[w]);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float ga = 0.f, ub = 0.f;
+#pragma unroll
+                            for (int w = 0; w < MW; ++w) {
+                                if (G1 && (w & 1))
+                                    ub += __uint_as_float(r[w][i]);
+                                else
+                                    ga += __uint_as_float(r[w][i]);
+                            }
+                            if constexpr (G1) {
+                                if (a.g_dbg && c0 + i < cu.n) {
+                                    const size_t prow = static_cast<size_t>(cu.row0 + c0 + i);
+                                    a.g_dbg[prow * 2 * a.I + feat] = ga;
+                                    a.g_dbg[prow * 2 * a.I + a.I + feat] = ub;
+                                }
+                                if (L > 0.f) {
+                                    ga = fminf(ga, L);
+                                    ub = fminf(fmaxf(ub, -L), L);
+                                }
+                                v[16 * j + i] = __fdividef(ga, 1.0f + __expf(-ga)) * ub;  // SwiGLU, fast intrinsics
+                            } else {
+                                v[16 * j + i] = ga;
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                if (tracer) trace(a, 5, ui);
+                mbar_arrive(&acce[acc]);
+                if (C::NUM_ACC == 2) {
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1u;
+                } else {
+                    acc_phase ^= 1u;
+                }
             }
             if (!G1 && a.y8) {  // MXFP8 GEMM2 rows: this warp's 32 features are one 1x32 block
 #pragma unroll
