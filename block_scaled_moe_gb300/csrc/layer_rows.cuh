@@ -29,6 +29,7 @@ struct QuantArgs {
     const uint16_t* x;
     const int32_t* ids;
     int T, K, E, H, mtpr, words, NT, scheme;
+    int nb;  // 128-row scale atoms per route tile and K chunk
     Workspace ws;
 };
 
@@ -123,8 +124,8 @@ __device__ __forceinline__ void quant_scatter_seg(const QuantArgs& a, const int3
                 d[0] = o0;
                 d[1] = o1;
                 const int ci = ck[k];
-                a.ws.as[((size_t)gk[k] * ktiles + (blk >> 2)) * 512 + 16 * (ci & 31) + 4 * (ci >> 5) + (blk & 3)] =
-                    static_cast<uint8_t>(code);
+                a.ws.as[(((size_t)gk[k] * ktiles + (blk >> 2)) * a.nb + (ci >> 7)) * 512 + 16 * (ci & 31) +
+                        4 * ((ci >> 5) & 3) + (blk & 3)] = static_cast<uint8_t>(code);
             }
         }
     }

@@ -150,8 +150,11 @@ void compute_geometry(moe_ctx* h, Geometry* g) {
     g->mtpr = g->cap;
     g->words = (g->cap + 31) / 32;
     int NT = h->route_tile;
-    if (NT == 0) NT = ((long long)g->cap * g->K <= 8LL * g->E) ? 32 : 128;
+    // decode tiles of 32 rows; prefill tiles of 144: most experts of a uniform 8192-row prefill hold
+    // 110-150 routes, which 128-row tiles would split into a full tile and a nearly empty one
+    if (NT == 0) NT = ((long long)g->cap * g->K <= 8LL * g->E) ? 32 : 144;
     g->NT = NT;
+    g->nb = (NT + 127) / 128;
     const long long slots = (long long)g->cap * g->K;
     if (fixed) {
         g->rows_cap = (long long)g->E * g->mtpr;
@@ -477,8 +480,8 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     h->launches += 1;
     mark(3);
     // GEMM2: W2 x h rows, K = I
-    // 128-row route tiles take W2 tiles in pairs (one 256-row box, two accumulator chains)
-    const bool w2_pairs = g.NT == 128 && g.H % 256 == 0;
+    // prefill route tiles take W2 tiles in pairs (one 256-row box, two accumulator chains)
+    const bool w2_pairs = g.NT >= 128 && g.H % 256 == 0;
     a.w_sf = wb.w2s;
     a.w_rows = g.H;
     a.ld_sf = g.I / 32;
@@ -578,7 +581,8 @@ int moe_set_option(moe_handle h, int key, double value) {
             } else if (key == MOE_OPT_DEBUG_CAPTURE) {
                 h->debug = v ? 1 : 0;
             } else {
-                if (v != 0 && v != 32 && v != 128) return fail(h, MOE_EINVAL, "route tile must be 0, 32 or 128");
+                if (v != 0 && v != 32 && v != 128 && v != 144)
+                    return fail(h, MOE_EINVAL, "route tile must be 0, 32, 128 or 144");
                 h->route_tile = v;
             }
             Geometry g;

@@ -879,6 +879,7 @@ cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaun
     f.q.mtpr = g.mtpr;
     f.q.words = g.words;
     f.q.NT = g.NT;
+    f.q.nb = g.nb;
     f.q.scheme = g.scheme;
     f.q.ws = ws;
     f.nvr = fl.nvr;

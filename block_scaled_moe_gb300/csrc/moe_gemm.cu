@@ -59,7 +59,8 @@ struct Cfg {
     // reads (two codes per byte), not the 16-byte-aligned footprint it writes.
     static constexpr int A_TX = 128 * 128 / 2;
     static constexpr int B_BYTES = NT * 128;               // one row chunk in smem
-    static constexpr int STAGE_BYTES = KC * (NA * A_BYTES + B_BYTES + (NA + 1) * 512);
+    static constexpr int NB = (NT + 127) / 128;            // 128-row scale atoms per row chunk
+    static constexpr int STAGE_BYTES = KC * (NA * A_BYTES + B_BYTES + (NA + NB) * 512);
     static constexpr int TAB_E = 512;                      // experts whose plan fits the smem tables
     static constexpr int TAB_BYTES = 4 * (3 * TAB_E + 4);
     static constexpr int STAGES = (220 * 1024 - TAB_BYTES) / STAGE_BYTES > 12 ? 12
@@ -74,13 +75,14 @@ struct Cfg {
     static constexpr int CW = NT / (EW / 4);               // accumulator columns per epilogue warp
     static constexpr int ACC_COLS = MW * NT;               // one accumulator set: MW chains of NT columns
     static constexpr int SF_SLOTS = 2;                     // scale slots per chain (alternating stages)
-    static constexpr int SF_SLOT_COLS = 8 * KC;            // KC weight atoms then KC row atoms, 4 columns each
+    // KC weight atoms, then KC x NB row atoms, 4 columns each (row atom b holds rows 128 b .. 128 b + 127)
+    static constexpr int SF_SLOT_COLS = 4 * KC * (1 + NB);
     static constexpr int SF_BASE = 512 - MW * SF_SLOTS * SF_SLOT_COLS;
     // 128-row tiles with two chains (GEMM1 gate/up, paired W2 tiles) cannot double-buffer 2 x 256
     // columns next to the scale columns; they rotate three single-chain slots instead: unit u's chain w
     // accumulates in slot (2u + w) % 3, each slot with its own full / free barriers, so the next unit's
     // first chain always finds a free slot and its second waits only for one drained slot.
-    static constexpr bool ROT3 = PAIR && NT == 128;
+    static constexpr bool ROT3 = PAIR && NT >= 128;
     static constexpr int NUM_ACC = ROT3 ? 1 : ((2 * ACC_COLS <= SF_BASE) ? 2 : 1);
     // warps: 0 TMA producer, 1 scale producer, 2..1+NI MMA issuers, then EW epilogue warps
     static constexpr int MMA_WARP0 = 2;
@@ -92,11 +94,21 @@ struct Cfg {
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(4 % KS == 0, "K-steps per stage must split evenly");
     static_assert(!G1 || KC == 1, "GEMM1 stages hold one K chunk (the W13 pair box)");
-    static_assert(!WIDE || (!G1 && NT == 128 && KC == 1), "wide units: GEMM2, 128-row route tiles");
+    static_assert(!WIDE || (!G1 && NT >= 128 && KC == 1), "wide units: GEMM2, prefill route tiles");
     static_assert(!ROT3 || (MW == 2 && NI == 2 && 3 * NT <= SF_BASE), "three rotating slots");
     static_assert(MW <= 4, "barrier slots");
-    static_assert(CW % 16 == 0, "epilogue column split");
+    static_assert(CW % 8 == 0, "epilogue column split");
+    static constexpr int LDC = CW % 16 == 0 ? 16 : 8;      // TMEM columns per epilogue load
 };
+
+// LDC-column TMEM load (32 lanes x 32 bit) of the epilogue
+template <int L>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[L]) {
+    if constexpr (L == 16)
+        tmem_ld16(taddr, r);
+    else
+        tmem_ld8(taddr, r);
+}
 
 template <bool G1, int NT, int KC, bool WIDE>
 __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
@@ -107,18 +119,19 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = sm;
-    // per stage: sA [NA][KC] chunks, sB [KC] chunks, sSFA [NA][KC] atoms, sSFB [KC] atoms
+    // per stage: sA [NA][KC] chunks, sB [KC] chunks, sSFA [NA][KC] atoms, sSFB [KC][NB] atoms
+    constexpr int NB = C::NB;
     uint8_t* sB = sA + STAGES * NA * KC * C::A_BYTES;
     uint8_t* sSFA = sB + STAGES * KC * C::B_BYTES;
     uint8_t* sSFB = sSFA + STAGES * NA * KC * 512;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * KC * 512);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * KC * NB * 512);
     uint64_t* empty = full + STAGES;
     uint64_t* accf = empty + STAGES;  // accumulator full: [2] sets, or [3] rotating slots (ROT3)
     uint64_t* acce = accf + 4;        // accumulator free, same indexing
     uint64_t* drain = acce + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int32_t* tab = reinterpret_cast<int32_t*>(sSFB + STAGES * KC * 512 + C::BAR_BYTES);
+    int32_t* tab = reinterpret_cast<int32_t*>(sSFB + STAGES * KC * NB * 512 + C::BAR_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntiles = __ldg(a.tile_base + a.E);
@@ -172,7 +185,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
             for (int ui = 0; ui < my_units && ok; ++ui) {
                 const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
                 const int wrow = cu.e * a.w_rows + cu.m * a.m_rows;  // GEMM2 (GEMM1 reads the W13 pair view)
-                const uint8_t* b_sf = a.b_sf + static_cast<size_t>(cu.g) * a.ktiles * 512;
+                const uint8_t* b_sf = a.b_sf + static_cast<size_t>(cu.g) * a.ktiles * NB * 512;
                 for (int kk = 0; kk < KT; ++kk) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
                                    kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
@@ -180,7 +193,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                         break;
                     }
                     trace(a, 0, issued);
-                    mbar_expect_tx(&full[stage], KC * (NA * C::A_TX + C::B_BYTES + 512));
+                    mbar_expect_tx(&full[stage], KC * (NA * C::A_TX + C::B_BYTES + NB * 512));
 #pragma unroll
                     for (int c = 0; c < KC; ++c) {
                         const int k0 = (kk * KC + c) * 128;
@@ -191,7 +204,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                             tma_load_2d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0, wrow, pol_w);
                         tma_load_2d(sB + (stage * KC + c) * C::B_BYTES, &tm_b, &full[stage], k0, cu.row0, pol_b);
                     }
-                    bulk_load(sSFB + stage * KC * 512, b_sf + kk * KC * 512, KC * 512, &full[stage]);
+                    bulk_load(sSFB + stage * KC * NB * 512, b_sf + kk * KC * NB * 512, KC * NB * 512, &full[stage]);
                     mbar_arrive(&full[stage]);
                     trace(a, 1, issued);
                     ++issued;
@@ -321,7 +334,10 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                             if (c < c_lo || c > c_hi) continue;
                             tc_cp_32x128b_x4(sfc + 4 * c,
                                              desc_sf_atom(smem_u32(sSFA + ((stage * NA + op) * KC + c) * 512)));
-                            tc_cp_32x128b_x4(sfc + 4 * KC + 4 * c, desc_sf_atom(smem_u32(sSFB + (stage * KC + c) * 512)));
+#pragma unroll
+                            for (int b = 0; b < NB; ++b)
+                                tc_cp_32x128b_x4(sfc + 4 * KC + 4 * (c * NB + b),
+                                                 desc_sf_atom(smem_u32(sSFB + ((stage * KC + c) * NB + b) * 512)));
                         }
 #pragma unroll
                         for (int k = 0; k < 4 * KC; ++k) {
@@ -333,7 +349,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                             const uint64_t db = desc_kmajor_sw128(smem_u32(sB + (stage * KC + c) * C::B_BYTES)) +
                                                 static_cast<uint64_t>((k4 * 32) >> 4);
                             const uint32_t idesc = idesc_mx(128, N, 5, 0, k4, k4);
-                            tc_mma_mx(d_tmem, da, db, idesc, sfc + 4 * c, sfc + 4 * KC + 4 * c,
+                            tc_mma_mx(d_tmem, da, db, idesc, sfc + 4 * c, sfc + 4 * KC + 4 * NB * c,
                                       (kk > 0 || k != kfirst) ? 1u : 0u);
                         }
                     }
@@ -394,16 +410,17 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                     tc_fence_after();
                     if (tracer && w == 0) trace(a, 4, ui);
                     const uint32_t tbs = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(rslot * NT);
+                    constexpr int LDC = C::LDC;
 #pragma unroll
-                    for (int j = 0; j < CW / 16; ++j) {  // 16 columns per load: the gate values stay live
-                        const int c0 = cbase + 16 * j;
+                    for (int j = 0; j < CW / LDC; ++j) {  // LDC columns per load: the gate values stay live
+                        const int c0 = cbase + LDC * j;
                         if (c0 < cu.n) {
-                            uint32_t r[16];
-                            tmem_ld16(tbs + c0, r);
+                            uint32_t r[LDC];
+                            tmem_ld_cols<LDC>(tbs + c0, r);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int vi = 16 * j + i;
+                            for (int i = 0; i < LDC; ++i) {
+                                const int vi = LDC * j + i;
                                 if constexpr (G1) {
                                     if (w == 0) {
                                         v[vi] = 0.f + __uint_as_float(r[i]);  // gate (+0 like the chain sums)
@@ -463,16 +480,17 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                 if (tracer) trace(a, 4, ui);
                 const uint32_t tb =
                     tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * C::ACC_COLS);
+                constexpr int LDC = C::LDC;
 #pragma unroll
-                for (int j = 0; j < CW / 16; ++j) {
-                    const int c0 = cbase + 16 * j;
+                for (int j = 0; j < CW / LDC; ++j) {
+                    const int c0 = cbase + LDC * j;
                     if (c0 < cu.n) {
-                        uint32_t r[MW][16];
+                        uint32_t r[MW][LDC];
 #pragma unroll
-                        for (int w = 0; w < MW; ++w) tmem_ld16(tb + w * NT + c0, r[w]);
+                        for (int w = 0; w < MW; ++w) tmem_ld_cols<LDC>(tb + w * NT + c0, r[w]);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
+                        for (int i = 0; i < LDC; ++i) {
                             float ga = 0.f, ub = 0.f;
 #pragma unroll
                             for (int w = 0; w < MW; ++w) {
@@ -491,9 +509,9 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                                     ga = fminf(ga, L);
                                     ub = fminf(fmaxf(ub, -L), L);
                                 }
-                                v[16 * j + i] = __fdividef(ga, 1.0f + __expf(-ga)) * ub;  // SwiGLU, fast intrinsics
+                                v[LDC * j + i] = __fdividef(ga, 1.0f + __expf(-ga)) * ub;  // SwiGLU, fast intrinsics
                             } else {
-                                v[16 * j + i] = ga;
+                                v[LDC * j + i] = ga;
                             }
                         }
                     }
@@ -534,8 +552,8 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                         const float mul = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
                         a.hq[prow * a.I + feat] = __nv_cvt_float_to_fp8(h * mul, __NV_SATFINITE, __NV_E4M3);
                         if (lane == 0)
-                            a.hs[(static_cast<size_t>(cu.g) * (a.I >> 7) + cu.m) * 512 + 16 * (c & 31) +
-                                 4 * (c >> 5) + q] = static_cast<uint8_t>(code);
+                            a.hs[((static_cast<size_t>(cu.g) * (a.I >> 7) + cu.m) * NB + (c >> 7)) * 512 +
+                                 16 * (c & 31) + 4 * ((c >> 5) & 3) + q] = static_cast<uint8_t>(code);
                     } else {
                         a.y[prow * a.H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
                     }
@@ -569,6 +587,9 @@ cudaError_t launch(const GemmArgs& a, const CUtensorMap* tw, const CUtensorMap* 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
     if ((e = set_attr<true, 128, 1, false>()) != cudaSuccess) return e;
+    if ((e = set_attr<true, 144, 1, false>()) != cudaSuccess) return e;
+    if ((e = set_attr<false, 144, 1, false>()) != cudaSuccess) return e;
+    if ((e = set_attr<false, 144, 1, true>()) != cudaSuccess) return e;
     if ((e = set_attr<true, 32, 1, false>()) != cudaSuccess) return e;
     if ((e = set_attr<false, 128, 1, false>()) != cudaSuccess) return e;
     if ((e = set_attr<false, 32, 1, false>()) != cudaSuccess) return e;
@@ -578,8 +599,9 @@ cudaError_t gemm_set_attributes() {
 
 cudaError_t launch_gemm1(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_x, int NT, int grid,
                          cudaStream_t s) {
-    return NT == 32 ? launch<true, 32, 1, false>(a, tm_w, tm_x, grid, s)
-                    : launch<true, 128, 1, false>(a, tm_w, tm_x, grid, s);
+    if (NT == 32) return launch<true, 32, 1, false>(a, tm_w, tm_x, grid, s);
+    return NT == 128 ? launch<true, 128, 1, false>(a, tm_w, tm_x, grid, s)
+                     : launch<true, 144, 1, false>(a, tm_w, tm_x, grid, s);
 }
 
 cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_w_wide,
@@ -587,9 +609,12 @@ cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUten
     // decode tiles stream W2 in 256-wide K stages when I allows it (halves the per-stage cost per byte)
     if (NT == 32) return a.ktiles % 2 == 0 ? launch<false, 32, 2, false>(a, tm_w, tm_h, grid, s)
                                            : launch<false, 32, 1, false>(a, tm_w, tm_h, grid, s);
-    // 128-row route tiles: pairs of W2 tiles (a.m_rows == 256) when H allows it
-    return a.m_rows == 256 ? launch<false, 128, 1, true>(a, tm_w_wide, tm_h, grid, s)
-                           : launch<false, 128, 1, false>(a, tm_w, tm_h, grid, s);
+    // prefill route tiles: pairs of W2 tiles (a.m_rows == 256) when H allows it
+    if (NT == 128)
+        return a.m_rows == 256 ? launch<false, 128, 1, true>(a, tm_w_wide, tm_h, grid, s)
+                               : launch<false, 128, 1, false>(a, tm_w, tm_h, grid, s);
+    return a.m_rows == 256 ? launch<false, 144, 1, true>(a, tm_w_wide, tm_h, grid, s)
+                           : launch<false, 144, 1, false>(a, tm_w, tm_h, grid, s);
 }
 
 }  // namespace bmoe

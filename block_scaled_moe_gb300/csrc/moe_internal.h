@@ -52,7 +52,8 @@ struct Geometry {
     int scheme;            // 1 fixed, 2 compact
     int mtpr;              // fixed-slot capacity per expert (= cap)
     int words;             // ceil(mtpr/32)
-    int NT;                // route tile width (MMA N upper bound)
+    int NT;                // route tile width (MMA N upper bound): 32 decode, 144 prefill (or 128)
+    int nb;                // 128-row scale atoms per route tile and K chunk: (NT + 127) / 128
     long long rows_cap;    // packed rows
     long long tiles_cap;   // route tiles
     int nchunks_cap;

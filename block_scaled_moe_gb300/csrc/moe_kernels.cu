@@ -247,9 +247,9 @@ size_t workspace_layout(const Geometry& g, char* base, Workspace* ws) {
     w.ticket = reinterpret_cast<uint32_t*>(carve(sizeof(uint32_t) * 4));
     w.status = reinterpret_cast<uint32_t*>(carve(sizeof(uint32_t) * 4));
     w.aq = reinterpret_cast<uint8_t*>(carve((size_t)g.rows_cap * g.H));
-    w.as = reinterpret_cast<uint8_t*>(carve((size_t)g.tiles_cap * (g.H / 128) * 512));
+    w.as = reinterpret_cast<uint8_t*>(carve((size_t)g.tiles_cap * (g.H / 128) * g.nb * 512));
     w.hq = reinterpret_cast<uint8_t*>(carve((size_t)g.rows_cap * g.I));
-    w.hs = reinterpret_cast<uint8_t*>(carve((size_t)g.tiles_cap * (g.I / 128) * 512));
+    w.hs = reinterpret_cast<uint8_t*>(carve((size_t)g.tiles_cap * (g.I / 128) * g.nb * 512));
     w.y = reinterpret_cast<uint16_t*>(carve((size_t)g.rows_cap * g.H * 2));
     w.ready = reinterpret_cast<uint32_t*>(carve(sizeof(uint32_t) * (size_t)g.tiles_cap));
     w.rids = reinterpret_cast<int32_t*>(carve(sizeof(int32_t) * slots));
@@ -294,6 +294,7 @@ cudaError_t launch_quant_scatter(const Geometry& g, const Workspace& ws, const u
     a.mtpr = g.mtpr;
     a.words = g.words;
     a.NT = g.NT;
+    a.nb = g.nb;
     a.scheme = g.scheme;
     a.ws = ws;
     const int items = T * ((g.H / 32 + rows::kQuantBlocks - 1) / rows::kQuantBlocks);

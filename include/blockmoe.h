@@ -74,7 +74,7 @@ typedef void* moe_stream_t;
 #define MOE_OPT_FIXED_SLOT_MAX 3  /* fixed-slot threshold on capacity, default 255
                                      (vLLM PR #61262: FIXED_SLOT_MAX_MTPR) */
 #define MOE_OPT_DEBUG_CAPTURE 4   /* 1 = also keep canonical MXFP8 codes of x and raw GEMM1 outputs */
-#define MOE_OPT_ROUTE_TILE 5      /* route-tile width NT in {0 (auto), 32, 128} */
+#define MOE_OPT_ROUTE_TILE 5      /* route-tile width NT in {0 (auto: 32 decode, 144 prefill), 32, 128, 144} */
 #define MOE_OPT_PROFILE 6         /* 1 = bracket each stage of every forward with CUDA events
                                      (eager use only: keep 0 while capturing a CUDA graph) */
 #define MOE_OPT_LAUNCHES 7        /* read-only: CUDA kernels this handle has launched so far */

@@ -335,3 +335,20 @@ def test_full_largem_compact_dispatch_bit_exact():
     assert np.array_equal(L.debug_array("perm")[:R], d["perm"])
     assert np.array_equal(L.debug_array("route_row").reshape(w.T, w.K), d["route_row"])
     assert torch.count_nonzero(out).item() == 0
+
+
+@pytest.mark.parametrize("disp", ["compact", "fixed"])
+def test_route_tile_144_experts_past_128_rows(disp):
+    """Prefill route tiles of 144 rows: experts with 129..144 rows fill the second 128-row scale atom
+    of a tile, longer experts take two tiles."""
+    w = synth.micro(300, 256, 256, 2, 1, nvr=298, invalid_frac=0.0, dispatch=disp, seed=99, swiglu_limit=10.0,
+                    capacity=300)
+    c = Case(w)
+    counts = np.bincount(c.ids[: w.nvr].reshape(-1), minlength=w.E)
+    assert counts.max() > 144 and counts.min() > 128, counts
+    for nt in (144, 128):
+        L = c.layer(route_tile=nt)
+        got = _out_bits(c.run(L))
+        torch.cuda.synchronize()
+        assert_close(got, c.oracle(), f"{disp} NT={nt}")
+        assert L.read_status() == 0
