@@ -89,6 +89,11 @@ WORKLOADS = {
     "decode_flash_e64": Workload("decode_flash_e64", T=32, H=5120, I=2304, E=64, K=6, nvr=32,
                                  routing="uniform", invalid_frac=0.0, swiglu_limit=10.0,
                                  dispatch="fixed", capacity=32),
+    # Profiling stand-in for the large-input workload: Pro shape, 48 experts (1.7 GB of MXFP4
+    # weights) and 1024 rows, so experts hold ~128 routes each as in the 8192-row case.
+    "largem_pro_e48": Workload("largem_pro_e48", T=1024, H=7168, I=3072, E=48, K=6, nvr=1024,
+                               routing="uniform", invalid_frac=0.02, swiglu_limit=10.0,
+                               dispatch="compact", capacity=1024),
 }
 
 
