@@ -120,6 +120,10 @@ MICRO = [
     (300, 128, 128, 2, 2, 250, "uniform", 0.1, 0.0, "fixed", 128),     # fixed slots, capacity 300
     (200, 256, 128, 6, 4, 190, "hot_zipf", 0.0, 0.0, "compact", 32),   # repeated experts per row
     (64, 384, 384, 5, 2, 64, "hot_zipf", 0.0, 10.0, "fixed", 128),     # repeated experts share a slot
+    (400, 384, 256, 3, 2, 390, "uniform", 0.05, 10.0, "compact", 144),  # H % 256 != 0: single W2 tiles
+    (300, 512, 384, 2, 1, 300, "uniform", 0.0, 0.0, "fixed", 144),     # paired W2 tiles, I % 256 != 0
+    (160, 256, 128, 20, 16, 160, "uniform", 0.1, 10.0, "compact", 144),  # top-16, prefill tiles
+    (200, 256, 128, 1, 1, 200, "uniform", 0.0, 0.0, "compact", 144),    # one expert, two tiles
 ]
 
 
