@@ -415,16 +415,24 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
         mark(1);
         mark(2);
         e = bmoe::launch_fused(g, ws, fl, &wb.tm_w13p, &h->tm_aq, &wb.tm_w2, &h->tm_hq, h->num_sms, s);
-        if (e != cudaSuccess) return cuda_fail(h, e, "fused launch");
-        h->launches += 1;
-        mark(3);
-        mark(4);
-        mark(5);
-        h->profiled = prof;
-        h->forwarded = true;
-        h->last_T = T;
-        h->last_path = MOE_PATH_FUSED;
-        return MOE_OK;
+        if (e == cudaErrorCooperativeLaunchTooLarge && h->opt_path != MOE_PATH_FUSED) {
+            // the driver could not make the grid co-resident (fewer SMs available to this context than
+            // the device reports): nothing was enqueued; take the multi-kernel path from now on
+            (void)cudaGetLastError();
+            h->coop = false;
+        } else if (e != cudaSuccess) {
+            return cuda_fail(h, e, "fused launch");
+        } else {
+            h->launches += 1;
+            mark(3);
+            mark(4);
+            mark(5);
+            h->profiled = prof;
+            h->forwarded = true;
+            h->last_T = T;
+            h->last_path = MOE_PATH_FUSED;
+            return MOE_OK;
+        }
     }
     if (g.scheme == 1) {
         e = cudaMemsetAsync(ws.occ, 0, sizeof(uint32_t) * (size_t)g.E * g.words, s);

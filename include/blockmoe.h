@@ -85,9 +85,13 @@ typedef void* moe_stream_t;
  * tokens every step of the layer happens inside one kernel launch) when the
  * handle allows it: capacity <= 512, route tile 32, E <= 512, and a device
  * that supports cooperative launches; otherwise it runs the multi-kernel path.
+ * If the driver refuses the cooperative launch because the grid (one CTA per
+ * SM) cannot be co-resident, AUTO takes the multi-kernel path for that forward
+ * and every later one on the handle.
  * MOE_PATH_FUSED insists on the fused kernel (setting it is refused when the
- * handle does not allow it); MOE_PATH_MULTI always runs the separate kernels.  Both
- * paths produce the same bits. */
+ * handle does not allow it, and a refused launch is returned as an error);
+ * MOE_PATH_MULTI always runs the separate kernels.  Both paths produce the same
+ * bits. */
 #define MOE_PATH_AUTO 0
 #define MOE_PATH_FUSED 1
 #define MOE_PATH_MULTI 2
@@ -176,7 +180,8 @@ int moe_select_layer(moe_handle h, int slot);
  *                  "Per-pass real row counts").  Rows at or past it give +0.
  *   out            bf16 [T, H]; every row is written (T = 0 writes nothing)
  * No host synchronisation, no allocation; enqueues only on `stream`, so the
- * call can be captured in a CUDA graph.  Returns MOE_ECAPACITY if T exceeds
+ * call can be captured in a CUDA graph.  Forwards on one handle share its
+ * workspace: issue them on one stream (or order them with events).  Returns MOE_ECAPACITY if T exceeds
  * the capacity, MOE_ENOTBOUND without weights. */
 int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const float* topk_weights,
                 const int32_t* num_valid_rows, void* out, int T, moe_stream_t stream);
