@@ -238,7 +238,7 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
     return true;
 }
 
-// MMA issue of one unit by chain w (its warp's lane 0).  GEMM1: chain w multiplies operand
+// MMA issue of one unit by chain w (its warp, converged, one elected lane issuing).  GEMM1: chain w multiplies operand
 // w & 1 (gate / up) over the K-steps k with k % 2 == w >> 1; GEMM2: chain w takes the KC
 // consecutive K-steps [w*KC, w*KC + KC) of the stage (k = 4 * chunk + step in chunk), all in
 // chunk w*KC/4.  Either way a chain reads one weight atom and one row atom per stage, which
@@ -253,9 +253,9 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
 #ifdef BMOE_TRACE
         const long long tw0 = (long long)globaltimer_ns();
 #endif
-        if (!mbar_wait(&p.full[r.stage], r.phase, p.abort_flag, p.status, kStTimeout | (1u << (kSiteShift + 3)),
-                       kWaitLimitNs))
-            return false;
+        const bool got = mbar_wait(&p.full[r.stage], r.phase, p.abort_flag, p.status,
+                                   kStTimeout | (1u << (kSiteShift + 3)), kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, got)) return false;  // the warp stays converged for the elected issue
 #ifdef BMOE_TRACE
         const long long tw1 = (long long)globaltimer_ns();
         wait_ns += tw1 - tw0;
@@ -264,11 +264,11 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
         (void)issue_ns;
 #endif
         tc_fence_after();
-        if (lane == 0) {
+        {
             const uint32_t sfa = p.tmem + static_cast<uint32_t>(F_SF_BASE + (w * 2 + (job & 1)) * F_SF_SLOT);
             const uint32_t sfb = sfa + 4;
-            tc_cp_32x128b_x4(sfa, desc_sf_atom(smem_u32(p.sSFA + (r.stage * 2 + ach) * 512)));
-            tc_cp_32x128b_x4(sfb, desc_sf_atom(smem_u32(p.sSFB + (r.stage * 2 + bch) * 512)));
+            tc_cp_32x128b_x4_w(sfa, desc_sf_atom(smem_u32(p.sSFA + (r.stage * 2 + ach) * 512)));
+            tc_cp_32x128b_x4_w(sfb, desc_sf_atom(smem_u32(p.sSFB + (r.stage * 2 + bch) * 512)));
             const uint64_t da0 = desc_kmajor_sw128(smem_u32(p.sA + (r.stage * 2 + ach) * F_A_BYTES));
             const uint64_t db0 = desc_kmajor_sw128(smem_u32(p.sB + (r.stage * 2 + bch) * F_B_BYTES));
             if constexpr (!G2) {
@@ -276,20 +276,20 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
                     if ((k4 & 1) != kq) continue;
-                    tc_mma_mx(d_tmem, da0 + static_cast<uint64_t>((k4 * 32) >> 4),
-                              db0 + static_cast<uint64_t>((k4 * 32) >> 4), idesc_mx(128, N, 5, 0, k4, k4), sfa, sfb,
-                              (kk > 0 || k4 != kq) ? 1u : 0u);
+                    tc_mma_mx_w(d_tmem, da0 + static_cast<uint64_t>((k4 * 32) >> 4),
+                                db0 + static_cast<uint64_t>((k4 * 32) >> 4), idesc_mx(128, N, 5, 0, k4, k4), sfa, sfb,
+                                (kk > 0 || k4 != kq) ? 1u : 0u);
                 }
             } else {
 #pragma unroll
                 for (int j = 0; j < KC; ++j) {
                     const int k4 = (w * KC + j) & 3;
-                    tc_mma_mx(d_tmem, da0 + static_cast<uint64_t>((k4 * 32) >> 4),
-                              db0 + static_cast<uint64_t>((k4 * 32) >> 4), idesc_mx(128, N, 5, 0, k4, k4), sfa, sfb,
-                              (kk > 0 || j > 0) ? 1u : 0u);
+                    tc_mma_mx_w(d_tmem, da0 + static_cast<uint64_t>((k4 * 32) >> 4),
+                                db0 + static_cast<uint64_t>((k4 * 32) >> 4), idesc_mx(128, N, 5, 0, k4, k4), sfa, sfb,
+                                (kk > 0 || j > 0) ? 1u : 0u);
                 }
             }
-            tc_commit(&p.empty[r.stage]);
+            tc_commit_w(&p.empty[r.stage]);
 #ifdef BMOE_TRACE
             issue_ns += (long long)globaltimer_ns() - tw1;
 #endif
@@ -759,9 +759,9 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 const long long ta0 = (long long)globaltimer_ns();
 #endif
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * F_ACC_COLS + w * F_NT);
-                if (!mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, ws.status,
-                               kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs))
-                    break;
+                const bool got_acc = mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, ws.status,
+                                               kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs);
+                if (!__all_sync(0xffffffffu, got_acc)) break;
 #ifdef BMOE_TRACE
                 (fu.g2 ? aw2 : aw1) += (long long)globaltimer_ns() - ta0;
 #endif
@@ -770,12 +770,13 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                                 : f.kc2 == 2 ? mma_unit<true, 2>(p, ring, job, w, lane, d_tmem, N, kt2, fw2, mi2)
                                              : mma_unit<true, 1>(p, ring, job, w, lane, d_tmem, N, kt2, fw2, mi2);
                 if (!ok) break;
-                if (lane == 0) tc_commit(&accf[acc]);
+                tc_commit_w(&accf[acc]);
                 __syncwarp();
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
-            if (lane == 0) tc_commit(drain);
+            __syncwarp();
+            tc_commit_w(drain);
             if (lane == 0 && w == 0) {
                 FTRACE(6, (long long)globaltimer_ns());
                 FTRACE(18, fw1);

@@ -25,11 +25,12 @@
 //               [rows, K/32] layout into a 128x4 scale atom by the warp's 32
 //               lanes, loaded 8 stages ahead into registers and stored with a
 //               proxy fence before the stage's arrival.
-//   warps 2..   MMA issuers.  One thread can issue a tcgen05.mma only every
-//               ~170 cycles whatever N is, so small-N decode MMAs are issue
-//               bound; MW warps each own an accumulator chain (gate or up, and
-//               a residue class of the K-steps) and issue in parallel.  Each
-//               copies the stage's scale atoms into its own TMEM columns.
+//   warps 2..   MMA issuers, the whole warp converged and one elected lane
+//               issuing (~44 cycles per MMA at N = 32; small-N decode MMAs are
+//               still issue bound); MW warps each own an accumulator chain (gate
+//               or up, and a residue class of the K-steps) and issue in
+//               parallel.  Each copies the stage's scale atoms into its own TMEM
+//               columns.
 //   last EW     epilogue warps: tcgen05.ld of the MW partial accumulators (lane =
 //               output feature, column = routed row) and their fixed-order sum
 //               into registers, release of the accumulator, then the
@@ -294,27 +295,27 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
             const int N = (cu.n + 15) & ~15;
             // ROT3: this warp's one chain (w = wi) uses slot (2 ui + wi) % 3, its (2 ui + wi) / 3-th use
             const int rq = 2 * ui + wi, rslot = rq % 3;
-            if constexpr (C::ROT3) {
-                if (!mbar_wait(&acce[rslot], ((rq / 3) & 1u) ^ 1u, abort_flag, a.status,
-                               kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-            } else if (!mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, a.status,
-                                  kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs)) {
+            // every lane waits; the warp goes on only if all lanes saw the barrier (a timeout in one
+            // lane stops the whole warp), so that it stays converged for the elected issue
+            const bool got_acc = C::ROT3 ? mbar_wait(&acce[rslot], ((rq / 3) & 1u) ^ 1u, abort_flag, a.status,
+                                                     kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs)
+                                         : mbar_wait(&acce[acc], acc_phase ^ 1u, abort_flag, a.status,
+                                                     kStTimeout | (1u << (kSiteShift + 2)), kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, got_acc)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             for (int kk = 0; kk < KT; ++kk) {
-                if (!mbar_wait(&full[stage], phase, abort_flag, a.status, kStTimeout | (1u << (kSiteShift + 3)),
-                               kWaitLimitNs)) {
+                const bool got = mbar_wait(&full[stage], phase, abort_flag, a.status,
+                                           kStTimeout | (1u << (kSiteShift + 3)), kWaitLimitNs);
+                if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (lane == 0) {
-                    if (wi == 0) trace(a, 2, job);
+                {
+                    if (wi == 0 && lane == 0) trace(a, 2, job);
 #pragma unroll
                     for (int w = wi; w < MW; w += NI) {
                         // GEMM1: chain w multiplies operand w & 1 (0 gate, 1 up) over the K-steps k with
@@ -332,12 +333,12 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
 #pragma unroll
                         for (int c = 0; c < KC; ++c) {
                             if (c < c_lo || c > c_hi) continue;
-                            tc_cp_32x128b_x4(sfc + 4 * c,
-                                             desc_sf_atom(smem_u32(sSFA + ((stage * NA + op) * KC + c) * 512)));
+                            tc_cp_32x128b_x4_w(sfc + 4 * c,
+                                               desc_sf_atom(smem_u32(sSFA + ((stage * NA + op) * KC + c) * 512)));
 #pragma unroll
                             for (int b = 0; b < NB; ++b)
-                                tc_cp_32x128b_x4(sfc + 4 * KC + 4 * (c * NB + b),
-                                                 desc_sf_atom(smem_u32(sSFB + ((stage * KC + c) * NB + b) * 512)));
+                                tc_cp_32x128b_x4_w(sfc + 4 * KC + 4 * (c * NB + b),
+                                                   desc_sf_atom(smem_u32(sSFB + ((stage * KC + c) * NB + b) * 512)));
                         }
 #pragma unroll
                         for (int k = 0; k < 4 * KC; ++k) {
@@ -349,12 +350,12 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                             const uint64_t db = desc_kmajor_sw128(smem_u32(sB + (stage * KC + c) * C::B_BYTES)) +
                                                 static_cast<uint64_t>((k4 * 32) >> 4);
                             const uint32_t idesc = idesc_mx(128, N, 5, 0, k4, k4);
-                            tc_mma_mx(d_tmem, da, db, idesc, sfc + 4 * c, sfc + 4 * KC + 4 * NB * c,
-                                      (kk > 0 || k != kfirst) ? 1u : 0u);
+                            tc_mma_mx_w(d_tmem, da, db, idesc, sfc + 4 * c, sfc + 4 * KC + 4 * NB * c,
+                                        (kk > 0 || k != kfirst) ? 1u : 0u);
                         }
                     }
-                    tc_commit(&empty[stage]);
-                    if (wi == 0) trace(a, 3, job);
+                    tc_commit_w(&empty[stage]);
+                    if (wi == 0 && lane == 0) trace(a, 3, job);
                 }
                 __syncwarp();
                 ++job;
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                 }
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(&accf[C::ROT3 ? rslot : acc]);
+            tc_commit_w(&accf[C::ROT3 ? rslot : acc]);
             __syncwarp();
             if (C::NUM_ACC == 2) {
                 acc ^= 1;
@@ -373,8 +374,9 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                 acc_phase ^= 1u;
             }
         }
-        // Drain: all MMAs issued by this thread complete before TMEM is released.
-        if (lane == 0) tc_commit(drain);
+        // Drain: all MMAs issued by this warp complete before TMEM is released.
+        __syncwarp();
+        tc_commit_w(drain);
         __syncwarp();
         {
             volatile int never = 0;

@@ -214,6 +214,40 @@ __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint6
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
         : "memory");
 }
+// Warp-level issue: the three helpers below are executed by a whole converged warp and one lane,
+// elected with elect.sync over the full mask (the lowest lane, so the same lane every time),
+// issues the operation.  Keeping the issuing code warp-uniform lets its operands stay in the
+// uniform datapath: on GB300 one warp then issues a block-scaled MMA every ~44 cycles (N = 32)
+// and keeps the tensor pipe saturated from N = 128 up, where a divergent single-lane branch
+// needs ~100 cycles per MMA.  tcgen05.commit tracks the operations of the issuing thread, so
+// the MMAs, the scale copies and their commits of one warp all go through these helpers.
+__device__ __forceinline__ void tc_cp_32x128b_x4_w(uint32_t taddr, uint64_t sdesc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 e;\n\t"
+        "elect.sync e|p, 0xffffffff;\n\t"
+        "@p tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+        "l"(sdesc)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_mx_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b32 e;\n\t"
+        "elect.sync e|p, 0xffffffff;\n\t"
+        "setp.ne.b32 q, %4, 0;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], q;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_w(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 e;\n\t"
+        "elect.sync e|p, 0xffffffff;\n\t"
+        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
 // Each thread of the warp reads 16 consecutive 32-bit columns of its TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
