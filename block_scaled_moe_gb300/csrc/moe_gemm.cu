@@ -100,6 +100,7 @@ struct Cfg {
     static_assert(MW <= 4, "barrier slots");
     static_assert(CW % 8 == 0, "epilogue column split");
     static constexpr int LDC = CW % 16 == 0 ? 16 : 8;      // TMEM columns per epilogue load
+    static constexpr bool SF_VEC = KC == 1 && NT >= 128;   // weight scales read as 16-byte vectors (4 stages)
 };
 
 // LDC-column TMEM load (32 lanes x 32 bit) of the epilogue
@@ -224,64 +225,135 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
         // words are loaded SD stages ahead of their stage into registers so that
         // their latency stays off this warp's path; the stores are made visible to
         // the tensor core's async proxy here, before the warp arrives on the stage.
-        constexpr int SD = 8;
-        constexpr int NW = 4 * NA * KC;  // words per lane per stage: [op][chunk][row group]
-        uint32_t ring[SD][NW];
-        int p_ui = 0, p_kk = 0, p_ecur = 0;  // load cursor (SD stages ahead)
-        const uint8_t* p_src = nullptr;
-        auto load_next = [&](uint32_t(&dst)[NW]) {
-            if (p_ui >= my_units) return;
-            if (p_kk == 0) {
-                const UnitInfo pu = decode_unit(blockIdx.x + p_ui * gridDim.x, p_ecur, pl, a.mtiles, NT);
-                p_src = a.w_sf + (static_cast<size_t>(pu.e) * a.w_rows + (pu.m * a.m_rows + lane) * a.w_rs) * a.ld_sf;
-            }
+        // Prefill tiles leave ~20 KB of L1 beside the stage ring, less than the 32 KB of scale lines a
+        // unit touches, so 4-byte gathers per row and stage miss L1 every time and their requests,
+        // not the weight stream, set the pace.  When the rows' scale stride allows, each lane loads
+        // one 16-byte vector per row that holds the scales of 4 consecutive stages, two groups of 4
+        // stages ahead.
+        const bool sf_vec = C::SF_VEC && (a.ld_sf & 15) == 0 && (KT & 3) == 0 &&
+                            (reinterpret_cast<uintptr_t>(a.w_sf) & 15) == 0;
+        if (sf_vec) {
+            constexpr int GD = 2;          // groups of 4 stages loaded ahead
+            constexpr int NV = 4 * NA;     // 16-byte vectors per lane and group: [op][row group]
+            uint4 gring[GD][NV];
+            const int GPU = KT >> 2;       // groups per unit
+            int q_ui = 0, q_g = 0, q_ecur = 0;
+            const uint8_t* q_src = nullptr;
+            auto gload = [&](uint4(&dst)[NV]) {
+                if (q_ui >= my_units) return;
+                if (q_g == 0) {
+                    const UnitInfo pu = decode_unit(blockIdx.x + q_ui * gridDim.x, q_ecur, pl, a.mtiles, NT);
+                    q_src = a.w_sf +
+                            (static_cast<size_t>(pu.e) * a.w_rows + (pu.m * a.m_rows + lane) * a.w_rs) * a.ld_sf;
+                }
 #pragma unroll
-            for (int op = 0; op < NA; ++op)
-#pragma unroll
-                for (int c = 0; c < KC; ++c) {
-                    const uint8_t* src = p_src + static_cast<size_t>(op * a.up_off) * a.ld_sf + (p_kk * KC + c) * 4;
+                for (int op = 0; op < NA; ++op)
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        dst[(op * KC + c) * 4 + i] =
-                            __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(32 * i * a.w_rs) * a.ld_sf));
+                        dst[op * 4 + i] = __ldg(reinterpret_cast<const uint4*>(
+                            q_src + static_cast<size_t>(op * a.up_off + 32 * i * a.w_rs) * a.ld_sf + q_g * 16));
+                if (++q_g == GPU) {
+                    q_g = 0;
+                    ++q_ui;
                 }
-            if (++p_kk == KT) {
-                p_kk = 0;
-                ++p_ui;
-            }
-        };
+            };
 #pragma unroll
-        for (int d = 0; d < SD; ++d) load_next(ring[d]);
-        const long njobs = static_cast<long>(my_units) * KT;
-        int stage = 0;
-        uint32_t phase = 0;
-        long issued = 0;
-        for (long J0 = 0; J0 < njobs; J0 += SD) {
+            for (int d = 0; d < GD; ++d) gload(gring[d]);
+            const long ngroups = static_cast<long>(my_units) * GPU;
+            int stage = 0;
+            uint32_t phase = 0;
             bool ok = true;
+            for (long G0 = 0; G0 < ngroups && ok; G0 += GD) {
 #pragma unroll
-            for (int d = 0; d < SD; ++d) {
-                if (J0 + d < njobs && ok) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
-                                   kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
-                        ok = false;
-                    } else {
-                        uint4* dst = reinterpret_cast<uint4*>(sSFA + stage * NA * KC * 512) + lane;
+                for (int d = 0; d < GD; ++d) {
+                    if (G0 + d >= ngroups || !ok) continue;
 #pragma unroll
-                        for (int a4 = 0; a4 < NA * KC; ++a4)  // atom (op, chunk) is 32 uint4 further
-                            dst[32 * a4] = make_uint4(ring[d][4 * a4], ring[d][4 * a4 + 1], ring[d][4 * a4 + 2],
-                                                      ring[d][4 * a4 + 3]);
+                    for (int sq = 0; sq < 4; ++sq) {
+                        if (!ok) continue;
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
+                                       kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
+                            ok = false;
+                            continue;
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(sSFA + stage * NA * 512) + lane;
+#pragma unroll
+                        for (int op = 0; op < NA; ++op) {  // stage sq's word of each row is component sq
+                            const uint4* v = gring[d] + op * 4;
+                            dst[32 * op] = sq == 0   ? make_uint4(v[0].x, v[1].x, v[2].x, v[3].x)
+                                           : sq == 1 ? make_uint4(v[0].y, v[1].y, v[2].y, v[3].y)
+                                           : sq == 2 ? make_uint4(v[0].z, v[1].z, v[2].z, v[3].z)
+                                                     : make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
+                        }
                         fence_proxy_async_smem();
                         mbar_arrive(&full[stage]);
-                        ++issued;
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
-                        load_next(ring[d]);
                     }
+                    if (ok) gload(gring[d]);
                 }
             }
-            if (!ok) break;
+        } else {
+            constexpr int SD = 8;
+            constexpr int NW = 4 * NA * KC;  // words per lane per stage: [op][chunk][row group]
+            uint32_t ring[SD][NW];
+            int p_ui = 0, p_kk = 0, p_ecur = 0;  // load cursor (SD stages ahead)
+            const uint8_t* p_src = nullptr;
+            auto load_next = [&](uint32_t(&dst)[NW]) {
+                if (p_ui >= my_units) return;
+                if (p_kk == 0) {
+                    const UnitInfo pu = decode_unit(blockIdx.x + p_ui * gridDim.x, p_ecur, pl, a.mtiles, NT);
+                    p_src = a.w_sf + (static_cast<size_t>(pu.e) * a.w_rows + (pu.m * a.m_rows + lane) * a.w_rs) * a.ld_sf;
+                }
+    #pragma unroll
+                for (int op = 0; op < NA; ++op)
+    #pragma unroll
+                    for (int c = 0; c < KC; ++c) {
+                        const uint8_t* src = p_src + static_cast<size_t>(op * a.up_off) * a.ld_sf + (p_kk * KC + c) * 4;
+    #pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[(op * KC + c) * 4 + i] =
+                                __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<size_t>(32 * i * a.w_rs) * a.ld_sf));
+                    }
+                if (++p_kk == KT) {
+                    p_kk = 0;
+                    ++p_ui;
+                }
+            };
+    #pragma unroll
+            for (int d = 0; d < SD; ++d) load_next(ring[d]);
+            const long njobs = static_cast<long>(my_units) * KT;
+            int stage = 0;
+            uint32_t phase = 0;
+            long issued = 0;
+            for (long J0 = 0; J0 < njobs; J0 += SD) {
+                bool ok = true;
+    #pragma unroll
+                for (int d = 0; d < SD; ++d) {
+                    if (J0 + d < njobs && ok) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
+                                       kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
+                            ok = false;
+                        } else {
+                            uint4* dst = reinterpret_cast<uint4*>(sSFA + stage * NA * KC * 512) + lane;
+    #pragma unroll
+                            for (int a4 = 0; a4 < NA * KC; ++a4)  // atom (op, chunk) is 32 uint4 further
+                                dst[32 * a4] = make_uint4(ring[d][4 * a4], ring[d][4 * a4 + 1], ring[d][4 * a4 + 2],
+                                                          ring[d][4 * a4 + 3]);
+                            fence_proxy_async_smem();
+                            mbar_arrive(&full[stage]);
+                            ++issued;
+                            if (++stage == STAGES) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                            load_next(ring[d]);
+                        }
+                    }
+                }
+                if (!ok) break;
+            }
         }
     } else if (warp < C::EPI_WARP0) {
         // ------------------------------------------------------------ MMA issuers
