@@ -78,17 +78,17 @@ __device__ __forceinline__ void quant_scatter_seg(const QuantArgs& a, const int3
     }
     if (t >= nvr) return;  // warp-uniform
     const unsigned vmask = __ballot_sync(kFull, valid);
-    int pk[kMaxTopk], gk[kMaxTopk], ck[kMaxTopk];
-#pragma unroll
-    for (int k = 0; k < kMaxTopk; ++k) {
-        pk[k] = __shfl_sync(kFull, p, k);
-        gk[k] = __shfl_sync(kFull, gt, k);
-        ck[k] = __shfl_sync(kFull, c, k);
-    }
     const int H = a.H, nblk = H >> 5, ktiles = H >> 7;
-    const uint16_t* xrow = a.x + (size_t)t * H;
-    for (int blk = seg * kQuantBlocks + lane; blk < min(nblk, (seg + 1) * kQuantBlocks); blk += 32) {
-        const uint4* src = reinterpret_cast<const uint4*>(xrow + blk * 32);
+    static_assert(kQuantBlocks == 32, "one 32-element block per lane");
+    // Quantise this lane's block once, then store it for each valid slot in turn; the slots'
+    // destinations are broadcast from lane k one slot at a time (no per-slot register arrays, so
+    // the stand-alone kernel keeps enough warps resident to cover the loads' latency).
+    const int blk = seg * kQuantBlocks + lane;
+    const bool has = blk < nblk;
+    uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+    int code = 0;
+    if (has) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * H + blk * 32);
         float f[32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -103,30 +103,32 @@ __device__ __forceinline__ void quant_scatter_seg(const QuantArgs& a, const int3
         float amax = 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(f[j]));
-        int code = static_cast<int>(__float_as_uint(amax) >> 23) - 8;
+        code = static_cast<int>(__float_as_uint(amax) >> 23) - 8;
         code = code < 0 ? 0 : code;
         const float mul = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
         uint32_t o[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             o[j] = pack_fp8x4(f[4 * j] * mul, f[4 * j + 1] * mul, f[4 * j + 2] * mul, f[4 * j + 3] * mul);
-        const uint4 o0 = make_uint4(o[0], o[1], o[2], o[3]), o1 = make_uint4(o[4], o[5], o[6], o[7]);
+        o0 = make_uint4(o[0], o[1], o[2], o[3]);
+        o1 = make_uint4(o[4], o[5], o[6], o[7]);
         if (a.ws.xq) {
             uint4* d = reinterpret_cast<uint4*>(a.ws.xq + (size_t)t * H + blk * 32);
             d[0] = o0;
             d[1] = o1;
             a.ws.xs[(size_t)t * nblk + blk] = static_cast<uint8_t>(code);
         }
-#pragma unroll
-        for (int k = 0; k < kMaxTopk; ++k) {
-            if (k < K && ((vmask >> k) & 1u)) {
-                uint4* d = reinterpret_cast<uint4*>(a.ws.aq + (size_t)pk[k] * H + blk * 32);
-                d[0] = o0;
-                d[1] = o1;
-                const int ci = ck[k];
-                a.ws.as[(((size_t)gk[k] * ktiles + (blk >> 2)) * a.nb + (ci >> 7)) * 512 + 16 * (ci & 31) +
-                        4 * ((ci >> 5) & 3) + (blk & 3)] = static_cast<uint8_t>(code);
-            }
+    }
+#pragma unroll 1
+    for (int k = 0; k < K; ++k) {
+        if (!((vmask >> k) & 1u)) continue;  // warp-uniform
+        const int pk = __shfl_sync(kFull, p, k), gk = __shfl_sync(kFull, gt, k), ci = __shfl_sync(kFull, c, k);
+        if (has) {
+            uint4* d = reinterpret_cast<uint4*>(a.ws.aq + (size_t)pk * H + blk * 32);
+            d[0] = o0;
+            d[1] = o1;
+            a.ws.as[(((size_t)gk * ktiles + (blk >> 2)) * a.nb + (ci >> 7)) * 512 + 16 * (ci & 31) +
+                    4 * ((ci >> 5) & 3) + (blk & 3)] = static_cast<uint8_t>(code);
         }
     }
 }
