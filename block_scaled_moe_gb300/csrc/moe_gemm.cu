@@ -103,6 +103,33 @@ struct Cfg {
     static constexpr bool SF_VEC = KC == 1 && NT >= 128;   // weight scales read as 16-byte vectors (4 stages)
 };
 
+// SwiGLU of one (gate, up) pair with the optional clamp (ROCm/aiter PR #6154 "clamp-10 SwiGLU":
+// gate <= L, -L <= up <= L), fast exp / divide intrinsics; the clamp is a select, not a branch.
+__device__ __forceinline__ float swiglu(float ga, float ub, bool clamp, float L) {
+    ga = clamp ? fminf(ga, L) : ga;
+    ub = clamp ? fminf(fmaxf(ub, -L), L) : ub;
+    return __fdividef(ga, 1.0f + __expf(-ga)) * ub;
+}
+
+// BF16 rows of one warp's features: v[j] is row (row0 + j), feature `feat`, for j < n (n may exceed
+// CW or be <= 0).  Eight rows per group, branch-free stores for full groups.
+template <int CW>
+__device__ __forceinline__ void store_rows_bf16(uint16_t* y, const float (&v)[CW], int row0, int n, int H, int feat) {
+#pragma unroll
+    for (int j0 = 0; j0 < CW; j0 += 8) {
+        if (j0 >= n) break;
+        uint16_t* yr = y + static_cast<size_t>(row0 + j0) * H + feat;
+        if (j0 + 8 <= n) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) yr[static_cast<size_t>(i) * H] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j0 + i]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (j0 + i < n) yr[static_cast<size_t>(i) * H] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j0 + i]));
+        }
+    }
+}
+
 // LDC-column TMEM load (32 lanes x 32 bit) of the epilogue
 template <int L>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[L]) {
@@ -465,6 +492,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
         int acc = 0, ecur = 0;
         uint32_t acc_phase = 0;
         const float L = a.swiglu_limit;
+        const bool clamp = L > 0.f;
         const bool tracer = warp == C::EPI_WARP0 && lane == 0;
         for (int ui = 0; ui < my_units; ++ui) {
             const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
@@ -492,28 +520,27 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                             uint32_t r[LDC];
                             tmem_ld_cols<LDC>(tbs + c0, r);
                             tmem_ld_wait();
+                            if constexpr (G1) {
+                                // (the debug capture stores the chain as read, gate in pass 0, up in pass 1)
+                                if (a.g_dbg) {
 #pragma unroll
-                            for (int i = 0; i < LDC; ++i) {
-                                const int vi = LDC * j + i;
-                                if constexpr (G1) {
+                                    for (int i = 0; i < LDC; ++i)
+                                        if (c0 + i < cu.n)
+                                            a.g_dbg[static_cast<size_t>(cu.row0 + c0 + i) * 2 * a.I + w * a.I + feat] =
+                                                0.f + __uint_as_float(r[i]);
+                                }
+#pragma unroll
+                                for (int i = 0; i < LDC; ++i) {
+                                    const int vi = LDC * j + i;
                                     if (w == 0) {
                                         v[vi] = 0.f + __uint_as_float(r[i]);  // gate (+0 like the chain sums)
                                     } else {
-                                        float ga = v[vi], ub = 0.f + __uint_as_float(r[i]);
-                                        if (a.g_dbg && c0 + i < cu.n) {
-                                            const size_t prow = static_cast<size_t>(cu.row0 + c0 + i);
-                                            a.g_dbg[prow * 2 * a.I + feat] = ga;
-                                            a.g_dbg[prow * 2 * a.I + a.I + feat] = ub;
-                                        }
-                                        if (L > 0.f) {
-                                            ga = fminf(ga, L);
-                                            ub = fminf(fmaxf(ub, -L), L);
-                                        }
-                                        v[vi] = __fdividef(ga, 1.0f + __expf(-ga)) * ub;  // SwiGLU, fast intrinsics
+                                        v[vi] = swiglu(v[vi], 0.f + __uint_as_float(r[i]), clamp, L);
                                     }
-                                } else {
-                                    v[vi] = __uint_as_float(r[i]);
                                 }
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < LDC; ++i) v[LDC * j + i] = __uint_as_float(r[i]);
                             }
                         }
                     }
@@ -533,13 +560,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                                 }
                             }
                         } else {
-#pragma unroll
-                            for (int j = 0; j < CW; ++j) {
-                                const int c = cbase + j;
-                                if (c < cu.n)
-                                    a.y[static_cast<size_t>(cu.row0 + c) * a.H + featw] =
-                                        __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
-                            }
+                            store_rows_bf16<CW>(a.y, v, cu.row0 + cbase, cu.n - cbase, a.H, featw);
                         }
                     }
                 }
@@ -563,6 +584,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
 #pragma unroll
                         for (int w = 0; w < MW; ++w) tmem_ld_cols<LDC>(tb + w * NT + c0, r[w]);
                         tmem_ld_wait();
+                        float gav[LDC], ubv[LDC];
 #pragma unroll
                         for (int i = 0; i < LDC; ++i) {
                             float ga = 0.f, ub = 0.f;
@@ -573,20 +595,24 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                                 else
                                     ga += __uint_as_float(r[w][i]);
                             }
-                            if constexpr (G1) {
-                                if (a.g_dbg && c0 + i < cu.n) {
-                                    const size_t prow = static_cast<size_t>(cu.row0 + c0 + i);
-                                    a.g_dbg[prow * 2 * a.I + feat] = ga;
-                                    a.g_dbg[prow * 2 * a.I + a.I + feat] = ub;
-                                }
-                                if (L > 0.f) {
-                                    ga = fminf(ga, L);
-                                    ub = fminf(fmaxf(ub, -L), L);
-                                }
-                                v[LDC * j + i] = __fdividef(ga, 1.0f + __expf(-ga)) * ub;  // SwiGLU, fast intrinsics
-                            } else {
-                                v[LDC * j + i] = ga;
+                            gav[i] = ga;
+                            ubv[i] = ub;
+                        }
+                        if constexpr (G1) {
+                            if (a.g_dbg) {  // debug capture of the chain sums
+#pragma unroll
+                                for (int i = 0; i < LDC; ++i)
+                                    if (c0 + i < cu.n) {
+                                        const size_t prow = static_cast<size_t>(cu.row0 + c0 + i);
+                                        a.g_dbg[prow * 2 * a.I + feat] = gav[i];
+                                        a.g_dbg[prow * 2 * a.I + a.I + feat] = ubv[i];
+                                    }
                             }
+#pragma unroll
+                            for (int i = 0; i < LDC; ++i) v[LDC * j + i] = swiglu(gav[i], ubv[i], clamp, L);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < LDC; ++i) v[LDC * j + i] = gav[i];
                         }
                     }
                 }
@@ -613,25 +639,52 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                 }
                 continue;
             }
+            if constexpr (G1) {
+                // MXFP8 1x32 requantisation of h along I: this warp's 32 features of a row are one
+                // block.  Eight rows at a time are quantised without branches, then stored.
+                uint8_t* hs_tile = a.hs + (static_cast<size_t>(cu.g) * (a.I >> 7) + cu.m) * NB * 512 + q;
 #pragma unroll
-            for (int j = 0; j < CW; ++j) {
-                const int c = cbase + j;
-                if (c < cu.n) {
-                    const size_t prow = static_cast<size_t>(cu.row0 + c);
-                    if constexpr (G1) {
-                        const float h = v[j];
+                for (int j0 = 0; j0 < CW; j0 += 8) {
+                    const int c0 = cbase + j0;
+                    if (c0 >= cu.n) break;  // warp-uniform: the rest of the columns are past the tile's rows
+                    uint8_t q8[8];
+                    int cd[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float h = v[j0 + i];
                         const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
                         int code = static_cast<int>(amax >> 23) - 8;
                         code = code < 0 ? 0 : code;
                         const float mul = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
-                        a.hq[prow * a.I + feat] = __nv_cvt_float_to_fp8(h * mul, __NV_SATFINITE, __NV_E4M3);
-                        if (lane == 0)
-                            a.hs[((static_cast<size_t>(cu.g) * (a.I >> 7) + cu.m) * NB + (c >> 7)) * 512 +
-                                 16 * (c & 31) + 4 * ((c >> 5) & 3) + q] = static_cast<uint8_t>(code);
+                        q8[i] = __nv_cvt_float_to_fp8(h * mul, __NV_SATFINITE, __NV_E4M3);
+                        cd[i] = code;
+                    }
+                    uint8_t* hrow = a.hq + static_cast<size_t>(cu.row0 + c0) * a.I + feat;
+                    if (c0 + 8 <= cu.n) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) hrow[static_cast<size_t>(i) * a.I] = q8[i];
+                        if (lane == 0) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int c = c0 + i;
+                                hs_tile[(c >> 7) * 512 + 16 * (c & 31) + 4 * ((c >> 5) & 3)] = static_cast<uint8_t>(cd[i]);
+                            }
+                        }
                     } else {
-                        a.y[prow * a.H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int c = c0 + i;
+                            if (c < cu.n) {
+                                hrow[static_cast<size_t>(i) * a.I] = q8[i];
+                                if (lane == 0)
+                                    hs_tile[(c >> 7) * 512 + 16 * (c & 31) + 4 * ((c >> 5) & 3)] =
+                                        static_cast<uint8_t>(cd[i]);
+                            }
+                        }
                     }
                 }
+            } else {
+                store_rows_bf16<CW>(a.y, v, cu.row0 + cbase, cu.n - cbase, a.H, feat);
             }
         }
     }
