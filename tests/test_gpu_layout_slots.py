@@ -46,6 +46,10 @@ LAYOUT_CFGS = [
     (40, 256, 256, 6, 3, "compact", 32, "multi"),
     (64, 512, 384, 5, 2, "fixed", 32, "fused"),     # H % 512 == 0: 16-byte GEMM1 scale loads
     (200, 384, 256, 4, 4, "compact", 128, "multi"),
+    # H, I multiples of 512: prefill tiles read the weight scales as 16-byte vectors (4 K stages);
+    # several vector groups per unit, several units per CTA
+    (1200, 1024, 1024, 16, 2, "compact", 144, "multi"),
+    (600, 2048, 512, 8, 2, "compact", 128, "multi"),
 ]
 
 
