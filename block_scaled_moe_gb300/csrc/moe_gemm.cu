@@ -7,7 +7,7 @@
 // where a few rows meet each expert, the layer is a stream over the active
 // experts' weights (ROCm/aiter PR #6881 Technical Details: the small-input path
 // is dominated by reading expert weights); for prefill the same kernel runs
-// route tiles of up to NT=128 rows.
+// route tiles of up to NT=144 rows.
 //
 //   GEMM1 unit = (route tile, pair m): gate rows [128m,128m+128) and up rows
 //     I+[128m,128m+128) of W13[e], K = H.  Epilogue: SwiGLU (optional clamp,
