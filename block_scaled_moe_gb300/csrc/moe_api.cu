@@ -37,6 +37,7 @@ struct Binding {
     CUtensorMap tm_w13p{};  // W13 gate/up pair view (K, feature, half, expert)
     CUtensorMap tm_w2{};
     CUtensorMap tm_w2w{};   // W2 with 256-row boxes (paired tiles of prefill GEMM2)
+    CUtensorMap tm_w2k2{};  // W2 as (K in chunk, row, K chunk): one box = two 128-wide K chunks (I % 256 == 0)
 };
 
 struct moe_ctx {
@@ -58,6 +59,7 @@ struct moe_ctx {
     int opt_w13_layout = MOE_W13_CONCAT;  // layout the next bind assumes
     int y_format = MOE_Y_BF16;            // GEMM2 rows handed to the combine
     CUtensorMap tm_aq{}, tm_hq{};
+    CUtensorMap tm_hqk2{};  // h rows as (K in chunk, row, K chunk), two K chunks per box (I % 256 == 0)
     int last_T = 0;
     int profile = 0;
     bool profiled = false;
@@ -142,6 +144,23 @@ int make_map_w13_pair(moe_ctx* h, CUtensorMap* m, const void* base, uint64_t H, 
     return MOE_OK;
 }
 
+// K-major rows as a 3D view (128 K-elements of a chunk, row, chunk) so that one box {128, box_rows, 2}
+// brings two consecutive 128-wide K chunks, landing chunk-major in shared memory exactly like two
+// 2D boxes would: the decode GEMM2's 256-wide K stages take one TMA per operand instead of two.
+int make_map_k2(moe_ctx* h, CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t K, uint64_t rows,
+                uint64_t row_bytes, uint64_t chunk_bytes, uint32_t box_rows, CUtensorMapL2promotion l2) {
+    auto fn = encode_fn();
+    if (!fn) return fail(h, MOE_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {128, rows, K / 128};
+    cuuint64_t strides[2] = {row_bytes, chunk_bytes};
+    cuuint32_t box[3] = {128, box_rows, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(h, MOE_ECUDA, "cuTensorMapEncodeTiled failed (%d) for a two-chunk view", (int)r);
+    return MOE_OK;
+}
+
 void compute_geometry(moe_ctx* h, Geometry* g) {
     *g = h->geo;
     const bool fixed = h->opt_dispatch == MOE_DISPATCH_FIXED ||
@@ -175,8 +194,11 @@ int setup_workspace_maps(moe_ctx* h) {
     int rc = make_map(h, &h->tm_aq, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->ws.aq, g.H, g.rows_cap, g.H, g.NT,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
     if (rc) return rc;
-    return make_map(h, &h->tm_hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->ws.hq, g.I, g.rows_cap, g.I, g.NT,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+    rc = make_map(h, &h->tm_hq, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->ws.hq, g.I, g.rows_cap, g.I, g.NT,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+    if (rc || g.I % 256) return rc;
+    return make_map_k2(h, &h->tm_hqk2, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->ws.hq, g.I, g.rows_cap, g.I, 128, g.NT,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
 void release_workspace(moe_ctx* h) {
@@ -326,6 +348,10 @@ int prepare_binding(moe_handle h, Binding* b, const void* w13_fp4, const void* w
     if ((rc = make_map(h, &b->tm_w2w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2_fp4, g.I, (uint64_t)g.E * g.H, g.I / 2,
                        256, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
         return rc;
+    if (g.I % 256 == 0 &&
+        (rc = make_map_k2(h, &b->tm_w2k2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2_fp4, g.I, (uint64_t)g.E * g.H,
+                          g.I / 2, 64, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
+        return rc;
     b->w13_layout = h->opt_w13_layout;
     b->w13 = static_cast<const uint8_t*>(w13_fp4);
     b->w13s = static_cast<const uint8_t*>(w13_sf);
@@ -414,7 +440,10 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
         fl.T = T;
         mark(1);
         mark(2);
-        e = bmoe::launch_fused(g, ws, fl, &wb.tm_w13p, &h->tm_aq, &wb.tm_w2, &h->tm_hq, h->num_sms, s);
+        // 256-wide GEMM2 K stages (I % 256 == 0) read W2 and h through the two-chunk views
+        const bool k2 = g.I % 256 == 0;
+        e = bmoe::launch_fused(g, ws, fl, &wb.tm_w13p, &h->tm_aq, k2 ? &wb.tm_w2k2 : &wb.tm_w2,
+                               k2 ? &h->tm_hqk2 : &h->tm_hq, h->num_sms, s);
         if (e == cudaErrorCooperativeLaunchTooLarge && h->opt_path != MOE_PATH_FUSED) {
             // the driver could not make the grid co-resident (fewer SMs available to this context than
             // the device reports): nothing was enqueued; take the multi-kernel path from now on
@@ -501,7 +530,7 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     a.b_sf = ws.hs;
     a.y = ws.y;
     a.g_dbg = nullptr;
-    e = bmoe::launch_gemm2(a, &wb.tm_w2, &wb.tm_w2w, &h->tm_hq, g.NT, h->num_sms, s);
+    e = bmoe::launch_gemm2(a, &wb.tm_w2, &wb.tm_w2w, &wb.tm_w2k2, &h->tm_hq, &h->tm_hqk2, g.NT, h->num_sms, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "GEMM2 launch");
     h->launches += 1;
     mark(4);

@@ -220,11 +220,12 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
             bulk_load(p.sSFB + (r.stage * 2) * 512, bsf + static_cast<size_t>(kk) * 512, 512, fb);
         } else {
             mbar_expect_tx(fb, KC * (F_A_TX + F_B_BYTES + 512));
-#pragma unroll
-            for (int c = 0; c < KC; ++c) {
-                const int k0 = (kk * KC + c) * 128;
-                tma_load_2d(a0 + c * F_A_BYTES, tw, fb, k0, wrow, pol_w);
-                tma_load_2d(b0 + c * F_B_BYTES, tb, fb, k0, row0, pol_b);
+            if constexpr (KC == 2) {  // two-chunk views (the launch passes them for 256-wide stages)
+                tma_load_3d(a0, tw, fb, 0, wrow, kk * KC, pol_w);
+                tma_load_3d(b0, tb, fb, 0, row0, kk * KC, pol_b);
+            } else {
+                tma_load_2d(a0, tw, fb, kk * 128, wrow, pol_w);
+                tma_load_2d(b0, tb, fb, kk * 128, row0, pol_b);
             }
             bulk_load(p.sSFB + (r.stage * 2) * 512, bsf + static_cast<size_t>(kk) * KC * 512, KC * 512, fb);
         }

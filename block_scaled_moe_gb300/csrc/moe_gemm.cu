@@ -223,15 +223,21 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                     }
                     trace(a, 0, issued);
                     mbar_expect_tx(&full[stage], KC * (NA * C::A_TX + C::B_BYTES + NB * 512));
+                    if constexpr (KC == 2) {  // two-chunk views: one box per operand lands both K chunks
+                        tma_load_3d(sA + (stage * NA) * KC * C::A_BYTES, &tm_w, &full[stage], 0, wrow, kk * KC, pol_w);
+                        tma_load_3d(sB + stage * KC * C::B_BYTES, &tm_b, &full[stage], 0, cu.row0, kk * KC, pol_b);
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < KC; ++c) {
-                        const int k0 = (kk * KC + c) * 128;
-                        if constexpr (G1)  // gate and up tiles of feature tile m: one box {128, 128, 2, 1}
-                            tma_load_4d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0, cu.m * 128,
-                                        0, cu.e, pol_w);
-                        else  // W2 tile (WIDE: a 256-row box, the unit's two tiles back to back)
-                            tma_load_2d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0, wrow, pol_w);
-                        tma_load_2d(sB + (stage * KC + c) * C::B_BYTES, &tm_b, &full[stage], k0, cu.row0, pol_b);
+                        for (int c = 0; c < KC; ++c) {
+                            const int k0 = (kk * KC + c) * 128;
+                            if constexpr (G1)  // gate and up tiles of feature tile m: one box {128, 128, 2, 1}
+                                tma_load_4d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0,
+                                            cu.m * 128, 0, cu.e, pol_w);
+                            else  // W2 tile (WIDE: a 256-row box, the unit's two tiles back to back)
+                                tma_load_2d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0, wrow,
+                                            pol_w);
+                            tma_load_2d(sB + (stage * KC + c) * C::B_BYTES, &tm_b, &full[stage], k0, cu.row0, pol_b);
+                        }
                     }
                     bulk_load(sSFB + stage * KC * NB * 512, b_sf + kk * KC * NB * 512, KC * NB * 512, &full[stage]);
                     mbar_arrive(&full[stage]);
@@ -732,9 +738,11 @@ cudaError_t launch_gemm1(const GemmArgs& a, const CUtensorMap* tm_w, const CUten
 }
 
 cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_w_wide,
-                         const CUtensorMap* tm_h, int NT, int grid, cudaStream_t s) {
-    // decode tiles stream W2 in 256-wide K stages when I allows it (halves the per-stage cost per byte)
-    if (NT == 32) return a.ktiles % 2 == 0 ? launch<false, 32, 2, false>(a, tm_w, tm_h, grid, s)
+                         const CUtensorMap* tm_w_k2, const CUtensorMap* tm_h, const CUtensorMap* tm_h_k2, int NT,
+                         int grid, cudaStream_t s) {
+    // decode tiles stream W2 in 256-wide K stages when I allows it (halves the per-stage cost per byte),
+    // each operand's two K chunks in one box of its two-chunk view
+    if (NT == 32) return a.ktiles % 2 == 0 ? launch<false, 32, 2, false>(a, tm_w_k2, tm_h_k2, grid, s)
                                            : launch<false, 32, 1, false>(a, tm_w, tm_h, grid, s);
     // prefill route tiles: pairs of W2 tiles (a.m_rows == 256) when H allows it
     if (NT == 128)

@@ -105,8 +105,10 @@ struct GemmArgs {
 cudaError_t launch_gemm1(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_x, int NT, int grid,
                          cudaStream_t s);
 // tm_w_wide: W2 with 256-row boxes, used when a.m_rows == 256 (128-row route tiles, H % 256 == 0)
+// tm_w_k2 / tm_h_k2: two-chunk views (one box = two 128-wide K chunks) for 256-wide K stages
 cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_w_wide,
-                         const CUtensorMap* tm_h, int NT, int grid, cudaStream_t s);
+                         const CUtensorMap* tm_w_k2, const CUtensorMap* tm_h, const CUtensorMap* tm_h_k2, int NT,
+                         int grid, cudaStream_t s);
 cudaError_t gemm_set_attributes();
 
 // ------------------------------------------------------------------ single-launch fused path (moe_fused.cu)
