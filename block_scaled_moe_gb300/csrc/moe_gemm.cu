@@ -100,7 +100,7 @@ struct Cfg {
     static_assert(MW <= 4, "barrier slots");
     static_assert(CW % 8 == 0, "epilogue column split");
     static constexpr int LDC = CW % 16 == 0 ? 16 : 8;      // TMEM columns per epilogue load
-    static constexpr bool SF_VEC = KC == 1 && NT >= 128;   // weight scales read as 16-byte vectors (4 stages)
+    static constexpr bool SF_VEC = KC == 1 && NT >= 128;   // prefill tiles: weight scales as 8- or 16-byte vectors
 };
 
 // SwiGLU of one (gate, up) pair with the optional clamp (ROCm/aiter PR #6154 "clamp-10 SwiGLU":
@@ -129,6 +129,12 @@ __device__ __forceinline__ void store_rows_bf16(uint16_t* y, const float (&v)[CW
         }
     }
 }
+
+// 32-bit word j of a vector of weight-scale words
+__device__ __forceinline__ uint32_t vword(const uint4& v, int j) {
+    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ uint32_t vword(const uint2& v, int j) { return j == 0 ? v.x : v.y; }
 
 // LDC-column TMEM load (32 lanes x 32 bit) of the epilogue
 template <int L>
@@ -261,18 +267,26 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
         // Prefill tiles leave ~20 KB of L1 beside the stage ring, less than the 32 KB of scale lines a
         // unit touches, so 4-byte gathers per row and stage miss L1 every time and their requests,
         // not the weight stream, set the pace.  When the rows' scale stride allows, each lane loads
-        // one 16-byte vector per row that holds the scales of 4 consecutive stages, two groups of 4
-        // stages ahead.
-        const bool sf_vec = C::SF_VEC && (a.ld_sf & 15) == 0 && (KT & 3) == 0 &&
-                            (reinterpret_cast<uintptr_t>(a.w_sf) & 15) == 0;
-        if (sf_vec) {
-            constexpr int GD = 2;          // groups of 4 stages loaded ahead
-            constexpr int NV = 4 * NA;     // 16-byte vectors per lane and group: [op][row group]
-            uint4 gring[GD][NV];
-            const int GPU = KT >> 2;       // groups per unit
+        // one 16-byte (else 8-byte) vector per row that holds the scales of 4 (2) consecutive stages,
+        // 8 stages ahead.  (Decode tiles keep the 4-byte gathers: their scale lines stay in L1, and
+        // 8-byte vectors for the 256-wide GEMM2 stages measured slower.)
+        // Vector widths: 16 bytes (uint4) or 8 bytes (uint2) per row, covering SPV = bytes / (4 KC)
+        // consecutive K stages, when the scale rows and the unit's stages allow it.
+        auto vec_ok = [&](int vb) {
+            const int spv = vb / (4 * KC);
+            return spv >= 1 && a.ld_sf % vb == 0 && KT % spv == 0 && (reinterpret_cast<uintptr_t>(a.w_sf) % vb) == 0;
+        };
+        auto vec_loop = [&](auto vtag) {
+            using V = decltype(vtag);
+            constexpr int WPV = static_cast<int>(sizeof(V)) / 4;  // 32-bit words per vector
+            constexpr int SPV = WPV / KC;                         // K stages per vector
+            constexpr int GD = 8 / SPV > 1 ? 8 / SPV : 1;          // vector groups loaded ahead (8 stages)
+            constexpr int NV = 4 * NA;                            // vectors per lane and group: [op][row group]
+            V gring[GD][NV];
+            const int GPU = KT / SPV;  // groups per unit
             int q_ui = 0, q_g = 0, q_ecur = 0;
             const uint8_t* q_src = nullptr;
-            auto gload = [&](uint4(&dst)[NV]) {
+            auto gload = [&](V(&dst)[NV]) {
                 if (q_ui >= my_units) return;
                 if (q_g == 0) {
                     const UnitInfo pu = decode_unit(blockIdx.x + q_ui * gridDim.x, q_ecur, pl, a.mtiles, NT);
@@ -283,8 +297,9 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                 for (int op = 0; op < NA; ++op)
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        dst[op * 4 + i] = __ldg(reinterpret_cast<const uint4*>(
-                            q_src + static_cast<size_t>(op * a.up_off + 32 * i * a.w_rs) * a.ld_sf + q_g * 16));
+                        dst[op * 4 + i] = __ldg(reinterpret_cast<const V*>(
+                            q_src + static_cast<size_t>(op * a.up_off + 32 * i * a.w_rs) * a.ld_sf +
+                            static_cast<size_t>(q_g) * sizeof(V)));
                 if (++q_g == GPU) {
                     q_g = 0;
                     ++q_ui;
@@ -301,22 +316,23 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                 for (int d = 0; d < GD; ++d) {
                     if (G0 + d >= ngroups || !ok) continue;
 #pragma unroll
-                    for (int sq = 0; sq < 4; ++sq) {
+                    for (int sq = 0; sq < SPV; ++sq) {
                         if (!ok) continue;
                         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
                                        kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
                             ok = false;
                             continue;
                         }
-                        uint4* dst = reinterpret_cast<uint4*>(sSFA + stage * NA * 512) + lane;
+                        uint4* dst = reinterpret_cast<uint4*>(sSFA + stage * NA * KC * 512) + lane;
 #pragma unroll
-                        for (int op = 0; op < NA; ++op) {  // stage sq's word of each row is component sq
-                            const uint4* v = gring[d] + op * 4;
-                            dst[32 * op] = sq == 0   ? make_uint4(v[0].x, v[1].x, v[2].x, v[3].x)
-                                           : sq == 1 ? make_uint4(v[0].y, v[1].y, v[2].y, v[3].y)
-                                           : sq == 2 ? make_uint4(v[0].z, v[1].z, v[2].z, v[3].z)
-                                                     : make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
-                        }
+                        for (int op = 0; op < NA; ++op)
+#pragma unroll
+                            for (int c = 0; c < KC; ++c) {  // atom (op, chunk): word sq * KC + c of each row
+                                const V* v = gring[d] + op * 4;
+                                const int j = sq * KC + c;
+                                dst[32 * (op * KC + c)] =
+                                    make_uint4(vword(v[0], j), vword(v[1], j), vword(v[2], j), vword(v[3], j));
+                            }
                         fence_proxy_async_smem();
                         mbar_arrive(&full[stage]);
                         if (++stage == STAGES) {
@@ -327,6 +343,11 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                     if (ok) gload(gring[d]);
                 }
             }
+        };
+        if (C::SF_VEC && vec_ok(16)) {
+            vec_loop(uint4{});
+        } else if (C::SF_VEC && vec_ok(8)) {
+            vec_loop(uint2{});
         } else {
             constexpr int SD = 8;
             constexpr int NW = 4 * NA * KC;  // words per lane per stage: [op][chunk][row group]
