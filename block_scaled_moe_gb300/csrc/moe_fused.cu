@@ -658,6 +658,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             // of 16 bytes take one 16-byte load per row and group: the weight-scale lines then need
             // not stay in L1, which this kernel's shared-memory footprint leaves small.
             const bool g1_vec = (H % 512) == 0;
+            const bool g2_pair = f.kc2 == 2 && (I / 32) % 8 == 0;  // 8-byte aligned scale rows
             int q_ui = 0, q_kk = 0, q_kt = 0, q_ld = 0, q_rs = 1;
             bool q_g2 = false;
             const uint8_t* q_base = nullptr;
@@ -682,6 +683,19 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                         for (int i = 0; i < 4; ++i)
                             g[a4][i] = __ldg(reinterpret_cast<const uint4*>(
                                 q_base + static_cast<size_t>(a4 * f.w13_up + 32 * i * q_rs) * q_ld + q_kk * 4));
+                } else if (q_g2 && g2_pair) {
+                    // 256-wide GEMM2 stages: the two K chunks' words of a row are one 8-byte pair
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint2 p4[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            p4[j] = j < len ? __ldg(reinterpret_cast<const uint2*>(
+                                                  q_base + static_cast<size_t>(32 * i) * q_ld + (q_kk + j) * 8))
+                                            : make_uint2(0u, 0u);
+                        g[0][i] = make_uint4(p4[0].x, p4[1].x, p4[2].x, p4[3].x);
+                        g[1][i] = make_uint4(p4[0].y, p4[1].y, p4[2].y, p4[3].y);
+                    }
                 } else {
 #pragma unroll
                     for (int a4 = 0; a4 < 2; ++a4) {
