@@ -49,6 +49,8 @@ FUSED_CFGS = [
     (512, 256, 256, 16, 6, 500, "uniform", 0.05, 0.0, "compact"),  # the largest capacity the fused path takes
     (64, 128, 256, 512, 16, 64, "uniform", 0.1, 10.0, "compact"),  # E = 512 and top-16: the table limits
     (96, 384, 512, 40, 8, 90, "hot_zipf", 0.1, 0.0, "fixed"),
+    # GEMM1 units not a multiple of the grid, several rounds of GEMM2 units per CTA, H = 1024
+    (256, 1024, 512, 128, 8, 250, "uniform", 0.02, 10.0, "compact"),
 ]
 
 
