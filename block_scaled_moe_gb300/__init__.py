@@ -90,6 +90,12 @@ def load(path: Optional[str] = None):
         lib.moe_forward_routed.restype = i32
         lib.moe_dispatch_compact_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         lib.moe_dispatch_compact_noalloc.restype = i32
+        lib.moe_set_path_table.argtypes = [vp, vp, vp, i32]
+        lib.moe_set_path_table.restype = i32
+        lib.moe_get_path_table.argtypes = [vp, vp, vp, i32]
+        lib.moe_get_path_table.restype = i32
+        lib.moe_autotune.argtypes = [vp, vp, i32, i32, vp]
+        lib.moe_autotune.restype = i32
         _lib = lib
         return lib
 
@@ -170,6 +176,33 @@ def topk_softmax(router_logits, topk: int, num_valid_rows=None, renormalize: boo
                      None if num_valid_rows is None else num_valid_rows.data_ptr(), renormalize, ids.data_ptr(),
                      w.data_ptr(), s.cuda_stream)
     return ids, w
+
+
+def _i32_array(vals):
+    arr = (ctypes.c_int32 * max(1, len(vals)))(*[int(v) for v in vals])
+    return arr
+
+
+def moe_set_path_table(h, t: list, path: list):
+    if len(t) != len(path):
+        raise ValueError("t and path must have the same length")
+    ta, pa = _i32_array(t), _i32_array(path)
+    _check(h, load().moe_set_path_table(h, ctypes.cast(ta, ctypes.c_void_p), ctypes.cast(pa, ctypes.c_void_p), len(t)))
+
+
+def moe_get_path_table(h) -> tuple:
+    lib = load()
+    n = lib.moe_get_path_table(h, None, None, 0)
+    if n < 0:
+        _check(h, n)
+    ta, pa = _i32_array([0] * n), _i32_array([0] * n)
+    lib.moe_get_path_table(h, ctypes.cast(ta, ctypes.c_void_p), ctypes.cast(pa, ctypes.c_void_p), n)
+    return list(ta)[:n], list(pa)[:n]
+
+
+def moe_autotune(h, t_buckets: list, reps: int = 5, stream: int = 0):
+    ta = _i32_array(t_buckets)
+    _check(h, load().moe_autotune(h, ctypes.cast(ta, ctypes.c_void_p), len(t_buckets), reps, stream))
 
 
 def moe_destroy(h):
@@ -292,6 +325,24 @@ class BlockScaledMoE:
     @property
     def last_path(self) -> str:
         return {MOE_PATH_FUSED: "fused", MOE_PATH_MULTI: "multi"}.get(load().moe_last_path(self.h), "none")
+
+    def autotune(self, t_buckets, reps: int = 5, stream=None) -> dict:
+        """Measure the paths for each bucket T on synthetic inputs; returns {T: "fused" | "multi"}."""
+        import torch
+        s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        moe_autotune(self.h, list(t_buckets), reps, s)
+        return self.path_table
+
+    @property
+    def path_table(self) -> dict:
+        t, p = moe_get_path_table(self.h)
+        return {ti: {MOE_PATH_FUSED: "fused", MOE_PATH_MULTI: "multi"}[pi] for ti, pi in zip(t, p)}
+
+    def set_path_table(self, table: dict):
+        """Replace the T-bucketed path table ({T: "fused" | "multi"}; empty dict clears it)."""
+        items = sorted(table.items())
+        code = {"fused": MOE_PATH_FUSED, "multi": MOE_PATH_MULTI}
+        moe_set_path_table(self.h, [t for t, _ in items], [code[p] for _, p in items])
 
     @property
     def launches(self) -> int:

@@ -6,7 +6,9 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -65,6 +67,8 @@ struct moe_ctx {
     bool profiled = false;
     int opt_path = MOE_PATH_AUTO;
     int last_path = 0;
+    // T-bucketed path table (bucket T ascending, MOE_PATH_FUSED / MOE_PATH_MULTI); empty = default rule
+    std::vector<int32_t> tune_t, tune_path;
     bool coop = false;  // device supports cooperative launches
     cudaEvent_t ev[MOE_PROFILE_STAGES + 1] = {};
     unsigned long long launches = 0;
@@ -394,6 +398,21 @@ int moe_select_layer(moe_handle h, int slot) {
     return MOE_OK;
 }
 
+namespace {
+
+// Path of the table bucket nearest to T (ties: the larger bucket), as the pages' configuration
+// lookup does for a token count between measured buckets.
+int table_path(const moe_ctx* h, int T) {
+    size_t best = 0;
+    for (size_t i = 1; i < h->tune_t.size(); ++i) {
+        const long d = std::labs((long)h->tune_t[i] - T), db = std::labs((long)h->tune_t[best] - T);
+        if (d <= db) best = i;  // ascending buckets: "<=" lets the larger of two equal distances win
+    }
+    return h->tune_path[best];
+}
+
+}  // namespace
+
 int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const float* topk_weights,
                 const int32_t* num_valid_rows, void* out, int T, moe_stream_t stream) {
     if (!h) return MOE_EINVAL;
@@ -422,7 +441,8 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     uint8_t* ys = y8 ? y8 + (size_t)g.rows_cap * g.H : nullptr;
     mark(0);
     const bool fused = h->opt_path != MOE_PATH_MULTI && h->coop && bmoe::fused_supported(g) &&
-                       (h->opt_path == MOE_PATH_FUSED || T <= 512);
+                       (h->opt_path == MOE_PATH_FUSED ||
+                        (h->tune_t.empty() ? T <= 512 : table_path(h, T) == MOE_PATH_FUSED));
     if (fused) {
         bmoe::FusedLaunch fl;
         fl.x = static_cast<const uint16_t*>(x);
@@ -829,3 +849,128 @@ int moe_debug_copy(moe_handle h, int which, void* host_dst, size_t* bytes, moe_s
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ T-bucketed path table
+int moe_set_path_table(moe_handle h, const int32_t* t, const int32_t* path, int n) {
+    if (!h) return MOE_EINVAL;
+    if (n < 0 || n > MOE_TUNE_MAX || (n > 0 && (!t || !path)))
+        return fail(h, MOE_EINVAL, "a path table has 0..%d entries and non-NULL arrays", MOE_TUNE_MAX);
+    const bool fused_ok = h->coop && bmoe::fused_supported(h->geo);
+    for (int i = 0; i < n; ++i) {
+        if (t[i] < 1 || t[i] > h->geo.cap || (i > 0 && t[i] <= t[i - 1]))
+            return fail(h, MOE_EINVAL, "bucket T values must ascend strictly within [1, capacity=%d]", h->geo.cap);
+        if (path[i] != MOE_PATH_FUSED && path[i] != MOE_PATH_MULTI)
+            return fail(h, MOE_EINVAL, "entry %d: path %d is neither MOE_PATH_FUSED nor MOE_PATH_MULTI", i, path[i]);
+        if (path[i] == MOE_PATH_FUSED && !fused_ok)
+            return fail(h, MOE_EINVAL, "entry %d: this handle cannot run the fused path", i);
+    }
+    h->tune_t.assign(t, t + n);
+    h->tune_path.assign(path, path + n);
+    return MOE_OK;
+}
+
+int moe_get_path_table(moe_handle h, int32_t* t, int32_t* path, int cap) {
+    if (!h || cap < 0) return MOE_EINVAL;
+    const int n = static_cast<int>(h->tune_t.size());
+    for (int i = 0; i < n && i < cap; ++i) {
+        if (t) t[i] = h->tune_t[i];
+        if (path) path[i] = h->tune_path[i];
+    }
+    return n;
+}
+
+int moe_autotune(moe_handle h, const int32_t* t_buckets, int n, int reps, moe_stream_t stream) {
+    if (!h) return MOE_EINVAL;
+    if (n < 1 || n > MOE_TUNE_MAX || !t_buckets || reps < 1)
+        return fail(h, MOE_EINVAL, "autotune takes 1..%d bucket T values and reps >= 1", MOE_TUNE_MAX);
+    const Geometry& g = h->geo;
+    for (int i = 0; i < n; ++i)
+        if (t_buckets[i] < 1 || t_buckets[i] > g.cap || (i > 0 && t_buckets[i] <= t_buckets[i - 1]))
+            return fail(h, MOE_EINVAL, "bucket T values must ascend strictly within [1, capacity=%d]", g.cap);
+    if (!h->slots[h->cur].bound) return fail(h, MOE_ENOTBOUND, "no weights bound");
+    const bool fused_ok = h->coop && bmoe::fused_supported(g);
+    std::vector<int32_t> paths(n, MOE_PATH_MULTI);
+    if (!fused_ok) return moe_set_path_table(h, t_buckets, paths.data(), n);
+
+    // Synthetic inputs of the largest bucket: BF16 rows from a fixed linear congruential sequence,
+    // K distinct experts per row, equal weights.  A 256 MiB buffer is written before every timed
+    // forward so that the weights stream from HBM as they do in a real step.
+    const int T = t_buckets[n - 1], K = g.K, E = g.E, H = g.H;
+    std::vector<uint16_t> hx((size_t)T * H);
+    std::vector<int32_t> hid((size_t)T * K);
+    std::vector<float> hw((size_t)T * K, 1.0f / K);
+    uint32_t st = 12345u;
+    auto next = [&st]() { st = st * 1664525u + 1013904223u; return st; };
+    for (auto& v : hx) {
+        const float f = (static_cast<int>(next() >> 9) - (1 << 22)) / static_cast<float>(1 << 22);
+        uint32_t b;
+        std::memcpy(&b, &f, 4);
+        v = static_cast<uint16_t>(b >> 16);
+    }
+    for (int t = 0; t < T; ++t) {
+        const int base = static_cast<int>(next() % E), step = 1 + static_cast<int>(next() % std::max(1, E - 1));
+        for (int k = 0; k < K; ++k) hid[(size_t)t * K + k] = (base + k * step) % E;
+        // (distinct unless step shares a factor with E; a repeated id is a valid input too)
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *dx = nullptr, *did = nullptr, *dw = nullptr, *dout = nullptr, *dflush = nullptr;
+    const size_t flush_bytes = 256u << 20;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    int rc = MOE_OK;
+    const int saved_path = h->opt_path;
+    auto cleanup = [&]() {
+        h->opt_path = saved_path;
+        cudaFree(dx);
+        cudaFree(did);
+        cudaFree(dw);
+        cudaFree(dout);
+        cudaFree(dflush);
+        if (e0) cudaEventDestroy(e0);
+        if (e1) cudaEventDestroy(e1);
+    };
+    cudaError_t e = cudaMalloc(&dx, hx.size() * 2);
+    if (e == cudaSuccess) e = cudaMalloc(&did, hid.size() * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&dw, hw.size() * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&dout, hx.size() * 2);
+    if (e == cudaSuccess) e = cudaMalloc(&dflush, flush_bytes);
+    if (e == cudaSuccess) e = cudaEventCreate(&e0);
+    if (e == cudaSuccess) e = cudaEventCreate(&e1);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dx, hx.data(), hx.size() * 2, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(did, hid.data(), hid.size() * 4, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dw, hw.data(), hw.size() * 4, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) {
+        cleanup();
+        return cuda_fail(h, e, "autotune setup");
+    }
+    for (int i = 0; i < n && rc == MOE_OK; ++i) {
+        float best = 0.f;
+        for (int p : {MOE_PATH_FUSED, MOE_PATH_MULTI}) {
+            h->opt_path = p;
+            float total = 0.f;
+            for (int r = -1; r < reps && rc == MOE_OK; ++r) {  // r = -1: untimed warm-up
+                e = cudaMemsetAsync(dflush, r & 0xff, flush_bytes, s);
+                if (e == cudaSuccess) e = cudaEventRecord(e0, s);
+                if (e != cudaSuccess) break;
+                rc = moe_forward(h, dx, static_cast<const int32_t*>(did), static_cast<const float*>(dw), nullptr, dout,
+                                 t_buckets[i], stream);
+                if (rc != MOE_OK) break;
+                e = cudaEventRecord(e1, s);
+                if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+                float ms = 0.f;
+                if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+                if (e != cudaSuccess) break;
+                if (r >= 0) total += ms;
+            }
+            if (e != cudaSuccess && rc == MOE_OK) rc = cuda_fail(h, e, "autotune timing");
+            if (rc != MOE_OK) break;
+            if (p == MOE_PATH_FUSED || total < best) {
+                best = total;
+                paths[i] = p;
+            }
+        }
+    }
+    cleanup();
+    if (rc != MOE_OK) return rc;
+    return moe_set_path_table(h, t_buckets, paths.data(), n);
+}
+

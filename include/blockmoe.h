@@ -220,6 +220,32 @@ int moe_dispatch_scheme(moe_handle h);
 /* Path the last forward took: MOE_PATH_FUSED or MOE_PATH_MULTI (0 before any forward). */
 int moe_last_path(moe_handle h);
 
+/* ------------------------------------------------ T-bucketed path table
+ * ROCm/aiter PR #6154, "Changes and tuning": a measured configuration table per
+ * source-token bucket M, an arbitrary M taking the nearest bucket with ties to
+ * the larger.  Here the per-T choice is the path (the dispatch scheme and the
+ * route tile follow the handle's capacity).  With a non-empty table, a forward
+ * under MOE_PATH_AUTO takes the path of the bucket nearest to T (ties: the
+ * larger bucket); with an empty one (the default) it takes the fused kernel for
+ * T <= 512 whenever the handle allows it.  MOE_PATH_FUSED / MOE_PATH_MULTI set
+ * by moe_set_option still override the table. */
+#define MOE_TUNE_MAX 64
+/* Replace the table: n (0..MOE_TUNE_MAX) buckets, t strictly ascending in
+ * [1, capacity], path MOE_PATH_FUSED or MOE_PATH_MULTI (FUSED only where the
+ * handle allows it).  n = 0 clears it.  Refused tables change nothing. */
+int moe_set_path_table(moe_handle h, const int32_t* t, const int32_t* path, int n);
+/* Copy up to `cap` entries into t / path (either may be NULL); returns the
+ * number of entries (or a negative error). */
+int moe_get_path_table(moe_handle h, int32_t* t, int32_t* path, int cap);
+/* Measure each path the handle allows for every bucket T (strictly ascending
+ * in [1, capacity], n <= MOE_TUNE_MAX) on synthetic inputs and the bound
+ * weights: `reps` timed forwards after one warm-up, a 256 MiB buffer written
+ * before each so the weights come from HBM; record the faster path per bucket as
+ * the table.  Allocates its inputs (device memory for the largest T and the
+ * 256 MiB buffer), synchronises `stream`, and is not capturable: run it once
+ * after binding.  MOE_ENOTBOUND without weights. */
+int moe_autotune(moe_handle h, const int32_t* t_buckets, int n, int reps, moe_stream_t stream);
+
 /* ------------------------------------------------ router top-k in front of dispatch */
 #define MOE_DTYPE_F32 0
 #define MOE_DTYPE_BF16 1

@@ -22,6 +22,7 @@ def test_every_declared_symbol_is_exported(lib):
                 "moe_get_option", "moe_workspace_bytes", "moe_set_workspace", "moe_read_status",
                 "moe_last_error", "moe_dispatch_scheme", "moe_debug_copy", "moe_profile_read",
                 "moe_last_path", "moe_dispatch_compact_noalloc", "moe_bind_layer", "moe_select_layer", "moe_topk_softmax",
+                "moe_set_path_table", "moe_get_path_table", "moe_autotune",
                 "moe_forward_routed"}
     assert expected <= set(names)
     for n in names:
