@@ -207,12 +207,15 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer (one thread)
-        if (lane == 0) {
+        // ------------------------------------------------------------ TMA producer (one warp, one elected lane issues)
+        {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_b = policy_evict_last();
-            prefetch_tmap(&tm_w);
-            prefetch_tmap(&tm_b);
+            if (lane == 0) {
+                prefetch_tmap(&tm_w);
+                prefetch_tmap(&tm_b);
+            }
+            __syncwarp();
             int stage = 0, ecur = 0;
             uint32_t phase = 0;
             long issued = 0;
@@ -222,32 +225,36 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                 const int wrow = cu.e * a.w_rows + cu.m * a.m_rows;  // GEMM2 (GEMM1 reads the W13 pair view)
                 const uint8_t* b_sf = a.b_sf + static_cast<size_t>(cu.g) * a.ktiles * NB * 512;
                 for (int kk = 0; kk < KT; ++kk) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
-                                   kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
+                    const bool got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status,
+                                               kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs);
+                    if (!__all_sync(0xffffffffu, got)) {  // the lanes agree: the warp stays converged
                         ok = false;
                         break;
                     }
-                    trace(a, 0, issued);
-                    mbar_expect_tx(&full[stage], KC * (NA * C::A_TX + C::B_BYTES + NB * 512));
+                    if (lane == 0) trace(a, 0, issued);
+                    // the producer's arrival carries the stage's transaction bytes; the stage completes
+                    // when they have landed and the scale warp has arrived
+                    mbar_arrive_expect_tx_w(&full[stage], KC * (NA * C::A_TX + C::B_BYTES + NB * 512));
                     if constexpr (KC == 2) {  // two-chunk views: one box per operand lands both K chunks
-                        tma_load_3d(sA + (stage * NA) * KC * C::A_BYTES, &tm_w, &full[stage], 0, wrow, kk * KC, pol_w);
-                        tma_load_3d(sB + stage * KC * C::B_BYTES, &tm_b, &full[stage], 0, cu.row0, kk * KC, pol_b);
+                        tma_load_3d_w(sA + (stage * NA) * KC * C::A_BYTES, &tm_w, &full[stage], 0, wrow, kk * KC,
+                                      pol_w);
+                        tma_load_3d_w(sB + stage * KC * C::B_BYTES, &tm_b, &full[stage], 0, cu.row0, kk * KC, pol_b);
                     } else {
 #pragma unroll
                         for (int c = 0; c < KC; ++c) {
                             const int k0 = (kk * KC + c) * 128;
                             if constexpr (G1)  // gate and up tiles of feature tile m: one box {128, 128, 2, 1}
-                                tma_load_4d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0,
-                                            cu.m * 128, 0, cu.e, pol_w);
+                                tma_load_4d_w(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0,
+                                              cu.m * 128, 0, cu.e, pol_w);
                             else  // W2 tile (WIDE: a 256-row box, the unit's two tiles back to back)
-                                tma_load_2d(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0, wrow,
-                                            pol_w);
-                            tma_load_2d(sB + (stage * KC + c) * C::B_BYTES, &tm_b, &full[stage], k0, cu.row0, pol_b);
+                                tma_load_2d_w(sA + ((stage * NA) * KC + c) * C::A_BYTES, &tm_w, &full[stage], k0,
+                                              wrow, pol_w);
+                            tma_load_2d_w(sB + (stage * KC + c) * C::B_BYTES, &tm_b, &full[stage], k0, cu.row0,
+                                          pol_b);
                         }
                     }
-                    bulk_load(sSFB + stage * KC * NB * 512, b_sf + kk * KC * NB * 512, KC * NB * 512, &full[stage]);
-                    mbar_arrive(&full[stage]);
-                    trace(a, 1, issued);
+                    bulk_load_w(sSFB + stage * KC * NB * 512, b_sf + kk * KC * NB * 512, KC * NB * 512, &full[stage]);
+                    if (lane == 0) trace(a, 1, issued);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -255,7 +262,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                     }
                 }
             }
-            drain_stages<STAGES>(full, stage, phase, issued, a.status);
+            if (lane == 0) drain_stages<STAGES>(full, stage, phase, issued, a.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ weight-scale producer (32 lanes)
