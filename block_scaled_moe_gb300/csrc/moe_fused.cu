@@ -200,9 +200,9 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
 #ifdef BMOE_TRACE
         const long long tw0 = (long long)globaltimer_ns();
 #endif
-        if (!mbar_wait(&p.empty[r.stage], r.phase ^ 1u, p.abort_flag, p.status, kStTimeout | (1u << (kSiteShift + 0)),
-                       kWaitLimitNs))
-            return false;
+        const bool got = mbar_wait(&p.empty[r.stage], r.phase ^ 1u, p.abort_flag, p.status,
+                                   kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, got)) return false;  // the warp stays converged for the elected issue
 #ifdef BMOE_TRACE
         const long long tw1 = (long long)globaltimer_ns();
         wait_ns += tw1 - tw0;
@@ -213,23 +213,23 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
         uint64_t* fb = &p.full[r.stage];
         uint8_t* a0 = p.sA + (r.stage * 2) * F_A_BYTES;
         uint8_t* b0 = p.sB + (r.stage * 2) * F_B_BYTES;
+        // the producer's arrival carries the stage's transaction bytes (one elected lane issues)
         if constexpr (!G2) {
-            mbar_expect_tx(fb, 2 * F_A_TX + F_B_BYTES + 512);
-            tma_load_4d(a0, tw, fb, kk * 128, wrow, 0, e, pol_w);
-            tma_load_2d(b0, tb, fb, kk * 128, row0, pol_b);
-            bulk_load(p.sSFB + (r.stage * 2) * 512, bsf + static_cast<size_t>(kk) * 512, 512, fb);
+            mbar_arrive_expect_tx_w(fb, 2 * F_A_TX + F_B_BYTES + 512);
+            tma_load_4d_w(a0, tw, fb, kk * 128, wrow, 0, e, pol_w);
+            tma_load_2d_w(b0, tb, fb, kk * 128, row0, pol_b);
+            bulk_load_w(p.sSFB + (r.stage * 2) * 512, bsf + static_cast<size_t>(kk) * 512, 512, fb);
         } else {
-            mbar_expect_tx(fb, KC * (F_A_TX + F_B_BYTES + 512));
+            mbar_arrive_expect_tx_w(fb, KC * (F_A_TX + F_B_BYTES + 512));
             if constexpr (KC == 2) {  // two-chunk views (the launch passes them for 256-wide stages)
-                tma_load_3d(a0, tw, fb, 0, wrow, kk * KC, pol_w);
-                tma_load_3d(b0, tb, fb, 0, row0, kk * KC, pol_b);
+                tma_load_3d_w(a0, tw, fb, 0, wrow, kk * KC, pol_w);
+                tma_load_3d_w(b0, tb, fb, 0, row0, kk * KC, pol_b);
             } else {
-                tma_load_2d(a0, tw, fb, kk * 128, wrow, pol_w);
-                tma_load_2d(b0, tb, fb, kk * 128, row0, pol_b);
+                tma_load_2d_w(a0, tw, fb, kk * 128, wrow, pol_w);
+                tma_load_2d_w(b0, tb, fb, kk * 128, row0, pol_b);
             }
-            bulk_load(p.sSFB + (r.stage * 2) * 512, bsf + static_cast<size_t>(kk) * KC * 512, KC * 512, fb);
+            bulk_load_w(p.sSFB + (r.stage * 2) * 512, bsf + static_cast<size_t>(kk) * KC * 512, KC * 512, fb);
         }
-        mbar_arrive(fb);
 #ifdef BMOE_TRACE
         issue_ns += (long long)globaltimer_ns() - tw1;
 #endif
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         const Plan pl{t_tile, t_row, t_cnt};
         if (threadIdx.x == 0) {
             for (int s = 0; s < F_STAGES; ++s) {
-                mbar_init(&full[s], 1 + 32);
+                mbar_init(&full[s], 1 + 32);  // the producer's arrive.expect_tx + the scale warp's lanes
                 mbar_init(&empty[s], F_MW);
             }
             for (int b = 0; b < 2; ++b) {
@@ -585,8 +585,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         p.status = ws.status;
         p.tmem = tmem;
         if (warp == 0) {
-            // -------------------------------------------------------- TMA producer (one thread)
-            if (lane == 0 && my_units > 0) {
+            // -------------------------------------------------------- TMA producer (one warp, one elected lane issues)
+            if (my_units > 0) {
 #ifdef BMOE_TRACE
                 long long wait_ns = 0;
                 bool first_g2 = true;
@@ -622,6 +622,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                         }
                         __nanosleep(64);
                     }
+                    ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
 #ifdef BMOE_TRACE
                     {
@@ -647,7 +648,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 FTRACE(28, pi1);
                 FTRACE(29, pi2);
 #endif
-                drain_stages<F_STAGES>(full, ring.stage, ring.phase, issued, ws.status);
+                if (lane == 0) drain_stages<F_STAGES>(full, ring.stage, ring.phase, issued, ws.status);
             }
         } else if (warp == 1) {
             // -------------------------------------------------------- weight-scale producer (32 lanes)
