@@ -30,10 +30,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
         "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
         : "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -81,16 +77,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
-// ------------------------------------------------------------------ cp.async
-// 4-byte asynchronous copy global -> shared (cached in L1 and L2).
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-// Arrive on `bar` once every cp.async this thread issued so far has landed
-// (the arrival counts against the barrier's expected count).
-__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -115,10 +101,6 @@ __device__ __forceinline__ uint32_t atom_add_release_u32(uint32_t* p, uint32_t v
     asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
-// Named barrier over `n` threads (a multiple of 32) of the CTA.
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 // ------------------------------------------------------------------ L2 policies
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -133,43 +115,10 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 }
 
 // ------------------------------------------------------------------ TMA
-// 2D tiled load of one box into shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
-        : "memory");
-}
-// 4D tiled load of one box into shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
-                                            int c3, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
-        : "memory");
-}
-// 3D tiled load of one box into shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-        : "memory");
-}
-// Contiguous bulk copy global -> shared (16-byte aligned, size multiple of 16).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-// Warp-level forms of the loads above: executed by a whole converged warp, one lane (elected
-// with elect.sync over the full mask) issues.  A single thread issuing from a divergent branch
+// Tiled TMA loads (2D / 3D / 4D box into shared memory, completing on `bar`), the contiguous bulk
+// copy (16-byte aligned, size a multiple of 16) and the producer's arrival with its transaction
+// bytes, in warp-level form: executed by a whole converged warp, one lane (elected with elect.sync
+// over the full mask) issues.  A single thread issuing from a divergent branch
 // spends ~440 cycles per box plus barrier operation on GB300; the converged form ~330, and a second
 // issuing warp doubles the rate, so the producers issue this way.
 #define BMOE_ELECT_ISSUE(body) \
@@ -211,16 +160,6 @@ __device__ __forceinline__ void bulk_load_w(void* dst, const void* src, uint32_t
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
-// Prefetch one box of a tensor map into L2 (no shared-memory destination).// Prefetch one box of a tensor map into L2 (no shared-memory destination).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
-}
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
-}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -243,29 +182,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
-}
-// Copy 32 rows x 128 bits from shared memory into TMEM lanes 0-31 (replicated
-// into the four 32-lane quadrants), four 32-bit columns starting at taddr.
-__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-// D(tmem) (+)= A(smem) * B(smem)^T with one E8M0 scale per 32 K-elements per row
-// of A and of B, the scales read from TMEM (kind::mxf8f6f4).
-__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-        : "memory");
-}
 // Warp-level issue: the three helpers below are executed by a whole converged warp and one lane,
 // elected with elect.sync over the full mask (the lowest lane, so the same lane every time),
 // issues the operation.  Keeping the issuing code warp-uniform lets its operands stay in the
@@ -273,6 +189,9 @@ __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint6
 // and keeps the tensor pipe saturated from N = 128 up, where a divergent single-lane branch
 // needs ~100 cycles per MMA.  tcgen05.commit tracks the operations of the issuing thread, so
 // the MMAs, the scale copies and their commits of one warp all go through these helpers.
+//
+// Copy 32 rows x 128 bits from shared memory into TMEM lanes 0-31 (replicated into the four
+// 32-lane quadrants), four 32-bit columns starting at taddr.
 __device__ __forceinline__ void tc_cp_32x128b_x4_w(uint32_t taddr, uint64_t sdesc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t.reg .b32 e;\n\t"
@@ -281,6 +200,8 @@ __device__ __forceinline__ void tc_cp_32x128b_x4_w(uint32_t taddr, uint64_t sdes
         "l"(sdesc)
         : "memory");
 }
+// D(tmem) (+)= A(smem) * B(smem)^T with one E8M0 scale per 32 K-elements per row of A and of B,
+// the scales read from TMEM (kind::mxf8f6f4); `accumulate` = 0 overwrites D.
 __device__ __forceinline__ void tc_mma_mx_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
     asm volatile(
@@ -292,6 +213,7 @@ __device__ __forceinline__ void tc_mma_mx_w(uint32_t d_tmem, uint64_t adesc, uin
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
         : "memory");
 }
+// Arrive on `bar` once every tcgen05 operation the issuing lane issued so far has completed.
 __device__ __forceinline__ void tc_commit_w(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t.reg .b32 e;\n\t"
