@@ -240,11 +240,11 @@ def main():
     __graft_entry__.build()
     import block_scaled_moe_gb300 as bm
 
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)  # before the process group, so that NCCL binds this rank's GPU
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
 
     x = synth.make_x(w)
     ids, wts = synth.make_routing(w)
