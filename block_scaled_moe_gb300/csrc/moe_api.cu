@@ -601,6 +601,15 @@ int moe_set_option(moe_handle h, int key, double value) {
             h->y_format = v;
             return MOE_OK;
         }
+        case MOE_OPT_DEBUG_GRID_GEN: {
+            if (value < 0 || value >= 4294967296.0 || static_cast<double>(static_cast<uint64_t>(value)) != value)
+                return fail(h, MOE_EINVAL, "the generation word takes an integer in [0, 2^32)");
+            if (!h->ws_mem) return fail(h, MOE_ENOMEM, "no workspace");
+            const uint32_t g = static_cast<uint32_t>(static_cast<uint64_t>(value));
+            cudaError_t e = cudaMemcpy(h->ws.ticket + 3, &g, sizeof(g), cudaMemcpyHostToDevice);
+            if (e != cudaSuccess) return cuda_fail(h, e, "presetting the grid-barrier word");
+            return MOE_OK;
+        }
         case MOE_OPT_LAYER_SLOTS: {
             const int v = static_cast<int>(value);
             if (static_cast<double>(v) != value || v < 1 || v > 4096)

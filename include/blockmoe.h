@@ -100,6 +100,10 @@ typedef void* moe_stream_t;
 #define MOE_OPT_LAYER_SLOTS 10    /* number of layer slots (>= 1, default 1); see moe_bind_layer */
 #define MOE_OPT_LAYER 11          /* read-only: the current layer slot */
 #define MOE_OPT_Y_FORMAT 12       /* MOE_Y_*: GEMM2 rows handed to the combine */
+#define MOE_OPT_DEBUG_GRID_GEN 13 /* test-only, write-only: preset the single-launch kernel's grid-barrier
+                                     generation word to a value in [0, 2^32) (the pages test epoch words
+                                     preset just below 2^31 and 2^32; aiter #6881 commit notes).  The
+                                     barrier compares the word for a change, so it may wrap.  Synchronous. */
 
 /* GEMM2 rows.  BF16: one BF16 row per route (default).  MXFP8: the rows go to
  * the combine as 1x32 E4M3 codes with one E8M0 scale per 32 along H (ROCm/aiter
