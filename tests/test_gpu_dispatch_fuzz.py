@@ -1,0 +1,94 @@
+"""GPU dispatch fuzz against the oracle, bit-exact (the pages' test list: a negative id takes no slot,
+fuzzed over row counts and pad-row fractions).
+
+Each seeded case draws T in [3, 512], a valid-row count from 0 to T, E and top-k, distinct expert ids
+per row, then overwrites a random fraction (0 to 100%) of the slots with negative ids (-1, -2, -1000,
+INT32_MIN) and, in some cases, a few slots with ids >= E. Rows at or past the valid-row count carry
+arbitrary ids, out-of-range ones included. For both dispatch schemes and both execution paths:
+
+* compact: counts, offsets, the stable packed order and the slot -> packed position map equal the
+  oracle's;
+* fixed: counts, the occupancy bitmap and the slot -> e*capacity+t map equal the oracle's;
+* the layer output is within the parity tolerance of the oracle's, pad rows are zero;
+* the status word flags an id >= E exactly when a valid row holds one.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity_util import Case, assert_close, torch_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+NEG = np.array([-1, -2, -1000, np.iinfo(np.int32).min], dtype=np.int64)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a GB300"
+    torch.cuda.set_device(0)
+
+
+def _draw(seed):
+    rng = np.random.default_rng(1000 + seed)
+    T = {0: 3, 1: 512}.get(seed, int(rng.integers(3, 513)))
+    nvr = {2: 0, 3: T, 4: T}.get(seed, int(rng.integers(0, T + 1)))
+    E = int(rng.choice([4, 8, 13, 32]))
+    K = int(rng.integers(1, min(E, 8) + 1))
+    ids = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int64)  # distinct per row
+    neg_frac = [0.0, 0.05, 0.3, 1.0, float(rng.random())][seed % 5]
+    m = rng.random((T, K)) < neg_frac
+    ids[m] = NEG[rng.integers(0, NEG.size, m.sum())]
+    if seed % 3 == 0:  # a few out-of-range ids among the valid rows
+        n = int(rng.integers(1, 4))
+        ids[rng.integers(0, T, n), rng.integers(0, K, n)] = E + rng.integers(0, 5, n)
+    if nvr < T:  # pad rows hold arbitrary ids
+        ids[nvr:] = rng.integers(-3, E + 3, (T - nvr, K))
+    return T, nvr, E, K, ids.astype(np.int32)
+
+
+CASES = list(range(16))
+
+
+@pytest.mark.parametrize("seed", CASES)
+def test_dispatch_fuzz(seed):
+    import block_scaled_moe_gb300 as bm
+    T, nvr, E, K, ids = _draw(seed)
+    w = synth.micro(T, 128, 128, E, K, nvr=nvr, invalid_frac=0.0, capacity=T, seed=seed,
+                    swiglu_limit=10.0 if seed % 2 else 0.0)
+    c = Case(w)
+    c.ids = ids
+    c.idsd.copy_(torch.from_numpy(ids))
+    bad = bool(np.any(ids[:nvr] >= E))
+    ref = oracle.moe_forward(c.x, ids, c.wts, c.Wh, num_valid_rows=nvr, swiglu_limit=w.swiglu_limit)
+    dc = oracle.dispatch_compact(ids, E, nvr)
+    df = oracle.dispatch_fixed(ids, E, T, nvr)
+    paths = ["multi"] + (["fused"] if T <= 512 else [])
+    for scheme in ("compact", "fixed"):
+        for path in paths:
+            tag = f"T={T} nvr={nvr} E={E} K={K} {scheme} {path}"
+            L = c.layer(dispatch=scheme, route_tile=32, path=path, debug=True)
+            got = torch_bf16_bits(c.run(L))
+            torch.cuda.synchronize()
+            assert L.last_path == path, tag
+            st = L.read_status()
+            assert bool(st & bm.MOE_ST_BAD_ID) == bad, (tag, st)
+            assert st & ~bm.MOE_ST_BAD_ID == 0, (tag, st)
+            assert np.all(got[nvr:] == 0), tag
+            assert_close(got, ref, tag)
+            if scheme == "compact":
+                assert np.array_equal(L.debug_array("counts"), dc["counts"]), tag
+                assert np.array_equal(L.debug_array("offsets"), dc["offsets"]), tag
+                R = int(dc["offsets"][-1])
+                assert np.array_equal(L.debug_array("perm")[:R], dc["perm"]), tag
+                assert np.array_equal(L.debug_array("route_row").reshape(T, K), dc["route_row"]), tag
+            else:
+                assert np.array_equal(L.debug_array("counts"), df["counts"]), tag
+                assert np.array_equal(L.debug_array("occ").reshape(E, -1), df["occ"]), tag
+                assert np.array_equal(L.debug_array("route_slot").reshape(T, K), df["route_slot"]), tag
+            del L
