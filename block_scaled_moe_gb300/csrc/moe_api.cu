@@ -610,6 +610,15 @@ int moe_set_option(moe_handle h, int key, double value) {
             if (e != cudaSuccess) return cuda_fail(h, e, "presetting the grid-barrier word");
             return MOE_OK;
         }
+        case MOE_OPT_DEBUG_STALL_GRID: {
+            if (value != 1.0) return fail(h, MOE_EINVAL, "the stall takes the value 1");
+            if (!h->ws_mem) return fail(h, MOE_ENOMEM, "no workspace");
+            // far from the grid size, so that no arrival count ever equals it
+            const uint32_t c = 0x80000000u;
+            cudaError_t e = cudaMemcpy(h->ws.ticket + 2, &c, sizeof(c), cudaMemcpyHostToDevice);
+            if (e != cudaSuccess) return cuda_fail(h, e, "presetting the grid-barrier count");
+            return MOE_OK;
+        }
         case MOE_OPT_LAYER_SLOTS: {
             const int v = static_cast<int>(value);
             if (static_cast<double>(v) != value || v < 1 || v > 4096)

@@ -104,6 +104,13 @@ typedef void* moe_stream_t;
                                      generation word to a value in [0, 2^32) (the pages test epoch words
                                      preset just below 2^31 and 2^32; aiter #6881 commit notes).  The
                                      barrier compares the word for a change, so it may wrap.  Synchronous. */
+#define MOE_OPT_DEBUG_STALL_GRID 14 /* test-only, write-only, fault injection without a fault: 1 presets the
+                                     single-launch kernel's grid-barrier arrival count to 2^31, so that the
+                                     next fused forward's first grid barrier can never complete.  Every CTA
+                                     gives up after its bounded wait (2 s), sets MOE_ST_TIMEOUT with the
+                                     grid-barrier site bit (14) and ends; `out` is not written.  Reading
+                                     that status resets the words and the handle works again.  Other paths
+                                     do not use the word.  Synchronous. */
 
 /* GEMM2 rows.  BF16: one BF16 row per route (default).  MXFP8: the rows go to
  * the combine as 1x32 E4M3 codes with one E8M0 scale per 32 along H (ROCm/aiter

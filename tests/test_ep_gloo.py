@@ -4,10 +4,16 @@ Each rank owns half of the experts and a shard of the tokens.  Dispatch, a local
 rank's own experts (the CPU oracle stands in for the GPU layer), and combine must give, for every
 token, the single-process oracle output within the layer tolerance (the partial rows are rounded to
 BF16 before the owner adds them).  The runtime choice follows the largest token count over the ranks.
+
+Failure detection (host side, no GPU): a rank that leaves between steps, with none of its exchanges in
+flight, makes the other rank's next exchange end with an error within the process group's short
+timeout instead of waiting for ever.
 """
 
+import datetime
 import os
 import socket
+import time
 
 import numpy as np
 import pytest
@@ -100,3 +106,61 @@ def test_plan_routes_each_row_once_per_owner():
     assert torch.allclose(plan.weights, torch.tensor([[0.6, 0], [0.5, 0.5], [0, 1.0], [0, 0.4], [0.9, 0.1]]))
     with pytest.raises(ValueError):
         ep.make_plan(ids, w, E=8, world=3, rank=0)
+
+
+def _leave(result_q):
+    """End this process at once (no process-group teardown), after the queued result is sent."""
+    result_q.close()
+    result_q.join_thread()
+    os._exit(0)
+
+
+def _leaving_worker(rank, world, port, result_q):
+    import torch.distributed as dist
+    try:
+        os.environ["MASTER_ADDR"] = "127.0.0.1"
+        os.environ["MASTER_PORT"] = str(port)
+        dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=5))
+        from block_scaled_moe_gb300 import ep
+
+        w = synth.micro(24, 64, 64, 4, 2, nvr=24, routing="uniform", invalid_frac=0.0, seed=5)
+        x, ids, wts, _ = synth.make_all(w)
+        lo, hi = (0, 12) if rank == 0 else (12, 24)
+        plan = ep.make_plan(torch.from_numpy(ids[lo:hi]), torch.from_numpy(wts[lo:hi]), w.E, world, rank)
+        rcv = ep.dispatch(plan, x[lo:hi])                  # step 1, both ranks
+        ep.combine(plan, rcv, rcv.x, hi - lo)              # any BF16 rows stand in for the layer's
+        if rank == 1:
+            result_q.put((1, "left", 0.0))                 # leaves between steps
+            _leave(result_q)
+        t0 = time.monotonic()
+        try:
+            ep.dispatch(plan, x[lo:hi])                    # step 2: the peer is gone
+            result_q.put((0, "no error", time.monotonic() - t0))
+        except Exception as exc:  # the collective's error is the detection
+            result_q.put((0, type(exc).__name__, time.monotonic() - t0))
+        _leave(result_q)
+    except Exception as exc:  # pragma: no cover - reported to the parent
+        result_q.put((rank, "setup: " + repr(exc), -1.0))
+
+
+def test_rank_leaving_between_steps_is_detected():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_leaving_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = {}
+    try:
+        for _ in range(2):
+            r = q.get(timeout=120)
+            res[r[0]] = r
+    finally:
+        for p in procs:
+            p.join(timeout=30)
+            if p.is_alive():  # only this test's own child processes
+                p.kill()
+                p.join(timeout=10)
+    assert res[1][1] == "left", res
+    assert res[0][1] not in ("no error",) and not res[0][1].startswith("setup"), res
+    assert 0.0 <= res[0][2] < 60.0, res  # ended by the peer's closed connection or the 5 s timeout

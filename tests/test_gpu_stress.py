@@ -7,8 +7,14 @@ past `out`, every route on one expert).
 * two handles on the same weights (fused and multi-kernel path) alternate eager forwards and CUDA
   graph replays over changing T; every output equals the reference of its T bitwise;
 * guard rows after `out` stay untouched on both paths, with num_valid_rows below T;
-* every row routes its first slot to the same expert (one expert holds several route tiles).
+* every row routes its first slot to the same expert (one expert holds several route tiles);
+* failure detection without a fault: a grid barrier that can never complete (its arrival count
+  preset out of reach through the test-only MOE_OPT_DEBUG_STALL_GRID) makes every CTA give up after
+  the bounded wait; the status word reports the timeout and the grid-barrier site, and the next
+  forward, after the status was read, is bitwise the earlier result.
 """
+
+import time
 
 import numpy as np
 import pytest
@@ -131,3 +137,26 @@ def test_every_row_on_one_expert(route_tile):
     torch.cuda.synchronize()
     assert_close(got, c.oracle(), f"NT={route_tile}")
     assert L.read_status() == 0
+
+
+def test_stalled_grid_barrier_times_out_and_recovers():
+    import block_scaled_moe_gb300 as bm
+    c = _case()
+    Lf = c.layer(route_tile=32, path="fused")
+    ref = _fwd(c, Lf, 128)
+    assert Lf.read_status() == 0
+    with pytest.raises(bm.MoeError):
+        bm.moe_set_option(Lf.h, bm.MOE_OPT_DEBUG_STALL_GRID, 2.0)
+    bm.moe_set_option(Lf.h, bm.MOE_OPT_DEBUG_STALL_GRID, 1.0)
+    t0 = time.monotonic()
+    Lf.forward(c.xd, c.idsd, c.wtsd, None)
+    torch.cuda.synchronize()
+    waited = time.monotonic() - t0
+    assert Lf.last_path == "fused"
+    assert 1.5 < waited < 60, waited  # every CTA's wait is bounded at 2 s
+    st = Lf.read_status()
+    assert st & bm.MOE_ST_TIMEOUT, hex(st)
+    assert st & (1 << 14), hex(st)  # site: the fused path's grid barrier
+    for _ in range(2):  # reading the timeout reset the barrier words
+        assert np.array_equal(_fwd(c, Lf, 128), ref)
+    assert Lf.read_status() == 0
