@@ -16,7 +16,9 @@ import threading
 from typing import Optional
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "lib", "libblockmoe.so")
+# BMOE_LIB_VARIANT=bounds loads the bounds-checking build (libblockmoe_bounds.so) instead
+LIB_VARIANT = os.environ.get("BMOE_LIB_VARIANT", "")
+LIB_PATH = os.path.join(PKG, "lib", f"libblockmoe_{LIB_VARIANT}.so" if LIB_VARIANT else "libblockmoe.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "blockmoe.h")
 
 _lock = threading.Lock()
@@ -49,7 +51,8 @@ def load(path: Optional[str] = None):
             return _lib
         p = path or LIB_PATH
         if not os.path.exists(p):
-            raise ImportError(f"libblockmoe.so is not built ({p}); run __graft_entry__.build()")
+            raise ImportError(f"{os.path.basename(p)} is not built ({p}); run __graft_entry__.build()"
+                              + (f" or _build.build(variant={LIB_VARIANT!r})" if LIB_VARIANT else ""))
         lib = ctypes.CDLL(p)
         vp, i32, f64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_size_t
         lib.moe_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32]
@@ -449,7 +452,7 @@ class BlockScaledMoE:
                "xq": (MOE_DBG_XQ, np.uint8), "xs": (MOE_DBG_XS, np.uint8), "yrow": (MOE_DBG_YROW, np.int32),
                "hq": (MOE_DBG_HQ, np.uint8), "g": (MOE_DBG_G, np.float32), "y": (MOE_DBG_Y, np.uint16),
                "tiles": (MOE_DBG_TILES, np.int32), "topk_ids": (MOE_DBG_TOPK_IDS, np.int32),
-               "topk_weights": (MOE_DBG_TOPK_WEIGHTS, np.float32)}
+               "topk_weights": (MOE_DBG_TOPK_WEIGHTS, np.float32), "bounds": (MOE_DBG_BOUNDS, np.uint32)}
         code, dt = ids[which]
         raw = moe_debug_copy(self.h, code, torch.cuda.current_stream().cuda_stream)
         return np.frombuffer(raw, dtype=dt).copy()

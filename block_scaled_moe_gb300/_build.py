@@ -1,4 +1,8 @@
-"""Build of libblockmoe.so: nvcc for sm_103a, translation units compiled in parallel."""
+"""Build of libblockmoe.so: nvcc for sm_103a, translation units compiled in parallel.
+
+Variant "bounds" builds libblockmoe_bounds.so with -DMOE_DEBUG_BOUNDS: every index the kernels compute
+into the workspace or an output row is checked, a miss is recorded in the status word and skipped.
+The binding loads it when BMOE_LIB_VARIANT=bounds is set."""
 
 from __future__ import annotations
 
@@ -12,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
-LIB = os.path.join(PKG, "lib", "libblockmoe.so")
+VARIANTS = {"": [], "bounds": ["-DMOE_DEBUG_BOUNDS"]}
 SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_gemm.cu", "moe_fused.cu", "moe_noalloc.cu", "moe_route.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC,-Wall", "-I", INCLUDE, "-I", CSRC,
@@ -31,16 +35,24 @@ def _deps():
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def lib_path(variant: str = "") -> str:
+    return os.path.join(PKG, "lib", f"libblockmoe_{variant}.so" if variant else "libblockmoe.so")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), variant: str = "") -> str:
+    if variant not in VARIANTS:
+        raise ValueError(f"unknown build variant {variant!r}; known: {sorted(VARIANTS)}")
+    LIB = lib_path(variant)
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps() and not extra_flags:
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    bdir = os.path.join(BUILD, variant) if variant else BUILD
+    os.makedirs(bdir, exist_ok=True)
     os.makedirs(os.path.dirname(LIB), exist_ok=True)
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [cc, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(bdir, os.path.splitext(src)[0] + ".o")
+        cmd = [cc, *FLAGS, *VARIANTS[variant], *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

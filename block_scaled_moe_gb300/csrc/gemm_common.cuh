@@ -58,6 +58,25 @@ __device__ __forceinline__ UnitInfo decode_unit(int u, int& ecur, const Plan& pl
     return r;
 }
 
+#ifdef MOE_DEBUG_BOUNDS
+// Bounds-checking builds: how many of the CTA's n units (unit i from decode(i)) lie inside the
+// workspace regions, i.e. a route tile below lim_tiles and rows [row0, row0 + n) below lim_rows with
+// 1 <= n <= NT, counted up to the first that does not; the CTA's roles all end their unit lists
+// there, so they stay in step.
+template <typename Decode>
+__device__ __forceinline__ int units_in_bounds(int n, Decode&& decode, int NT, int lim_rows, int lim_tiles,
+                                               uint32_t* status, uint32_t* ticket) {
+    for (int i = 0; i < n; ++i) {
+        const UnitInfo cu = decode(i);
+        if (!(bounds_ok(status, ticket, cu.g, lim_tiles, kBsUnit) && bounds_ok(status, ticket, cu.n - 1, NT, kBsUnit) &&
+              bounds_ok(status, ticket, cu.row0, lim_rows, kBsUnit) &&
+              bounds_ok(status, ticket, static_cast<long long>(cu.row0) + cu.n - 1, lim_rows, kBsUnit)))
+            return i;
+    }
+    return n;
+}
+#endif
+
 // The loads of the last STAGES jobs this producer issued land before the CTA
 // exits (they are consumed already unless another role gave up).  Bounded.
 template <int STAGES>

@@ -55,10 +55,14 @@ __device__ __forceinline__ void quant_scatter_seg(const QuantArgs& a, const int3
     const int K = a.K;
     int p = -1, gt = 0, c = 0;
     bool valid = false;
+    BMOE_BOUNDS_ONLY(const Workspace& ws = a.ws;)
     if (lane < K) {
         const int e = a.ids[(size_t)t * K + lane];
         if (t < nvr && e >= a.E) atomicOr(a.ws.status, kStBadId);
         valid = t < nvr && e >= 0 && e < a.E;
+        BMOE_BOUNDS_ONLY(
+            const bool slot_ok = bounds_ok(ws.status, ws.ticket, (long long)t * K + lane, ws.lim_slots, kBsSlot);
+            if (valid && !(a.scheme == 1 ? bounds_ok(ws.status, ws.ticket, t, a.mtpr, kBsOcc) : slot_ok)) valid = false;)
         if (valid) {
             int i;
             if (a.scheme == 1) {
@@ -74,7 +78,7 @@ __device__ __forceinline__ void quant_scatter_seg(const QuantArgs& a, const int3
             gt = tile_base[e] + i / a.NT;
             c = i % a.NT;
         }
-        if (seg == 0) a.ws.yrow[(size_t)t * K + lane] = valid ? p : -1;
+        if (seg == 0 BMOE_BOUNDS_ONLY(&& slot_ok)) a.ws.yrow[(size_t)t * K + lane] = valid ? p : -1;
     }
     if (t >= nvr) return;  // warp-uniform
     const unsigned vmask = __ballot_sync(kFull, valid);
@@ -123,7 +127,9 @@ __device__ __forceinline__ void quant_scatter_seg(const QuantArgs& a, const int3
     for (int k = 0; k < K; ++k) {
         if (!((vmask >> k) & 1u)) continue;  // warp-uniform
         const int pk = __shfl_sync(kFull, p, k), gk = __shfl_sync(kFull, gt, k), ci = __shfl_sync(kFull, c, k);
-        if (has) {
+        if (has BMOE_BOUNDS_ONLY(&& bounds_ok(ws.status, ws.ticket, pk, ws.lim_rows, kBsRow) &&
+                                 bounds_ok(ws.status, ws.ticket, gk, ws.lim_tiles, kBsAtom) &&
+                                 bounds_ok(ws.status, ws.ticket, ci, a.nb * 128, kBsAtom))) {
             uint4* d = reinterpret_cast<uint4*>(a.ws.aq + (size_t)pk * H + blk * 32);
             d[0] = o0;
             d[1] = o1;
@@ -149,7 +155,25 @@ struct CombineArgs {
     int T, K, H;
     const uint8_t* y8;  // non-null: GEMM2 rows are MXFP8 codes [rows][H] ...
     const uint8_t* ys;  // ... with E8M0 scales [rows][H/32]
+#ifdef MOE_DEBUG_BOUNDS
+    uint32_t* status;   // workspace status and ticket words (bounds-miss record)
+    uint32_t* ticket;
+    int lim_rows, lim_slots;  // packed rows of y, entries of yrow
+#endif
 };
+
+#ifdef MOE_DEBUG_BOUNDS
+// The packed row slot k of token t combines (-1: none), where a row outside y or a slot outside yrow
+// counts as none.
+__device__ __forceinline__ int combine_row(const CombineArgs& a, int t, int k) {
+    if (!bounds_ok(a.status, a.ticket, (long long)t * a.K + k, a.lim_slots, kBsSlot)) return -1;
+    const int r = __ldcg(a.yrow + (size_t)t * a.K + k);
+    return (r < 0 || bounds_ok(a.status, a.ticket, r, a.lim_rows, kBsYRow)) ? r : -1;
+}
+#define BMOE_COMBINE_ROW(a, t, k) combine_row(a, t, k)
+#else
+#define BMOE_COMBINE_ROW(a, t, k) __ldcg(a.yrow + (size_t)t * a.K + k)
+#endif
 
 // One MXFP8 1x32 block held by a warp, one element per lane (OCP MX rule as for
 // the input rows): returns the lane's E4M3 code; *scale receives the E8M0 code.
@@ -177,7 +201,7 @@ __device__ __forceinline__ void combine_item_bf16(const CombineArgs& a, int item
     int r_l = -1;
     float w_l = 0.f;
     if (lane < a.K) {
-        r_l = __ldcg(a.yrow + (size_t)t * a.K + lane);
+        r_l = BMOE_COMBINE_ROW(a, t, lane);
         w_l = a.w[(size_t)t * a.K + lane];
     }
     int rows[kMaxTopk];
@@ -229,7 +253,7 @@ __device__ __forceinline__ void combine_item_fp8(const CombineArgs& a, int item,
     int r_l = -1;
     float w_l = 0.f;
     if (lane < a.K) {
-        r_l = __ldcg(a.yrow + (size_t)t * a.K + lane);
+        r_l = BMOE_COMBINE_ROW(a, t, lane);
         w_l = a.w[(size_t)t * a.K + lane];
     }
     const int v1 = min(a.H >> 3, (seg + 1) * kCombineVecs);

@@ -218,7 +218,7 @@ int adopt_workspace(moe_ctx* h, void* mem, size_t bytes, bool owned) {
     Workspace w{};
     const size_t need = bmoe::workspace_layout(h->geo, static_cast<char*>(mem), &w);
     if (bytes < need) return fail(h, MOE_ENOMEM, "workspace holds %zu bytes, %zu needed", bytes, need);
-    cudaError_t e = cudaMemset(w.ticket, 0, 4 * sizeof(uint32_t));
+    cudaError_t e = cudaMemset(w.ticket, 0, 8 * sizeof(uint32_t));
     if (e == cudaSuccess) e = cudaMemset(w.status, 0, 4 * sizeof(uint32_t));
     if (e != cudaSuccess) return cuda_fail(h, e, "clearing workspace counters");
     release_workspace(h);
@@ -505,6 +505,11 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     a.E = g.E;
     a.swiglu_limit = static_cast<float>(h->swiglu_limit);
     a.status = ws.status;
+#ifdef MOE_DEBUG_BOUNDS
+    a.ticket = ws.ticket;
+    a.lim_rows = ws.lim_rows;
+    a.lim_tiles = ws.lim_tiles;
+#endif
     a.y8 = y8;
     a.ys = ys;
     a.trace = nullptr;
@@ -619,6 +624,17 @@ int moe_set_option(moe_handle h, int key, double value) {
             if (e != cudaSuccess) return cuda_fail(h, e, "presetting the grid-barrier count");
             return MOE_OK;
         }
+        case MOE_OPT_DEBUG_BOUNDS_ROWS: {
+#ifdef MOE_DEBUG_BOUNDS
+            const long long v = static_cast<long long>(value);
+            if (static_cast<double>(v) != value || v < 1 || v > h->geo.rows_cap)
+                return fail(h, MOE_EINVAL, "the row limit takes an integer in [1, %lld]", h->geo.rows_cap);
+            h->ws.lim_rows = static_cast<int>(v);
+            return MOE_OK;
+#else
+            return fail(h, MOE_ESTATE, "not a bounds-checking build (libblockmoe_bounds.so)");
+#endif
+        }
         case MOE_OPT_LAYER_SLOTS: {
             const int v = static_cast<int>(value);
             if (static_cast<double>(v) != value || v < 1 || v > 4096)
@@ -697,6 +713,11 @@ int moe_get_option(moe_handle h, int key, double* value) {
         case MOE_OPT_Y_FORMAT: *value = h->y_format; return MOE_OK;
         case MOE_OPT_LAYER_SLOTS: *value = static_cast<double>(h->slots.size()); return MOE_OK;
         case MOE_OPT_LAYER: *value = h->cur; return MOE_OK;
+#ifdef MOE_DEBUG_BOUNDS
+        case MOE_OPT_BOUNDS_BUILD: *value = 1; return MOE_OK;
+#else
+        case MOE_OPT_BOUNDS_BUILD: *value = 0; return MOE_OK;
+#endif
         default: return fail(h, MOE_EINVAL, "unknown option %d", key);
     }
 }
@@ -725,6 +746,8 @@ int moe_read_status(moe_handle h, uint32_t* flags, moe_stream_t stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     // a timed-out fused launch may leave its grid-barrier words mid-count
     if (e == cudaSuccess && (v & MOE_ST_TIMEOUT)) e = cudaMemset(h->ws.ticket + 2, 0, 2 * sizeof(uint32_t));
+    // the first-miss record goes with its status bit
+    if (e == cudaSuccess && (v & MOE_ST_BOUNDS)) e = cudaMemset(h->ws.ticket + 5, 0, 2 * sizeof(uint32_t));
     if (e != cudaSuccess) return cuda_fail(h, e, "reading the status word");
     *flags = v;
     return MOE_OK;
@@ -825,6 +848,7 @@ int moe_debug_copy(moe_handle h, int which, void* host_dst, size_t* bytes, moe_s
         case MOE_DBG_Y: src = w.y; n = (size_t)g.rows_cap * g.H * 2; break;
         case MOE_DBG_TOPK_IDS: src = w.rids; n = sizeof(int32_t) * (size_t)h->last_T * g.K; break;
         case MOE_DBG_TOPK_WEIGHTS: src = w.rw; n = sizeof(float) * (size_t)h->last_T * g.K; break;
+        case MOE_DBG_BOUNDS: src = w.ticket + 5; n = 2 * sizeof(uint32_t); break;
         case MOE_DBG_TILES: {
             std::vector<int32_t> cnt(g.E), rb(g.E + 1), tb(g.E + 1);
             cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -441,7 +441,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         for (int s = gtid; s < T * K; s += gstride) {
             const int t = s / K, e = q.ids[s];
             if (t < nvr && e >= E) atomicOr(ws.status, kStBadId);
-            if (t < nvr && e >= 0 && e < E) {
+            BMOE_BOUNDS_ONLY(if (!bounds_ok(ws.status, ws.ticket, s, ws.lim_slots, kBsSlot)) continue;)
+            if (t < nvr && e >= 0 && e < E BMOE_BOUNDS_ONLY(&& bounds_ok(ws.status, ws.ticket, t, q.mtpr, kBsOcc))) {
                 atomicOr(&ws.occ[(size_t)e * q.words + (t >> 5)], 1u << (t & 31));
                 ws.route_slot[s] = e * q.mtpr + t;
             } else {
@@ -463,6 +464,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     } else {
         // compact (vLLM PR #61262): per-chunk histograms, scan, stable pack
         int* cnt = scr;
+        // every CTA takes the same branch
+        BMOE_BOUNDS_ONLY(if (!bounds_ok(ws.status, ws.ticket, f.nchunks, ws.lim_chunks + 1, kBsChunk)) goto finish;)
         for (int c = blockIdx.x; c < f.nchunks; c += gridDim.x) {
             for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
             __syncthreads();
@@ -510,9 +513,11 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                     const unsigned peers = __match_any_sync(0xffffffffu, key);
                     if (valid) {
                         const int p = run[e] + __popc(peers & lt);
+                        BMOE_BOUNDS_ONLY(if (bounds_ok(ws.status, ws.ticket, s, ws.lim_slots, kBsSlot)))
                         ws.route_row[s] = p;
+                        BMOE_BOUNDS_ONLY(if (bounds_ok(ws.status, ws.ticket, p, ws.lim_slots, kBsPerm)))
                         ws.perm[p] = s;
-                    } else if (in) {
+                    } else if (in BMOE_BOUNDS_ONLY(&& bounds_ok(ws.status, ws.ticket, s, ws.lim_slots, kBsSlot))) {
                         ws.route_row[s] = -1;
                     }
                     __syncwarp();
@@ -547,11 +552,21 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         const int ntiles = t_tile[E];
         const int mt1 = I / 128, mt2 = H / 128;
         const int U1 = ntiles * mt1, U = U1 + ntiles * mt2;
-        const int my_units = static_cast<int>(blockIdx.x) < U
-                                 ? (U - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                                 : 0;
+#ifdef MOE_DEBUG_BOUNDS
+        const int all_units =
+#else
+        const int my_units =
+#endif
+            static_cast<int>(blockIdx.x) < U ? (U - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                                             : 0;
         const int kt1 = H / 128, kt2 = I / (128 * f.kc2), ktot2 = I / 128;
         const Plan pl{t_tile, t_row, t_cnt};
+#ifdef MOE_DEBUG_BOUNDS
+        FCursor chk_cur;
+        const int my_units = units_in_bounds(
+            all_units, [&](int i) { return fused_unit(blockIdx.x + i * gridDim.x, U1, chk_cur, pl, mt1, mt2).u; },
+            F_NT, ws.lim_rows, ws.lim_tiles, ws.status, ws.ticket);
+#endif
         if (threadIdx.x == 0) {
             for (int s = 0; s < F_STAGES; ++s) {
                 mbar_init(&full[s], 1 + 32);  // the producer's arrive.expect_tx + the scale warp's lanes
@@ -864,6 +879,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         ca.H = H;
         ca.y8 = f.y8;
         ca.ys = f.ys;
+        BMOE_BOUNDS_ONLY(ca.status = ws.status; ca.ticket = ws.ticket; ca.lim_rows = ws.lim_rows;
+                         ca.lim_slots = ws.lim_slots;)
         const int items = rows::combine_items(ca);
         for (int it = blockIdx.x * (blockDim.x >> 5) + warp; it < items; it += gridDim.x * (blockDim.x >> 5))
             rows::combine_item(ca, it, lane);

@@ -172,7 +172,12 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
     const int ntiles = __ldg(a.tile_base + a.E);
     const int n_units = ntiles * a.mtiles;
     if (static_cast<int>(blockIdx.x) >= n_units) return;  // whole CTA
-    const int my_units = (n_units - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1;
+#ifdef MOE_DEBUG_BOUNDS
+    const int all_units =
+#else
+    const int my_units =
+#endif
+        (n_units - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1;
     const int KT = a.ktiles / KC;  // K stages per unit
 
     Plan pl{a.tile_base, a.rowbase, a.counts};
@@ -205,6 +210,13 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+#ifdef MOE_DEBUG_BOUNDS
+    int chk_ecur = 0;
+    const int my_units = units_in_bounds(
+        all_units,
+        [&](int i) { return decode_unit(blockIdx.x + i * gridDim.x, chk_ecur, pl, a.mtiles, NT); }, NT, a.lim_rows,
+        a.lim_tiles, a.status, a.ticket);
+#endif
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (one warp, one elected lane issues)

@@ -13,7 +13,7 @@ constexpr int kChunk = 512;            // flat slots per compact-dispatch chunk
 constexpr int kMaxTopk = 16;
 constexpr int kMaxExperts = 4096;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per device-side wait
-constexpr uint32_t kStBadId = 0x1u, kStTimeout = 0x2u, kStOverflow = 0x4u;
+constexpr uint32_t kStBadId = 0x1u, kStTimeout = 0x2u, kStOverflow = 0x4u, kStBounds = 0x8u;
 // Wait sites recorded next to kStTimeout (bit 8 + site): 0 producer/empty,
 // 1 producer drain, 2 MMA/accumulator-free, 3 MMA/stage-full, 4 MMA drain,
 // 5 epilogue/accumulator-full.
@@ -32,7 +32,8 @@ struct Workspace {
     int32_t* yrow;         // [cap*K] packed row of the GEMM2 output each slot combines (-1 invalid)
     uint32_t* occ;         // [E*words] fixed-slot occupancy bits
     int32_t* chunk_base;   // [nchunks*E] compact per-chunk counts, then per-chunk base rows
-    uint32_t* ticket;      // [4] self-resetting last-block counters
+    uint32_t* ticket;      // [8] last-block counters (0, 1), fused grid-barrier count and generation (2, 3),
+                           //     first bounds miss: site and index (5, 6; bounds-checking builds)
     uint32_t* status;      // [1] MOE_ST_* bits
     uint8_t* aq;           // [rows_cap][H] packed E4M3 codes of the dispatched rows
     uint8_t* as;           // [tiles_cap][H/128][512] scale atoms of aq, per route tile
@@ -45,7 +46,42 @@ struct Workspace {
     uint32_t* ready;       // [tiles_cap] fused path: GEMM1 units finished per route tile
     int32_t* rids;         // [cap*K] router top-k ids (moe_forward_routed)
     float* rw;             // [cap*K] router top-k weights (moe_forward_routed)
+#ifdef MOE_DEBUG_BOUNDS
+    // region sizes, checked by the bounds-checking build
+    int lim_rows;          // packed rows of aq / hq / y
+    int lim_tiles;         // route tiles of as / hs / ready
+    int lim_slots;         // cap*K entries of perm / route_row / route_slot / yrow
+    int lim_chunks;        // compact-dispatch chunks of chunk_base
+#endif
 };
+
+// Bounds-checking build (-DMOE_DEBUG_BOUNDS, a second library next to the normal one): every index
+// a kernel computes into a workspace region or an output row is checked before use.  A miss sets
+// kStBounds, records the first miss (site, low 32 bits of the index) in ticket words 5 and 6, and
+// the access is skipped, so nothing outside the regions is touched.  The checks, the limits they
+// use and their arguments exist only in that build (BMOE_BOUNDS_ONLY): other builds compile the
+// unchecked code, token for token.
+enum BoundsSite : int {
+    kBsOcc = 1,      // occupancy word of (expert, token)
+    kBsSlot = 2,     // flat top-k slot of a per-slot array
+    kBsPerm = 3,     // packed position of a route
+    kBsChunk = 4,    // compact-dispatch chunk
+    kBsRow = 5,      // packed row written by the quantise-and-scatter step
+    kBsAtom = 6,     // route tile / row of a scale atom written by that step
+    kBsYRow = 7,     // packed row read by the combine
+    kBsUnit = 8,     // GEMM unit: route tile, first row, row count
+};
+#ifdef MOE_DEBUG_BOUNDS
+#define BMOE_BOUNDS_ONLY(...) __VA_ARGS__
+__device__ __forceinline__ bool bounds_ok(uint32_t* status, uint32_t* ticket, long long i, long long n, int site) {
+    if (i >= 0 && i < n) return true;
+    atomicOr(status, kStBounds);
+    if (atomicCAS(ticket + 5, 0u, static_cast<uint32_t>(site)) == 0u) ticket[6] = static_cast<uint32_t>(i);
+    return false;
+}
+#else
+#define BMOE_BOUNDS_ONLY(...)
+#endif
 
 struct Geometry {
     int H, I, E, K, cap;
@@ -99,6 +135,10 @@ struct GemmArgs {
     uint16_t* y;  int H;                    // GEMM2
     float swiglu_limit;
     uint32_t* status;
+#ifdef MOE_DEBUG_BOUNDS
+    uint32_t* ticket;      // workspace ticket words (bounds-miss record)
+    int lim_rows, lim_tiles;  // packed rows of hq / y, route tiles of b_sf / hs
+#endif
     long long* trace;      // pipeline trace buffer (tracing builds only), else null
 };
 

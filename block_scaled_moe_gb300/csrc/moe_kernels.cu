@@ -84,7 +84,9 @@ __global__ void __launch_bounds__(256) k_fixed_mark(DispatchArgs a) {
     if (s < a.T * a.K) {
         const int t = s / a.K, e = a.ids[s];
         if (t < nvr && e >= a.E) atomicOr(a.ws.status, kStBadId);
-        if (t < nvr && e >= 0 && e < a.E) {
+        BMOE_BOUNDS_ONLY(const Workspace& ws = a.ws; if (!bounds_ok(ws.status, ws.ticket, s, ws.lim_slots, kBsSlot)) {
+        } else)
+        if (t < nvr && e >= 0 && e < a.E BMOE_BOUNDS_ONLY(&& bounds_ok(ws.status, ws.ticket, t, a.mtpr, kBsOcc))) {
             atomicOr(&a.ws.occ[(size_t)e * a.words + (t >> 5)], 1u << (t & 31));
             a.ws.route_slot[s] = e * a.mtpr + t;
         } else {
@@ -127,6 +129,7 @@ __global__ void __launch_bounds__(512) k_compact_count(DispatchArgs a) {
         if (t < nvr && e >= 0 && e < E) atomicAdd(&cnt[e], 1);
     }
     __syncthreads();
+    BMOE_BOUNDS_ONLY(if (!bounds_ok(a.ws.status, a.ws.ticket, a.nchunks, a.ws.lim_chunks + 1, kBsChunk)) return;)
     for (int e = threadIdx.x; e < E; e += blockDim.x) a.ws.chunk_base[(size_t)blockIdx.x * E + e] = cnt[e];
     if (!last_block(&a.ws.ticket[1], &is_last)) return;
     int* offs = sm + E;
@@ -161,6 +164,8 @@ __global__ void __launch_bounds__(32) k_compact_rank(DispatchArgs a) {
     extern __shared__ int run[];  // [E]
     const int lane = threadIdx.x;
     const int E = a.E;
+    BMOE_BOUNDS_ONLY(const Workspace& ws = a.ws;
+                     if (!bounds_ok(ws.status, ws.ticket, a.nchunks, ws.lim_chunks + 1, kBsChunk)) return;)
     for (int e = lane; e < E; e += 32) run[e] = a.ws.chunk_base[(size_t)blockIdx.x * E + e];
     __syncwarp();
     const int nvr = read_nvr(a.nvr, a.T);
@@ -174,9 +179,11 @@ __global__ void __launch_bounds__(32) k_compact_rank(DispatchArgs a) {
         const unsigned peers = __match_any_sync(kFull, key);
         if (valid) {
             const int p = run[e] + __popc(peers & lt);
+            BMOE_BOUNDS_ONLY(if (bounds_ok(ws.status, ws.ticket, s, ws.lim_slots, kBsSlot)))
             a.ws.route_row[s] = p;
+            BMOE_BOUNDS_ONLY(if (bounds_ok(ws.status, ws.ticket, p, ws.lim_slots, kBsPerm)))
             a.ws.perm[p] = s;
-        } else if (in) {
+        } else if (in BMOE_BOUNDS_ONLY(&& bounds_ok(ws.status, ws.ticket, s, ws.lim_slots, kBsSlot))) {
             a.ws.route_row[s] = -1;
         }
         __syncwarp();
@@ -244,7 +251,7 @@ size_t workspace_layout(const Geometry& g, char* base, Workspace* ws) {
     w.yrow = reinterpret_cast<int32_t*>(carve(sizeof(int32_t) * slots));
     w.occ = reinterpret_cast<uint32_t*>(carve(sizeof(uint32_t) * (size_t)g.E * g.words));
     w.chunk_base = reinterpret_cast<int32_t*>(carve(sizeof(int32_t) * (size_t)g.nchunks_cap * g.E));
-    w.ticket = reinterpret_cast<uint32_t*>(carve(sizeof(uint32_t) * 4));
+    w.ticket = reinterpret_cast<uint32_t*>(carve(sizeof(uint32_t) * 8));
     w.status = reinterpret_cast<uint32_t*>(carve(sizeof(uint32_t) * 4));
     w.aq = reinterpret_cast<uint8_t*>(carve((size_t)g.rows_cap * g.H));
     w.as = reinterpret_cast<uint8_t*>(carve((size_t)g.tiles_cap * (g.H / 128) * g.nb * 512));
@@ -259,6 +266,12 @@ size_t workspace_layout(const Geometry& g, char* base, Workspace* ws) {
         w.xs = reinterpret_cast<uint8_t*>(carve((size_t)g.cap * (g.H / 32)));
         w.g = reinterpret_cast<float*>(carve((size_t)g.rows_cap * 2 * g.I * sizeof(float)));
     }
+#ifdef MOE_DEBUG_BOUNDS
+    w.lim_rows = static_cast<int>(g.rows_cap);
+    w.lim_tiles = static_cast<int>(g.tiles_cap);
+    w.lim_slots = static_cast<int>(slots);
+    w.lim_chunks = g.nchunks_cap;
+#endif
     off = (off + 255) & ~size_t(255);
     if (ws) *ws = w;
     return off;
@@ -314,6 +327,7 @@ cudaError_t launch_combine(const Geometry& g, const Workspace& ws, const float* 
     a.H = g.H;
     a.y8 = y8;
     a.ys = ys;
+    BMOE_BOUNDS_ONLY(a.status = ws.status; a.ticket = ws.ticket; a.lim_rows = ws.lim_rows; a.lim_slots = ws.lim_slots;)
     const int items = T * ((g.H / 8 + rows::kCombineVecs - 1) / rows::kCombineVecs);
     if (y8)
         k_combine<true><<<(items + 7) / 8, 256, 0, s>>>(a);

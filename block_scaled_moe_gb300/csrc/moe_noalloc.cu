@@ -23,7 +23,7 @@ namespace {
 // words.  Every GPU that loads the library holds this array until the process
 // exits.  All calls share it, so calls that overlap on the GPU race.
 constexpr size_t kScratchBytes = size_t(1) << 20;  // 1 MiB
-constexpr size_t kScratchHeader = 256;             // ticket[4] and status[4] words, padded
+constexpr size_t kScratchHeader = 256;             // ticket[8] and status[4] words, padded
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -102,8 +102,8 @@ int moe_dispatch_compact_noalloc(const int32_t* topk_ids, int T, int topk, int E
     g.cap = T;
     g.NT = 128;
     bmoe::Workspace w{};
-    w.ticket = reinterpret_cast<uint32_t*>(sc);
-    w.status = reinterpret_cast<uint32_t*>(sc + 16);
+    w.ticket = reinterpret_cast<uint32_t*>(sc);       // 8 words
+    w.status = reinterpret_cast<uint32_t*>(sc + 32);
     w.chunk_base = reinterpret_cast<int32_t*>(sc + kScratchHeader);
     const size_t nchunks = (static_cast<size_t>(T) * topk + bmoe::kChunk - 1) / bmoe::kChunk;
     w.tile_base = w.chunk_base + nchunks * E;
@@ -111,6 +111,10 @@ int moe_dispatch_compact_noalloc(const int32_t* topk_ids, int T, int topk, int E
     w.rowbase = offsets;
     w.perm = perm;
     w.route_row = route_row;
+#ifdef MOE_DEBUG_BOUNDS
+    w.lim_slots = T * topk;  // the caller's perm and route_row
+    w.lim_chunks = static_cast<int>(nchunks);
+#endif
     e = bmoe::launch_compact_dispatch(g, w, topk_ids, T, num_valid_rows, s);
     if (e != cudaSuccess) {
         char buf[256];

@@ -62,6 +62,8 @@ typedef void* moe_stream_t;
 #define MOE_ST_BAD_ID 0x1u      /* a top-k id >= E was seen (skipped like -1) */
 #define MOE_ST_TIMEOUT 0x2u     /* a bounded device-side wait gave up */
 #define MOE_ST_OVERFLOW 0x4u    /* internal tile list overflow (bug guard) */
+#define MOE_ST_BOUNDS 0x8u      /* bounds-checking build: a kernel computed an index outside its region
+                                   (the access was skipped; MOE_DBG_BOUNDS holds the first one) */
 /* With MOE_ST_TIMEOUT, bits 8..15 name the wait that gave up (diagnostic):
  * 8 producer/stage-free, 9 producer drain, 10 MMA/accumulator-free,
  * 11 MMA/stage-full, 12 MMA drain, 13 epilogue/accumulator-full,
@@ -111,6 +113,13 @@ typedef void* moe_stream_t;
                                      grid-barrier site bit (14) and ends; `out` is not written.  Reading
                                      that status resets the words and the handle works again.  Other paths
                                      do not use the word.  Synchronous. */
+#define MOE_OPT_DEBUG_BOUNDS_ROWS 15 /* test-only, write-only, bounds-checking builds only (MOE_ESTATE
+                                     otherwise): the packed-row count the kernels check row indices
+                                     against, 1 .. the workspace's rows (default).  A smaller value
+                                     makes legitimate rows count as misses, which the kernels skip and
+                                     record: it shows that the checks run.  Results are then wrong. */
+#define MOE_OPT_BOUNDS_BUILD 16   /* read-only: 1 in the bounds-checking build (-DMOE_DEBUG_BOUNDS,
+                                     libblockmoe_bounds.so), else 0 */
 
 /* GEMM2 rows.  BF16: one BF16 row per route (default).  MXFP8: the rows go to
  * the combine as 1x32 E4M3 codes with one E8M0 scale per 32 along H (ROCm/aiter
@@ -339,6 +348,10 @@ int moe_dispatch_compact_noalloc(const int32_t* topk_ids, int T, int topk, int E
 #define MOE_DBG_TILES 13        /* int32 [1 + 3*tiles]: tile count, then (expert, row0, n) per tile */
 #define MOE_DBG_TOPK_IDS 14     /* int32 [T][topk]: router ids of the last moe_forward_routed */
 #define MOE_DBG_TOPK_WEIGHTS 15 /* float [T][topk]: router weights of the last moe_forward_routed */
+#define MOE_DBG_BOUNDS 16       /* uint32 [2]: site (1 occupancy word, 2 top-k slot, 3 packed position,
+                                   4 dispatch chunk, 5 scattered row, 6 scale atom, 7 combined row,
+                                   8 GEMM unit) and low 32 bits of the index of the first bounds miss;
+                                   zeros if none.  moe_read_status clears it with MOE_ST_BOUNDS. */
 int moe_debug_copy(moe_handle h, int which, void* host_dst, size_t* bytes, moe_stream_t stream);
 
 #ifdef __cplusplus
