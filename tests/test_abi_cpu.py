@@ -80,3 +80,17 @@ def test_topk_softmax_refuses_bad_arguments_before_cuda(lib, dtype, T, E, K):
 def test_topk_softmax_empty_batch_is_a_no_op(lib):
     import block_scaled_moe_gb300 as bm
     assert lib.moe_topk_softmax(None, bm.MOE_DTYPE_BF16, 0, 384, 6, None, 1, None, None, None) == bm.MOE_OK
+
+
+def test_bounds_checking_build_builds_and_exports_everything():
+    """libblockmoe_bounds.so (-DMOE_DEBUG_BOUNDS) compiles and exports the same functions; an
+    unknown build variant is refused."""
+    from block_scaled_moe_gb300 import _build
+    path = _build.build(variant="bounds")
+    assert path.endswith("libblockmoe_bounds.so")
+    blib = ctypes.CDLL(path)
+    for n in bm.exported_symbols_from_header():
+        assert hasattr(blib, n), n
+    with pytest.raises(ValueError):
+        _build.build(variant="asan")
+    assert bm.MOE_ST_BOUNDS == 8 and bm.MOE_DBG_BOUNDS == 16 and bm.MOE_OPT_BOUNDS_BUILD == 16
