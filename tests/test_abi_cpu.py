@@ -94,3 +94,20 @@ def test_bounds_checking_build_builds_and_exports_everything():
     with pytest.raises(ValueError):
         _build.build(variant="asan")
     assert bm.MOE_ST_BOUNDS == 8 and bm.MOE_DBG_BOUNDS == 16 and bm.MOE_OPT_BOUNDS_BUILD == 16
+
+
+def test_variant_switch_loads_the_bounds_library():
+    """BMOE_LIB_VARIANT=bounds makes the binding load libblockmoe_bounds.so (checked in a child
+    process, since the parent already holds the normal library)."""
+    import os
+    import subprocess
+    import sys
+    from block_scaled_moe_gb300 import _build
+    _build.build(variant="bounds")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import block_scaled_moe_gb300 as bm, os; lib = bm.load(); "
+            "print(os.path.basename(lib._name))")
+    env = dict(os.environ, BMOE_LIB_VARIANT="bounds")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == "libblockmoe_bounds.so"
