@@ -111,3 +111,17 @@ def test_variant_switch_loads_the_bounds_library():
     r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == "libblockmoe_bounds.so"
+
+
+def test_every_option_and_debug_region_is_handled():
+    """Each MOE_OPT_* key and MOE_DBG_* region the header defines has a case in the library's option
+    and debug-copy switches (the header and the implementation do not drift apart)."""
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = open(os.path.join(root, "block_scaled_moe_gb300", "csrc", "moe_api.cu")).read()
+    cases = set(re.findall(r"case\s+(MOE_(?:OPT|DBG)_\w+)\s*:", src))
+    keys = [k for k in bm.C if k.startswith("MOE_OPT_") or k.startswith("MOE_DBG_")]
+    assert keys
+    missing = [k for k in keys if k not in cases]
+    assert not missing, missing
