@@ -1,7 +1,7 @@
 // moe_route.cu -- router top-k with softmax weights, the step in front of
 // dispatch (ROCm/ATOM PR #2725, linked commits on the Triton softmax top-k
-// routing with a device count of real rows): rows at or past the count get ids
-// -1 and weight 0; each pick takes the largest remaining logit, ties to the
+// routing driven by the number of valid rows held on the device): every row
+// from that number on gets ids -1 and weight 0; each pick takes the largest remaining logit, ties to the
 // lowest expert id, and clears it to -inf, so a row that runs out of finite
 // logits picks expert 0 again with weight 0; weights are exp(l - max) over the
 // picked experts' sum (renormalised) or over the whole row's.

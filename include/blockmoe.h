@@ -104,7 +104,7 @@ typedef void* moe_stream_t;
 #define MOE_OPT_Y_FORMAT 12       /* MOE_Y_*: GEMM2 rows handed to the combine */
 #define MOE_OPT_DEBUG_GRID_GEN 13 /* test-only, write-only: preset the single-launch kernel's grid-barrier
                                      generation word to a value in [0, 2^32) (the pages test epoch words
-                                     preset just below 2^31 and 2^32; aiter #6881 commit notes).  The
+                                     preset a few counts short of 2^31 and 2^32; aiter #6881 commit notes).  The
                                      barrier compares the word for a change, so it may wrap.  Synchronous. */
 #define MOE_OPT_DEBUG_STALL_GRID 14 /* test-only, write-only, fault injection without a fault: 1 presets the
                                      single-launch kernel's grid-barrier arrival count to 2^31, so that the

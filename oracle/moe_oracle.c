@@ -412,10 +412,10 @@ int orc_max_threads(void) {
 
 /* Router top-k with softmax weights, the step in front of dispatch (ROCm/ATOM
  * PR #2725, linked commits on the Triton softmax top-k routing: an optional
- * device count of real rows sends rows at or past it to ids -1 with weight 0;
- * an expert once picked is cleared to -inf and picks use a strict greater-than
- * scan, so ties go to the lowest id and, once a row's finite logits run out,
- * expert 0 is picked again with weight 0; weights are renormalised over the
+ * valid-row count on the device gives every row from that count on ids -1 and
+ * weight 0; an expert once picked is cleared to -inf and picks use a strict
+ * greater-than scan, so ties go to the lowest id and a row with no finite
+ * logit left picks expert 0 again with weight 0; weights are renormalised over the
  * picked experts unless `renormalize` is 0).
  *
  * Per row t < nvr, with m = max_e logit[t,e]:

@@ -1,8 +1,8 @@
-"""GPU stress and boundary tests (the pages' test list: epoch words preset just below 2^31 and 2^32,
+"""GPU stress and boundary tests (the pages' test list: epoch words preset a few counts short of 2^31 and 2^32,
 interleaved calls of the two paths, eager and graph forwards over many shape transitions, no writes
 past `out`, every route on one expert).
 
-* the single-launch kernel's grid-barrier generation word preset just below 2^32 and 2^31 wraps
+* the single-launch kernel's grid-barrier generation word preset a few counts short of 2^32 and 2^31 wraps
   during the next forwards without changing a bit;
 * two handles on the same weights (fused and multi-kernel path) alternate eager forwards and CUDA
   graph replays over changing T; every output equals the reference of its T bitwise;
