@@ -16,7 +16,9 @@ import threading
 from typing import Optional
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-# BMOE_LIB_VARIANT=bounds loads the bounds-checking build (libblockmoe_bounds.so) instead
+# BMOE_LIB_VARIANT=bounds loads the bounds-checking build (libblockmoe_bounds.so) instead; other
+# values are refused at load time
+LIB_VARIANTS = ("", "bounds")
 LIB_VARIANT = os.environ.get("BMOE_LIB_VARIANT", "")
 LIB_PATH = os.path.join(PKG, "lib", f"libblockmoe_{LIB_VARIANT}.so" if LIB_VARIANT else "libblockmoe.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "blockmoe.h")
@@ -49,6 +51,8 @@ def load(path: Optional[str] = None):
     with _lock:
         if _lib is not None:
             return _lib
+        if path is None and LIB_VARIANT not in LIB_VARIANTS:
+            raise ImportError(f"BMOE_LIB_VARIANT={LIB_VARIANT!r} is not a build variant; known: {LIB_VARIANTS}")
         p = path or LIB_PATH
         if not os.path.exists(p):
             raise ImportError(f"{os.path.basename(p)} is not built ({p}); run __graft_entry__.build()"

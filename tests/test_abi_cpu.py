@@ -125,3 +125,14 @@ def test_every_option_and_debug_region_is_handled():
     assert keys
     missing = [k for k in keys if k not in cases]
     assert not missing, missing
+
+
+def test_unknown_variant_is_refused():
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, BMOE_LIB_VARIANT="../../elsewhere")
+    r = subprocess.run([sys.executable, "-c", "import block_scaled_moe_gb300 as bm; bm.load()"], cwd=root, env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0 and "not a build variant" in r.stderr
