@@ -29,7 +29,7 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _worker(rank, world, port, result_q):
+def _worker(rank, world, port, result_q, cut=17):
     import torch.distributed as dist
     try:
         os.environ["MASTER_ADDR"] = "127.0.0.1"
@@ -43,8 +43,7 @@ def _worker(rank, world, port, result_q):
         x, ids, wts, W = synth.make_all(w)
         Wh = [t.cpu() for t in W]
         per = ep.experts_per_rank(w.E, world)
-        # this rank's token shard (uneven on purpose) and its experts' weights
-        cut = 17
+        # this rank's token shard (uneven on purpose, or empty) and its experts' weights
         lo, hi = (0, cut) if rank == 0 else (cut, w.T)
         nv_local = max(0, min(hi, w.nvr) - lo)
         xl, idsl, wtsl = x[lo:hi], torch.from_numpy(ids[lo:hi]), torch.from_numpy(wts[lo:hi])
@@ -62,19 +61,23 @@ def _worker(rank, world, port, result_q):
         c = compare(got, ref)
         zero_rows_ok = bool(np.all(got[nv_local:] == 0))
         # runtime choice: the same answer on every rank, from the largest local count
-        choice_small = ep.select_runtime(hi - lo, small_max=25)    # max(17, 23) = 23 <= 25
-        choice_large = ep.select_runtime(hi - lo, small_max=20)    # 23 > 20
+        biggest = max(cut, w.T - cut)
+        choice_small = ep.select_runtime(hi - lo, small_max=biggest)      # the largest shard fits
+        choice_large = ep.select_runtime(hi - lo, small_max=biggest - 1)  # it does not
         result_q.put((rank, c, zero_rows_ok, choice_small, choice_large, plan.send_counts, rcv.recv_counts))
         dist.destroy_process_group()
     except Exception as exc:  # pragma: no cover - reported to the parent
         result_q.put((rank, repr(exc), None, None, None, None, None))
 
 
-def test_ep_dispatch_combine_two_gloo_ranks():
+@pytest.mark.parametrize("cut", [17, 0, 40], ids=["uneven", "rank0_idle", "rank1_idle"])
+def test_ep_dispatch_combine_two_gloo_ranks(cut):
+    """Token shards [0, cut) and [cut, 40): uneven, or one rank holding no tokens (it still computes
+    the rows the other rank sends to its experts)."""
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q, cut)) for r in range(2)]
     for p in procs:
         p.start()
     res = {}
