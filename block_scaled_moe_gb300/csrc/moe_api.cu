@@ -299,6 +299,7 @@ int moe_create(moe_handle* out, int H, int I, int E, int topk, int capacity) {
                     prop.major, prop.minor);
     e = bmoe::gemm_set_attributes();
     if (e == cudaSuccess) e = bmoe::fused_set_attributes();
+    if (e == cudaSuccess) e = bmoe::dispatch_set_attributes();
     if (e != cudaSuccess) return fail(nullptr, MOE_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     int coop = 0;
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
@@ -514,8 +515,9 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     a.ys = ys;
     a.trace = nullptr;
 #ifdef BMOE_TRACE
-    static long long* trace_buf = nullptr;  // [2 GEMMs][2 CTAs][6][512] clock64 stamps
-    if (!trace_buf) cudaMalloc(&trace_buf, sizeof(long long) * 2 * 2 * 6 * 512);
+    // per GEMM: [2 CTAs][8][512] clock64 stamps, then [1024 CTAs][2] globaltimer start / end
+    static long long* trace_buf = nullptr;
+    if (!trace_buf) cudaMalloc(&trace_buf, sizeof(long long) * 2 * (2 * 8 * 512 + 2 * 1024));
     a.trace = trace_buf;
     bmoe_trace_buffer = trace_buf;
 #endif
@@ -536,7 +538,7 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     a.g_dbg = g.debug ? ws.g : nullptr;
     e = bmoe::launch_gemm1(a, &wb.tm_w13p, &h->tm_aq, g.NT, h->num_sms, s);
 #ifdef BMOE_TRACE
-    a.trace = trace_buf + 2 * 6 * 512;
+    a.trace = trace_buf + 2 * 8 * 512 + 2 * 1024;
 #endif
     if (e != cudaSuccess) return cuda_fail(h, e, "GEMM1 launch");
     h->launches += 1;

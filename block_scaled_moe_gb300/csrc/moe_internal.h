@@ -103,6 +103,9 @@ cudaError_t launch_fixed_mark(const Geometry& g, const Workspace& ws, const int3
                               const int32_t* nvr, cudaStream_t s);
 cudaError_t launch_compact_dispatch(const Geometry& g, const Workspace& ws, const int32_t* ids, int T,
                                     const int32_t* nvr, cudaStream_t s);
+// Shared-memory limit of the compact-dispatch count kernel for up to kMaxExperts experts; once per device
+// before the first launch (moe_create, and the allocation-free dispatch's per-device set-up).
+cudaError_t dispatch_set_attributes();
 cudaError_t launch_quant_scatter(const Geometry& g, const Workspace& ws, const uint16_t* x, const int32_t* ids,
                                  int T, const int32_t* nvr, cudaStream_t s);
 // y8/ys non-null: the GEMM2 rows are MXFP8 codes and scales instead of BF16 y.

@@ -285,6 +285,12 @@ cudaError_t launch_fixed_mark(const Geometry& g, const Workspace& ws, const int3
     return cudaGetLastError();
 }
 
+cudaError_t dispatch_set_attributes() {
+    // k_compact_count keeps 4E+2 int32 in dynamic shared memory: above the default 48 KB for E >= 3072
+    return cudaFuncSetAttribute(k_compact_count, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(sizeof(int) * (4 * kMaxExperts + 2)));
+}
+
 cudaError_t launch_compact_dispatch(const Geometry& g, const Workspace& ws, const int32_t* ids, int T,
                                     const int32_t* nvr, cudaStream_t s) {
     DispatchArgs a = dispatch_args(g, ws, ids, T, nvr);

@@ -35,7 +35,8 @@ int fail(int code, const char* msg) {
 }
 
 // Device address of the scratch array on the current device; looked up once per
-// device (the host-side symbol is only a stand-in and must not reach a kernel).
+// device (the host-side symbol is only a stand-in and must not reach a kernel),
+// together with the dispatch kernel's shared-memory limit.
 int scratch_address(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -48,6 +49,13 @@ int scratch_address(void** out) {
             char buf[256];
             snprintf(buf, sizeof(buf), "moe_dispatch_compact_noalloc: cudaGetSymbolAddress failed: %s",
                      cudaGetErrorString(e));
+            return fail(MOE_ECUDA, buf);
+        }
+        e = bmoe::dispatch_set_attributes();  // the count kernel's shared memory for large E, once per device
+        if (e != cudaSuccess) {
+            char buf[256];
+            snprintf(buf, sizeof(buf), "moe_dispatch_compact_noalloc: setting the dispatch kernel's shared memory "
+                     "limit failed: %s", cudaGetErrorString(e));
             return fail(MOE_ECUDA, buf);
         }
         g_scratch_ptr[dev] = p;

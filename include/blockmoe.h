@@ -314,15 +314,18 @@ int moe_profile_read(moe_handle h, float* ms, int n);
  * scan of counts with E+1 entries, perm, route_row; see MOE_DBG_* below for
  * their layouts), and allocates nothing: its scratch is a 1 MiB array built
  * into the library (every GPU that loads the library keeps it until the
- * process exits), so it accepts only sizes with (ceil(T*topk/512) + 1) * E
- * int32 values plus 256 bytes within 1 MiB, and refuses larger ones with
- * MOE_ECAPACITY.  All calls share that array, so calls that overlap on the GPU
+ * process exits), so it accepts only sizes that need at most
+ * 256 + 4 * (ceil(T*topk/512) * E + E + 1) bytes of scratch within 1 MiB, and
+ * refuses larger ones with MOE_ECAPACITY.  All calls share that array, so calls that overlap on the GPU
  * (other streams, other threads) race and must be serialised by the caller.
  * The first call on a device looks up the array's device address; make that
  * first call before any stream capture.  Outputs: counts int32 [E],
  * offsets int32 [E+1], perm int32 [T*topk] (first offsets[E] entries
  * written), route_row int32 [T*topk]; all device memory of the caller.
- * num_valid_rows as in moe_forward.  Errors: moe_last_error(NULL). */
+ * num_valid_rows as in moe_forward.  Ids outside [0, E) claim no slot, as in
+ * moe_forward, but this call reports nothing about ids >= E (it has no status
+ * word a caller can read).  The first call on a device also sets the dispatch
+ * kernel's shared-memory limit there.  Errors: moe_last_error(NULL). */
 int moe_dispatch_compact_noalloc(const int32_t* topk_ids, int T, int topk, int E, const int32_t* num_valid_rows,
                                  int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* route_row,
                                  moe_stream_t stream);

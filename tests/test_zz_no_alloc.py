@@ -1,4 +1,5 @@
-"""The allocation-free compact dispatch, checked against moe_forward's own dispatch.
+"""The allocation-free compact dispatch, checked against the oracle's dispatch and
+against moe_forward's own.
 
 Some callers may not allocate device memory at all (code running during CUDA
 graph capture, engines that reserve the whole GPU up front), so the library
@@ -42,20 +43,22 @@ def _forward_dispatch(ids: np.ndarray, E: int, nvr: int):
     return out
 
 
-def _noalloc_dispatch(ids: np.ndarray, E: int, nvr: int):
+def _noalloc_dispatch(ids: np.ndarray, E: int, nvr):
     import block_scaled_moe_gb300 as bm
     T, K = ids.shape
     dev = torch.device("cuda")
     ids_d = torch.from_numpy(ids).to(dev)
-    nvr_d = torch.tensor([nvr], dtype=torch.int32, device=dev)
+    nvr_d = None if nvr is None else torch.tensor([nvr], dtype=torch.int32, device=dev)
     # sentinel-filled outputs: everything the call must produce gets overwritten
     counts = torch.full((E,), -7, dtype=torch.int32, device=dev)
     offsets = torch.full((E + 1,), -7, dtype=torch.int32, device=dev)
     perm = torch.full((T * K,), -7, dtype=torch.int32, device=dev)
     route_row = torch.full((T * K,), -7, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream().cuda_stream
-    bm.moe_dispatch_compact_noalloc(ids_d.data_ptr(), T, K, E, nvr_d.data_ptr(), counts.data_ptr(),
-                                    offsets.data_ptr(), perm.data_ptr(), route_row.data_ptr(), stream)
+    bm.moe_dispatch_compact_noalloc(ids_d.data_ptr() if T else 0, T, K, E,
+                                    None if nvr_d is None else nvr_d.data_ptr(), counts.data_ptr(),
+                                    offsets.data_ptr(), perm.data_ptr() if T else 0,
+                                    route_row.data_ptr() if T else 0, stream)
     torch.cuda.synchronize()
     return {"counts": counts.cpu().numpy(), "offsets": offsets.cpu().numpy(), "perm": perm.cpu().numpy(),
             "route_row": route_row.cpu().numpy()}
@@ -66,7 +69,13 @@ def _same(a, b):
     assert np.array_equal(a["counts"], b["counts"])
     assert np.array_equal(a["offsets"], b["offsets"])
     assert np.array_equal(a["perm"][:R], b["perm"][:R])
-    assert np.array_equal(a["route_row"], b["route_row"])
+    assert np.array_equal(np.asarray(a["route_row"]).reshape(-1), np.asarray(b["route_row"]).reshape(-1))
+
+
+def _oracle(ids: np.ndarray, E: int, nvr):
+    import oracle
+    oracle.build()
+    return oracle.dispatch_compact(ids, E, nvr)
 
 
 def test_noalloc_dispatch_matches_forward_two_calls_in_a_row():
@@ -78,6 +87,8 @@ def test_noalloc_dispatch_matches_forward_two_calls_in_a_row():
     w2 = synth.get("tiny")
     ids2, _ = synth.make_routing(w2)
     a2 = _noalloc_dispatch(ids2, w2.E, w2.nvr)
+    _same(a1, _oracle(ids1, w1.E, w1.nvr))
+    _same(a2, _oracle(ids2, w2.E, w2.nvr))
     _same(a1, _forward_dispatch(ids1, w1.E, w1.nvr))
     _same(a2, _forward_dispatch(ids2, w2.E, w2.nvr))
     # and once more on the first input: identical to its first result
@@ -91,3 +102,17 @@ def test_noalloc_dispatch_refuses_sizes_beyond_its_scratch():
         bm.moe_dispatch_compact_noalloc(0, T, K, E, None, 1, 1, 1, 1, 0)
     assert ei.value.code == bm.MOE_ECAPACITY
     assert "scratch" in bm.moe_last_error(None)
+
+
+def test_noalloc_dispatch_empty_null_count_and_many_experts():
+    # T = 0: zero counts and offsets, nothing else touched
+    a0 = _noalloc_dispatch(np.zeros((0, 6), np.int32), 384, None)
+    assert not a0["counts"].any() and not a0["offsets"].any()
+    # no row count: every row is valid, as with num_valid_rows = T
+    rng = np.random.default_rng(7)
+    ids = rng.integers(-1, 40, size=(300, 4)).astype(np.int32)
+    _same(_noalloc_dispatch(ids, 40, None), _oracle(ids, 40, None))
+    _same(_noalloc_dispatch(ids, 40, None), _noalloc_dispatch(ids, 40, 300))
+    # E = 4096, the largest the library accepts (the count kernel then needs 64 KB of shared memory)
+    ids = rng.integers(-1, 4096, size=(200, 8)).astype(np.int32)
+    _same(_noalloc_dispatch(ids, 4096, 150), _oracle(ids, 4096, 150))
