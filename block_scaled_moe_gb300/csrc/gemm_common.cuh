@@ -11,18 +11,29 @@ namespace {
 
 // Pipeline tracing (compiled in with -DBMOE_TRACE): clock64 stamps of the first
 // kTraceJobs K stages of CTAs 0 and 1, per role, into GemmArgs::trace
-// ([2 CTAs][6 events][kTraceJobs] int64): 0 producer got a free stage, 1 producer
+// ([2 CTAs][8 events][kTraceJobs] int64): 0 producer got a free stage, 1 producer
 // issued it, 2 first MMA warp saw it full, 3 that warp issued its MMAs; per
-// unit: 4 epilogue saw the accumulator, 5 epilogue released it.
+// unit: 4 epilogue saw the accumulator, 5 epilogue released it; per stage again:
+// 6 weight-scale warp got the free stage, 7 it arrived on the full barrier.
 __device__ __forceinline__ void trace(const GemmArgs& a, int ev, long idx) {
 #ifdef BMOE_TRACE
     constexpr int kTraceJobs = 512;
     if (a.trace && blockIdx.x < 2 && idx < kTraceJobs)
-        a.trace[(static_cast<long>(blockIdx.x) * 6 + ev) * kTraceJobs + idx] = clock64();
+        a.trace[(static_cast<long>(blockIdx.x) * 8 + ev) * kTraceJobs + idx] = clock64();
 #else
     (void)a;
     (void)ev;
     (void)idx;
+#endif
+}
+
+// Tracing builds: globaltimer stamp `which` (0 start, 1 end) of this CTA, after the stage stamps.
+__device__ __forceinline__ void trace_cta(const GemmArgs& a, int which) {
+#ifdef BMOE_TRACE
+    if (a.trace && blockIdx.x < 1024) a.trace[2 * 8 * 512 + 2 * blockIdx.x + which] = static_cast<long long>(globaltimer_ns());
+#else
+    (void)a;
+    (void)which;
 #endif
 }
 

@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
     int32_t* tab = reinterpret_cast<int32_t*>(sSFB + STAGES * KC * NB * 512 + C::BAR_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) trace_cta(a, 0);
     const int ntiles = __ldg(a.tile_base + a.E);
     const int n_units = ntiles * a.mtiles;
     if (static_cast<int>(blockIdx.x) >= n_units) return;  // whole CTA
@@ -330,6 +331,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
+            long sjob = 0;
             for (long G0 = 0; G0 < ngroups && ok; G0 += GD) {
 #pragma unroll
                 for (int d = 0; d < GD; ++d) {
@@ -342,6 +344,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                             ok = false;
                             continue;
                         }
+                        if (lane == 0) trace(a, 6, sjob);
                         uint4* dst = reinterpret_cast<uint4*>(sSFA + stage * NA * KC * 512) + lane;
 #pragma unroll
                         for (int op = 0; op < NA; ++op)
@@ -354,6 +357,8 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                             }
                         fence_proxy_async_smem();
                         mbar_arrive(&full[stage]);
+                        if (lane == 0) trace(a, 7, sjob);
+                        ++sjob;
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -737,6 +742,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) trace_cta(a, 1);
     if (warp == C::MMA_WARP0) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
