@@ -79,8 +79,10 @@ def swiglu(g: np.ndarray, I: int, limit: float) -> np.ndarray:
 
 
 def grouped_forward(x_bf16: torch.Tensor, ids: np.ndarray, wts: np.ndarray, weights, nvr=None,
-                    swiglu_limit: float = 0.0, y_fp32: bool = False, y_mxfp8: bool = False) -> np.ndarray:
-    """Per-expert grouped formulation.  Returns BF16 bits [T,H]."""
+                    swiglu_limit: float = 0.0, y_fp32: bool = False, y_mxfp8: bool = False,
+                    swiglu_fn=None) -> np.ndarray:
+    """Per-expert grouped formulation.  Returns BF16 bits [T,H].  `swiglu_fn(g, I, limit)` replaces
+    the activation (tests use it to plant wrong readings of the clamp)."""
     w13, w13s, w2, w2s = (np.asarray(a.cpu().numpy() if isinstance(a, torch.Tensor) else a) for a in weights)
     E, I2, _ = w13.shape
     I = I2 // 2
@@ -98,7 +100,7 @@ def grouped_forward(x_bf16: torch.Tensor, ids: np.ndarray, wts: np.ndarray, weig
             continue
         A = xdq[t_idx]
         G = (A @ fp4_dequant(w13[e], w13s[e]).T).astype(np.float32)
-        h = swiglu(G, I, swiglu_limit)
+        h = (swiglu_fn or swiglu)(G, I, swiglu_limit)
         hq, hs = q8(h)
         Yv = (q8_dequant(hq, hs) @ fp4_dequant(w2[e], w2s[e]).T).astype(np.float32)
         if y_mxfp8:

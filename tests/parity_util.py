@@ -76,3 +76,51 @@ class Case:
     def oracle(self, rows=None, nvr=True, nthreads=0):
         return oracle.moe_forward(self.x, self.ids, self.wts, self.Wh, num_valid_rows=self.w.nvr if nvr else None,
                                   swiglu_limit=self.w.swiglu_limit, rows=rows, nthreads=nthreads)
+
+
+def cover_rows(ids: np.ndarray, E: int, nvr: int, route_tile: int, dispatch: str, extra: int = 0, seed: int = 0):
+    """Rows to compare at full size, chosen so that every active expert's first and last route tile
+    (the ragged one) holds at least one compared route: a greedy cover over the (expert, tile) pairs,
+    plus `extra` rows drawn at random.  A route's tile is its rank among the expert's packed rows
+    (compact: flat slot order t*K+k; fixed: one row per distinct token, tokens ascending) over the
+    route tile width."""
+    T, K = ids.shape
+    nvr = max(0, min(T, int(nvr)))
+    tile_of = {}        # (t, k) -> (e, j)
+    last = {}
+    seen = {}
+    for t in range(nvr):
+        for k in range(K):
+            e = int(ids[t, k])
+            if e < 0 or e >= E:
+                continue
+            if dispatch == "fixed":
+                key = (e, t)
+                if key not in seen:
+                    seen[key] = last.get(e, -1) + 1
+                    last[e] = seen[key]
+                rank = seen[key]
+            else:
+                rank = last.get(e, -1) + 1
+                last[e] = rank
+            tile_of[(t, k)] = (e, rank // route_tile)
+    need = set()
+    for e, r in last.items():
+        need.add((e, 0))
+        need.add((e, r // route_tile))
+    covers = {}
+    for (t, k), ej in tile_of.items():
+        if ej in need:
+            covers.setdefault(t, set()).add(ej)
+    chosen = []
+    while need:
+        t = max(covers, key=lambda r: (len(covers[r] & need), -r))
+        got = covers[t] & need
+        assert got, "uncoverable tile"
+        chosen.append(t)
+        need -= got
+    rng = np.random.default_rng(seed)
+    pool = np.setdiff1d(np.arange(nvr), chosen)
+    if extra and pool.size:
+        chosen += list(rng.choice(pool, size=min(extra, pool.size), replace=False))
+    return np.sort(np.array(chosen, dtype=np.int64))

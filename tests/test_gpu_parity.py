@@ -16,7 +16,7 @@ import torch
 
 import oracle
 import synth
-from parity_util import Case, assert_close, compare, torch_bf16_bits
+from parity_util import Case, assert_close, compare, cover_rows, torch_bf16_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -279,16 +279,21 @@ def test_refused_bind_keeps_previous_binding():
 
 # ------------------------------------------------------------------ full-size workloads
 
+def _route_tile(w):
+    """The handle's default route tile for a workload (32 for decode-sized capacities, else 144)."""
+    return 32 if w.capacity * w.K <= 8 * w.E else 144
+
+
 def _full_size(name, n_rows, **kw):
+    """Full-size workload in the bench's launch configuration against the oracle on a row sample that
+    covers every active expert's first and last (ragged) route tile, plus `n_rows` random rows."""
     w = synth.get(name)
     c = Case(w, weights_on_device=True)
     L = c.layer(**kw)
     out = c.run(L)
     torch.cuda.synchronize()
     got = _out_bits(out)
-    rng = np.random.default_rng(0)
-    valid_rows = np.arange(min(w.nvr, w.T))
-    rows = np.sort(rng.choice(valid_rows, size=min(n_rows, len(valid_rows)), replace=False))
+    rows = cover_rows(c.ids, w.E, w.nvr, kw.get("route_tile", _route_tile(w)), L.scheme, extra=n_rows)
     ref = c.oracle(rows=rows)
     cmp_ = assert_close(got[rows], ref, name)
     assert np.all(got[w.nvr:] == 0)

@@ -433,3 +433,28 @@ def test_mxfp8_gemm2_rows_equal_grouped_formulation(oracle_lib):
     b = oracle.bf16_bits_to_float(bf).astype(np.float64)
     rel = np.linalg.norm(a - b) / np.linalg.norm(b)
     assert 1e-3 < rel < 5e-2, rel
+
+
+def test_float_gemm2_rows_equal_grouped_formulation(oracle_lib):
+    """GEMM2 rows handed to the combine as float (no BF16 rounding of y): the oracle equals the grouped
+    formulation with y_fp32, bit for bit, on the tiny workload and on micro workloads with invalid
+    slots, repeated experts and the clamp; and the rounding of y to BF16 does change the result."""
+    import oracle
+    cases = [synth.get("tiny")]
+    for seed in range(6):
+        cases.append(synth.micro(24 + 7 * seed, 64 * (1 + seed % 3), 64 * (1 + (seed + 1) % 2), 3 + seed, 1 + seed % 4,
+                                 nvr=20 + 7 * seed, routing="hot_zipf" if seed % 2 else "uniform", invalid_frac=0.1,
+                                 swiglu_limit=10.0 if seed % 3 == 0 else 0.0, seed=100 + seed, hot_frac=0.5))
+    for w in cases:
+        x, ids, wts, W = synth.make_all(w)
+        got = oracle.moe_forward(x, ids, wts, [t.cpu() for t in W], num_valid_rows=w.nvr,
+                                 swiglu_limit=w.swiglu_limit, y_format="fp32")
+        ref = grouped_forward(x, ids, wts, W, nvr=w.nvr, swiglu_limit=w.swiglu_limit, y_fp32=True)
+        assert np.array_equal(got, ref), w
+        assert np.array_equal(got, oracle.moe_forward(x, ids, wts, [t.cpu() for t in W], num_valid_rows=w.nvr,
+                                                      swiglu_limit=w.swiglu_limit, y_fp32=True))
+    w = synth.get("tiny")
+    x, ids, wts, W = synth.make_all(w)
+    bf = oracle.moe_forward(x, ids, wts, [t.cpu() for t in W], num_valid_rows=w.nvr)
+    f32 = oracle.moe_forward(x, ids, wts, [t.cpu() for t in W], num_valid_rows=w.nvr, y_format="fp32")
+    assert not np.array_equal(bf, f32)
