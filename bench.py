@@ -13,6 +13,13 @@ single-launch fused kernel (the whole layer) when the forward takes that path,
 as decode does, else GEMM1 (it streams 2/3 of the active-expert weight bytes);
 `cpu_baseline` times the CPU oracle on a bounded sample of the same workload.
 
+`per_config` (one GPU) adds one record per other workload (small-M, large-M and
+skewed prefill by default): median step time, tokens/s, the layer's fraction of
+the measured HBM copy rate and of the dense FP8 tensor peak (2 x the measured
+BF16 rate), the dominant kernel's, and the CPU oracle (all cores and one core).
+Stage times come from a separate profiled pass, so the timed steps carry no
+events but their own.
+
 --impl reference times the CPU oracle itself on the same workload (bounded
 row sample per step) and prints the same line with "impl": "reference".
 Multi-GPU (torchrun): every rank runs an independent replica (the layer does
@@ -49,6 +56,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--path", default="auto", choices=["auto", "fused", "multi"],
                    help="layer path (auto: the fused kernel where the handle allows it)")
+    p.add_argument("--per-config", default="smallm_pro,largem_pro,skewed_flash",
+                   help="other workloads measured after the headline one (comma list, '' for none; one GPU only)")
     return p.parse_args()
 
 
@@ -177,7 +186,9 @@ def job_throughput(valid_rows_per_step: int, steps: int, world: int, max_ms: flo
     return valid_rows_per_step * steps * world / (max_ms / 1e3)
 
 
-def cpu_baseline(w, x, ids, wts, Wh, rows_n):
+def cpu_baseline(w, x, ids, wts, Wh, rows_n, rows_1core=2):
+    """The oracle as it stands on the host cores: a seeded sample of `rows_n` valid rows on every core of
+    the affinity mask, and `rows_1core` rows on one core."""
     import numpy as np
     import oracle
     rng = np.random.default_rng(1)
@@ -187,9 +198,157 @@ def cpu_baseline(w, x, ids, wts, Wh, rows_n):
     oracle.moe_forward(x, ids, wts, Wh, num_valid_rows=w.nvr, swiglu_limit=w.swiglu_limit, rows=rows,
                        nthreads=threads)
     dt = time.perf_counter() - t0
+    r1 = rows[:rows_1core]
+    t0 = time.perf_counter()
+    oracle.moe_forward(x, ids, wts, Wh, num_valid_rows=w.nvr, swiglu_limit=w.swiglu_limit, rows=r1, nthreads=1)
+    dt1 = time.perf_counter() - t0
     return {"value": len(rows) / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"{len(rows)} of {w.nvr} valid rows of the {w.name} workload (seeded), "
-                      f"{dt:.2f} s wall on {threads} threads"}
+                      f"{dt:.2f} s wall on {threads} threads",
+            "value_1core": len(r1) / dt1, "sample_1core": f"{len(r1)} of those rows on 1 thread, {dt1:.2f} s wall"}
+
+
+def fp8_peaks(bf16_tf, bf16_tf_sus):
+    """Dense FP8 tensor peak: the measured cuBLAS BF16 rate times the nominal FP8 / BF16 ratio (4.5 / 2.25)."""
+    return 2.0 * bf16_tf, 2.0 * bf16_tf_sus
+
+
+def measure(w, dev, args, path, stream, flush, world=1, e2e=False):
+    """One workload on this rank's GPU: warm-up, `args.steps` timed forwards (CUDA events on the forward's
+    stream, L2 flushed before each outside the events, no profiling events inside), then a separate
+    profiled pass for the per-stage times.  Inputs are device-resident; `e2e` adds the end-to-end pass."""
+    import numpy as np
+    import torch
+
+    import block_scaled_moe_gb300 as bm
+    import synth
+    x = synth.make_x(w)
+    ids, wts = synth.make_routing(w)
+    W = synth.make_weights(w, dev)
+    layer = bm.BlockScaledMoE(w.H, w.I, w.E, w.K, w.capacity, dispatch=w.dispatch, swiglu_limit=w.swiglu_limit,
+                              path=path)
+    layer.bind_weights(*W)
+    xd = x.to(dev)
+    idsd = torch.from_numpy(ids).to(dev)
+    wtsd = torch.from_numpy(wts).to(dev)
+    nvrd = torch.tensor([w.nvr], dtype=torch.int32, device=dev)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        layer.forward(xd, idsd, wtsd, nvrd, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    status = layer.read_status()
+    if status:
+        raise RuntimeError(f"device status {status:#x} after warm-up ({w.name})")
+
+    # ---- timed region: device-resident inputs, L2 flushed between steps (outside the events)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches0 = layer.launches
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for i in range(args.steps):
+            flush.fill_(1.0)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = layer.launches - launches0
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    # ---- per-stage times in a separate profiled pass (CUDA events between the stages)
+    layer.set_profile(True)
+    stage_ms = []
+    for _ in range(max(3, min(args.steps, 10))):
+        flush.fill_(1.0)
+        step()
+        stage_ms.append(layer.profile_ms())
+    layer.set_profile(False)
+    torch.cuda.synchronize()
+
+    r = {"w": w, "ids": ids, "x": x, "wts": wts, "W": W, "step_ms": step_ms, "launches": launches,
+         "stage_ms": [statistics.mean(s[i] for s in stage_ms) for i in range(5)], "path": layer.last_path,
+         "scheme": layer.scheme, "clocks": clk.summary()}
+    if e2e:
+        # ---- end to end: pinned host buffers, H2D inputs + forward + D2H output per step
+        xh = x.pin_memory()
+        idsh = torch.from_numpy(ids).pin_memory()
+        wtsh = torch.from_numpy(wts).pin_memory()
+        nvrh = torch.tensor([w.nvr], dtype=torch.int32).pin_memory()
+        outh = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+        xe, ie, we, ne = torch.empty_like(xd), torch.empty_like(idsd), torch.empty_like(wtsd), torch.empty_like(nvrd)
+
+        def e2e_step():
+            xe.copy_(xh, non_blocking=True)
+            ie.copy_(idsh, non_blocking=True)
+            we.copy_(wtsh, non_blocking=True)
+            ne.copy_(nvrh, non_blocking=True)
+            layer.forward(xe, ie, we, ne, out=out, stream=stream)
+            outh.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(1.0)
+            es[i].record(stream)
+            e2e_step()
+            ee[i].record(stream)
+        torch.cuda.synchronize()
+        r["e2e_ms"] = [s.elapsed_time(e) for s, e in zip(es, ee)]
+        r["h2d"] = xh.numel() * 2 + idsh.numel() * 4 + wtsh.numel() * 4 + 4
+        r["d2h"] = outh.numel() * 2
+    layer.close()
+    return r
+
+
+def config_record(r, hbm_gbs, bf16_tf, bf16_tf_sus, peak_src, cpu=None):
+    """One workload's record: median step time, tokens/s, the layer's HBM and FP8 tensor fractions, the
+    dominant kernel's, and the CPU oracle next to it."""
+    w = r["w"]
+    wb = workload_bytes_flops(w, r["ids"])
+    med = statistics.median(r["step_ms"])
+    fp8, fp8_sus = fp8_peaks(bf16_tf, bf16_tf_sus)
+    gbs = wb["step"] / (med / 1e3) / 1e9
+    tf = wb["flops"] / (med / 1e3) / 1e12
+    fused = r["path"] == "fused"
+    k_ms = r["stage_ms"][2]
+    k_bytes = wb["step"] if fused else wb["gemm1"]
+    k_flops = wb["flops"] if fused else 4 * w.H * w.I * wb["routes"]
+    ridge = fp8 * 1e12 / (hbm_gbs * 1e9)
+    rec = {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "topk": w.K, "num_valid_rows": w.nvr,
+           "dispatch": r["scheme"], "path": r["path"], "swiglu_limit": w.swiglu_limit, "routes": wb["routes"],
+           "active_experts": wb["active"], "steps": len(r["step_ms"]), "ms_median": med,
+           "ms_mean": statistics.mean(r["step_ms"]), "tokens_per_s": w.nvr / (med / 1e3),
+           "roofline": {"bytes_per_step": wb["step"], "flops_per_step": wb["flops"],
+                        "arithmetic_intensity": wb["flops"] / wb["step"], "ridge_flop_per_byte": ridge,
+                        "bound": "hbm" if wb["flops"] / wb["step"] < ridge else "tensor",
+                        "hbm": {"achieved_gbs": gbs, "peak_gbs": hbm_gbs, "frac": gbs / hbm_gbs},
+                        "fp8": {"achieved_tflops": tf, "peak_tflops": fp8, "frac": tf / fp8,
+                                "peak_tflops_sustained": fp8_sus, "frac_of_sustained": tf / fp8_sus},
+                        "peak_source": peak_src,
+                        "fp8_peak_derivation": "2 x the measured cuBLAS BF16 rate (nominal dense FP8 / BF16 = "
+                                               "4.5 / 2.25 PFLOP/s); burst figure for a step timed alone"},
+           "dominant_kernel": {"name": "fused layer kernel" if fused else "GEMM1", "ms_mean": k_ms,
+                               "hbm_frac": k_bytes / (k_ms / 1e3) / 1e9 / hbm_gbs,
+                               "fp8_frac": k_flops / (k_ms / 1e3) / 1e12 / fp8},
+           "stage_ms_mean": r["stage_ms"],
+           "stages": ["-", "-", "fused kernel", "-", "-"] if fused else
+                     ["dispatch", "quant+scatter", "gemm1", "gemm2", "combine"],
+           "gpu_launches_per_step": r["launches"] / max(1, len(r["step_ms"])), "clocks": r["clocks"]}
+    if cpu is not None:
+        rec["cpu_baseline"] = cpu
+    return rec
 
 
 def main():
@@ -238,104 +397,29 @@ def main():
 
     import __graft_entry__
     __graft_entry__.build()
-    import block_scaled_moe_gb300 as bm
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)  # before the process group, so that NCCL binds this rank's GPU
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-
-    x = synth.make_x(w)
-    ids, wts = synth.make_routing(w)
-    W = synth.make_weights(w, dev)
-    layer = bm.BlockScaledMoE(w.H, w.I, w.E, w.K, w.capacity, dispatch=w.dispatch, swiglu_limit=w.swiglu_limit,
-                              path=args.path)
-    layer.bind_weights(*W)
-    xd = x.to(dev)
-    idsd = torch.from_numpy(ids).to(dev)
-    wtsd = torch.from_numpy(wts).to(dev)
-    nvrd = torch.tensor([w.nvr], dtype=torch.int32, device=dev)
-    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 512 MiB > 129 MB L2
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = peaks()
 
-    def step():
-        layer.forward(xd, idsd, wtsd, nvrd, out=out, stream=stream)
-
-    layer.set_profile(True)
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        step()
-    torch.cuda.synchronize()
-    status = layer.read_status()
-    if status:
-        raise RuntimeError(f"device status {status:#x} after warm-up")
-
-    # ---- timed region: device-resident inputs, L2 flushed between steps (outside the events)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stage_ms = []
-    launches0 = layer.launches
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            flush.fill_(1.0)
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-            stage_ms.append(layer.profile_ms())
-        torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    launches = layer.launches - launches0
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    r = measure(w, dev, args, args.path, stream, flush, world=world, e2e=True)
+    step_ms = r["step_ms"]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
-    tokens = w.nvr * args.steps * world
     value = job_throughput(w.nvr, args.steps, world, total_ms)
-
-    # ---- end to end: pinned host buffers, H2D inputs + forward + D2H output per step
-    xh = x.pin_memory()
-    idsh = torch.from_numpy(ids).pin_memory()
-    wtsh = torch.from_numpy(wts).pin_memory()
-    nvrh = torch.tensor([w.nvr], dtype=torch.int32).pin_memory()
-    outh = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
-    xe, ie, we, ne = torch.empty_like(xd), torch.empty_like(idsd), torch.empty_like(wtsd), torch.empty_like(nvrd)
-    h2d = xh.numel() * 2 + idsh.numel() * 4 + wtsh.numel() * 4 + 4
-    d2h = outh.numel() * 2
-    layer.set_profile(False)
-
-    def e2e_step():
-        xe.copy_(xh, non_blocking=True)
-        ie.copy_(idsh, non_blocking=True)
-        we.copy_(wtsh, non_blocking=True)
-        ne.copy_(nvrh, non_blocking=True)
-        layer.forward(xe, ie, we, ne, out=out, stream=stream)
-        outh.copy_(out, non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.fill_(1.0)
-        es[i].record(stream)
-        e2e_step()
-        ee[i].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(es, ee)), world, dev)
+    e2e_ms = max_over_ranks(sum(r["e2e_ms"]), world, dev)
     e2e_value = job_throughput(w.nvr, args.steps, world, e2e_ms)
 
-    # ---- roofline of the dominant kernel from its live CUDA-event durations (stage slot 2 holds GEMM1, or
-    # the whole fused kernel on the single-launch path)
-    wb = workload_bytes_flops(w, ids)
-    fused = layer.last_path == "fused"
+    # ---- roofline of the dominant kernel from its CUDA-event durations (stage slot 2 holds GEMM1, or the
+    # whole fused kernel on the single-launch path), measured in the profiled pass
+    wb = workload_bytes_flops(w, r["ids"])
+    fused = r["path"] == "fused"
     kern = "fused" if fused else "gemm1"
-    k_ms = statistics.mean(s[2] for s in stage_ms)
-    hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = peaks()
+    k_ms = r["stage_ms"][2]
     k_bytes = wb["step"] if fused else wb["gemm1"]
     achieved = k_bytes / (k_ms / 1e3) / 1e9
     traffic = traffic_for(kern, w.name)
@@ -346,8 +430,8 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8 x mxfp4 (e4m3 x e2m1, fp32 accumulate)",
             "data": "synthetic",
             "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "topk": w.K,
-                       "num_valid_rows": w.nvr, "dispatch": layer.scheme, "capacity": w.capacity,
-                       "path": layer.last_path,
+                       "num_valid_rows": w.nvr, "dispatch": r["scheme"], "capacity": w.capacity,
+                       "path": r["path"],
                        "swiglu_limit": w.swiglu_limit, "routes": wb["routes"], "active_experts": wb["active"],
                        "l2": "512 MiB buffer written between timed steps (outside the events)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -356,22 +440,45 @@ def main():
                                    "GEMM1 (tcgen05 block-scaled, W13 stream + SwiGLU/MXFP8 epilogue)",
                          "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": achieved / hbm_gbs, "traffic": traffic, "peak_source": peak_src,
-                         "algorithmic_bytes_per_launch": k_bytes, "launch_ms": k_ms},
+                         "algorithmic_bytes_per_launch": k_bytes, "launch_ms": k_ms,
+                         "launch_ms_from": "separate profiled pass (CUDA events on the forward's stream)"},
             "step_roofline": {"bytes_per_step": wb["step"], "achieved_gbs": step_gbs,
                               "frac_of_hbm": step_gbs / hbm_gbs,
                               "tflops": wb["flops"] / (total_ms / args.steps / world / 1e3) / 1e12,
-                              "stage_ms_mean": [statistics.mean(s[i] for s in stage_ms) for i in range(5)],
+                              "ms_median": statistics.median(step_ms),
+                              "stage_ms_mean": r["stage_ms"],
                               "stages": (["-", "-", "fused kernel", "-", "-"] if fused else
                                          ["dispatch", "quant+scatter", "gemm1", "gemm2", "combine"])},
-            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches * world,
-            "clocks": clk.summary()}
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
+                    "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": r["launches"] * world,
+            "clocks": r["clocks"]}
+    cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        Wh = [t.cpu() for t in W]
-        line["cpu_baseline"] = cpu_baseline(w, x, ids, wts, Wh, args.cpu_rows)
+        cpu = cpu_baseline(w, r["x"], r["ids"], r["wts"], [t.cpu() for t in r["W"]], args.cpu_rows)
+        line["cpu_baseline"] = cpu
+    del r["W"]
+    # ---- the other workloads on this GPU, one record each (one GPU only: the scaling runs keep to the
+    # headline workload)
+    names = [n for n in args.per_config.split(",") if n and n != w.name] if world == 1 else []
+    if names:
+        per = {w.name: config_record(r, hbm_gbs, bf16_tf, bf16_tf_sus, peak_src, cpu)}
+        del r
+        torch.cuda.empty_cache()
+        for n in names:
+            wn = synth.get(n)
+            rn = measure(wn, dev, args, "auto", stream, flush)
+            cn = None
+            if not args.no_cpu_baseline:
+                cn = cpu_baseline(wn, rn["x"], rn["ids"], rn["wts"], [t.cpu() for t in rn["W"]], 8)
+            del rn["W"]
+            torch.cuda.empty_cache()
+            per[n] = config_record(rn, hbm_gbs, bf16_tf, bf16_tf_sus, peak_src, cn)
+            del rn
+            torch.cuda.empty_cache()
+        line["per_config"] = per
     if rank == 0:
         print(json.dumps(line), flush=True)
-    layer.close()
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0

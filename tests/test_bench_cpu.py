@@ -81,3 +81,22 @@ def test_reference_arm_json_line():
     e = d["e2e"]
     assert e["value"] == d["value"] and e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"] == "tiny"
+
+
+def test_per_config_record_fractions():
+    """A per-workload record from hand-set timings: HBM and FP8 fractions follow from the algorithmic
+    bytes and FLOPs over the median step time and the stated peaks."""
+    w = synth.get("largem_pro")
+    ids, _ = synth.make_routing(w)
+    r = {"w": w, "ids": ids, "step_ms": [3.0, 2.0, 4.0], "launches": 21, "stage_ms": [0.1, 0.1, 1.5, 1.0, 0.1],
+         "path": "multi", "scheme": "compact", "clocks": {}}
+    rec = bench.config_record(r, 6000.0, 2000.0, 1800.0, "measured", cpu={"value": 1.0})
+    wb = bench.workload_bytes_flops(w, ids)
+    assert rec["ms_median"] == 3.0 and rec["tokens_per_s"] == w.nvr / 3e-3
+    assert abs(rec["roofline"]["hbm"]["frac"] - wb["step"] / 3e-3 / 6000e9) < 1e-12
+    assert rec["roofline"]["fp8"]["peak_tflops"] == 4000.0
+    assert abs(rec["roofline"]["fp8"]["frac"] - wb["flops"] / 3e-3 / 4000e12) < 1e-12
+    assert rec["roofline"]["bound"] == "hbm"          # AI ~ 464 F/B below the ridge of 4000/6 ~ 667
+    k = rec["dominant_kernel"]
+    assert k["name"] == "GEMM1" and abs(k["fp8_frac"] - 4 * w.H * w.I * wb["routes"] / 1.5e-3 / 4000e12) < 1e-12
+    assert rec["gpu_launches_per_step"] == 7 and rec["cpu_baseline"] == {"value": 1.0}
