@@ -16,9 +16,9 @@ import threading
 from typing import Optional
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-# BMOE_LIB_VARIANT=bounds loads the bounds-checking build (libblockmoe_bounds.so) instead; other
-# values are refused at load time
-LIB_VARIANTS = ("", "bounds")
+# BMOE_LIB_VARIANT=bounds loads the bounds-checking build (libblockmoe_bounds.so) instead, =trace the
+# tracing build (libblockmoe_trace.so); other values are refused at load time
+LIB_VARIANTS = ("", "bounds", "trace")
 LIB_VARIANT = os.environ.get("BMOE_LIB_VARIANT", "")
 LIB_PATH = os.path.join(PKG, "lib", f"libblockmoe_{LIB_VARIANT}.so" if LIB_VARIANT else "libblockmoe.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "blockmoe.h")

@@ -2,7 +2,9 @@
 
 Variant "bounds" builds libblockmoe_bounds.so with -DMOE_DEBUG_BOUNDS: every index the kernels compute
 into the workspace or an output row is checked, a miss is recorded in the status word and skipped.
-The binding loads it when BMOE_LIB_VARIANT=bounds is set."""
+Variant "trace" builds libblockmoe_trace.so with -DBMOE_TRACE: the kernels stamp clocks into trace
+buffers that block_scaled_moe_gb300.trace reads back.  The binding loads a variant when
+BMOE_LIB_VARIANT names it."""
 
 from __future__ import annotations
 
@@ -16,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
-VARIANTS = {"": [], "bounds": ["-DMOE_DEBUG_BOUNDS"]}
+VARIANTS = {"": [], "bounds": ["-DMOE_DEBUG_BOUNDS"], "trace": ["-DBMOE_TRACE"]}
 SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_gemm.cu", "moe_fused.cu", "moe_noalloc.cu", "moe_route.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC,-Wall", "-I", INCLUDE, "-I", CSRC,

@@ -25,6 +25,12 @@ using bmoe::Workspace;
 #ifdef BMOE_TRACE
 extern "C" {
 long long* bmoe_trace_buffer = nullptr;  // device pointer of the pipeline trace (tracing builds)
+// Copy the stand-alone GEMMs' trace of the last multi-kernel forward into host memory (synchronous).
+int bmoe_gemm_trace_copy(void* dst, size_t bytes) {
+    if (!bmoe_trace_buffer) return -1;
+    const size_t all = sizeof(long long) * 2 * (2 * 8 * 512 + 2 * 1024);
+    return static_cast<int>(cudaMemcpy(dst, bmoe_trace_buffer, bytes < all ? bytes : all, cudaMemcpyDeviceToHost));
+}
 }
 #endif
 
