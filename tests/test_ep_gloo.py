@@ -1,9 +1,12 @@
 """Expert-parallel host logic on two gloo ranks (CPU processes, no GPU).
 
-Each rank owns half of the experts and a shard of the tokens.  Dispatch, a local layer over the
-rank's own experts (the CPU oracle stands in for the GPU layer), and combine must give, for every
-token, the single-process oracle output within the layer tolerance (the partial rows are rounded to
-BF16 before the owner adds them).  The runtime choice follows the largest token count over the ranks.
+Each rank owns half of the experts and a shard of the tokens.  Dispatch sends MXFP8 rows (codes and
+1x32 scales), each rank runs the layer (the CPU oracle stands in for the GPU layer) on one row per
+valid local slot with weight 1 and MXFP8 GEMM2 rows, the GEMM2 rows travel back as MXFP8 and the owner
+combines them with its own top-k weights.  For every token the result must equal the single-process
+oracle with MXFP8 GEMM2 rows bit for bit (both formats are exact for what they carry), and the bytes
+per row on the wire are the MXFP8 ones.  The runtime choice follows the largest token count over the
+ranks.
 
 Failure detection (host side, no GPU): a rank that leaves between steps, with none of its exchanges in
 flight, makes the other rank's next exchange end with an error within the process group's short
@@ -49,16 +52,19 @@ def _worker(rank, world, port, result_q, cut=17):
         xl, idsl, wtsl = x[lo:hi], torch.from_numpy(ids[lo:hi]), torch.from_numpy(wts[lo:hi])
         plan = ep.make_plan(idsl, wtsl, w.E, world, rank, num_valid_rows=nv_local)
         rcv = ep.dispatch(plan, xl)
+        rt = ep.routes(rcv)
         mine = [t[rank * per:(rank + 1) * per].contiguous() for t in Wh]
-        if rcv.x.shape[0]:
-            part = oracle.moe_forward(rcv.x, rcv.ids.numpy(), rcv.weights.numpy(), mine)
-            partial = torch.from_numpy(part.view(np.int16)).view(torch.bfloat16)
+        if rt.x.shape[0]:
+            part = oracle.moe_forward(rt.x, rt.ids.numpy(), rt.weights.numpy(), mine, y_format="mxfp8")
+            y_rows = torch.from_numpy(part.view(np.int16)).view(torch.bfloat16)
         else:
-            partial = torch.zeros((0, w.H), dtype=torch.bfloat16)
-        out = ep.combine(plan, rcv, partial, hi - lo)
-        ref = oracle.moe_forward(x, ids, wts, Wh, num_valid_rows=w.nvr)[lo:hi]
+            y_rows = torch.zeros((0, w.H), dtype=torch.bfloat16)
+        out, back_bytes = ep.combine(plan, rcv, rt, y_rows, wtsl, hi - lo)
+        ref = oracle.moe_forward(x, ids, wts, Wh, num_valid_rows=w.nvr, y_format="mxfp8")[lo:hi]
         got = out.view(torch.int16).numpy().view(np.uint16)
         c = compare(got, ref)
+        c["exact"] = bool(np.array_equal(got, ref))
+        c["wire"] = (rcv.wire_bytes_per_row, back_bytes)
         zero_rows_ok = bool(np.all(got[nv_local:] == 0))
         # runtime choice: the same answer on every rank, from the largest local count
         biggest = max(cut, w.T - cut)
@@ -87,10 +93,15 @@ def test_ep_dispatch_combine_two_gloo_ranks(cut):
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
+    H, K = 256, 3
     for rank in range(2):
         _, c, zero_ok, small, large, sent, recv = res[rank]
         assert isinstance(c, dict), c
         assert c["nan"] == 0 and c["rel_l2"] <= 1e-2 and c["bad"] == 0, (rank, c)
+        assert c["exact"], (rank, c)
+        # dispatch: H E4M3 codes + H/32 E8M0 scales + K int32 slot ids per row; combine: codes + scales
+        # + an 8-byte (position, slot) tag per GEMM2 row (a BF16 row alone would be 2H bytes)
+        assert c["wire"] == (H + H // 32 + 4 * K, H + H // 32 + 8), c["wire"]
         assert zero_ok
         assert small == "decode" and large == "large"
     # what rank a sends to rank b is what b receives from a
@@ -131,7 +142,8 @@ def _leaving_worker(rank, world, port, result_q):
         lo, hi = (0, 12) if rank == 0 else (12, 24)
         plan = ep.make_plan(torch.from_numpy(ids[lo:hi]), torch.from_numpy(wts[lo:hi]), w.E, world, rank)
         rcv = ep.dispatch(plan, x[lo:hi])                  # step 1, both ranks
-        ep.combine(plan, rcv, rcv.x, hi - lo)              # any BF16 rows stand in for the layer's
+        rt = ep.routes(rcv)
+        ep.combine(plan, rcv, rt, rt.x, torch.from_numpy(wts[lo:hi]), hi - lo)  # any rows stand in for the layer's
         if rank == 1:
             result_q.put((1, "left", 0.0))                 # leaves between steps
             _leave(result_q)
@@ -167,3 +179,22 @@ def test_rank_leaving_between_steps_is_detected():
     assert res[1][1] == "left", res
     assert res[0][1] not in ("no error",) and not res[0][1].startswith("setup"), res
     assert 0.0 <= res[0][2] < 60.0, res  # ended by the peer's closed connection or the 5 s timeout
+
+
+def test_mxfp8_rows_on_the_wire_are_exact():
+    """The wire format of the exchange: the OCP MX quantisation of BF16 rows equals the oracle's, and
+    dequantising then quantising again returns the same codes and scales (the receiving layer sees the
+    sender's quantised rows)."""
+    import oracle
+    from block_scaled_moe_gb300 import ep
+    oracle.build()
+    g = torch.Generator().manual_seed(3)
+    x = (torch.randn((37, 512), generator=g) * torch.logspace(-6, 6, 37)[:, None]).to(torch.bfloat16)
+    x[5, 64:96] = 0
+    x[6, :32] = -0.0
+    codes, scales = ep.mxfp8_rows(x)
+    oc, os_ = oracle.quant_mxfp8_rows(x)
+    assert np.array_equal(codes.numpy(), oc) and np.array_equal(scales.numpy(), os_)
+    back = ep.mxfp8_values(codes, scales).to(torch.bfloat16)
+    c2, s2 = ep.mxfp8_rows(back)
+    assert torch.equal(c2, codes) and torch.equal(s2, scales)
