@@ -30,15 +30,29 @@
 
 #ifdef BMOE_TRACE
 // Phase trace (tracing builds only): per CTA 32 int64 slots of globaltimer ns
-// stamps and counters, read back with bmoe_fused_trace_copy.
+// stamps and counters, read back with bmoe_fused_trace_copy; and per K stage of
+// CTAs 0 and 1, clock64 stamps [2 CTAs][6 events][4096 stages]: 0 producer got
+// a free stage, 1 producer issued it, 2 MMA chain 0 saw it full, 3 chain 0
+// issued, 4 weight-scale warp got it, 5 that warp filled it
+// (bmoe_fused_stage_trace_copy).
 __device__ long long g_fused_trace[1024 * 32];
+constexpr int kFusedTraceStages = 4096;
+__device__ long long g_fused_stage_trace[2 * 6 * kFusedTraceStages];
 #define FTRACE(ev, val)                                              \
     do {                                                             \
         if (blockIdx.x < 1024) g_fused_trace[blockIdx.x * 32 + (ev)] = (val); \
     } while (0)
+#define FSTRACE(ev, idx)                                                                         \
+    do {                                                                                         \
+        if (blockIdx.x < 2 && (idx) < kFusedTraceStages)                                          \
+            g_fused_stage_trace[(blockIdx.x * 6 + (ev)) * kFusedTraceStages + (idx)] = clock64(); \
+    } while (0)
 #else
 #define FTRACE(ev, val) \
     do {                \
+    } while (0)
+#define FSTRACE(ev, idx) \
+    do {                 \
     } while (0)
 #endif
 
@@ -63,6 +77,7 @@ constexpr int F_ACC_COLS = F_MW * F_NT;
 constexpr int F_SF_SLOT = 8;                                // [weight atom | row atom] of the chain's chunk
 constexpr int F_SF_BASE = 512 - F_MW * 2 * F_SF_SLOT;       // two slots per chain (alternating stages)
 constexpr int F_NUM_ACC = 2;
+constexpr bool kUnitPrefetch = true;  // L2 prefetch of each unit's first weight box one unit ahead
 constexpr int F_BAR_BYTES = (2 * F_STAGES + 2 * 2 + 1) * 8 + 16;
 constexpr int F_SMEM = 1024 + F_STAGES * F_STAGE_BYTES + F_TAB_BYTES + F_BAR_BYTES;
 static_assert(4 * F_SCR_INTS <= F_STAGES * F_STAGE_BYTES, "phase-0 scratch");
@@ -206,6 +221,7 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
 #ifdef BMOE_TRACE
         const long long tw1 = (long long)globaltimer_ns();
         wait_ns += tw1 - tw0;
+        if (threadIdx.x == 0) FSTRACE(0, issued);
 #else
         (void)wait_ns;
         (void)issue_ns;
@@ -232,6 +248,7 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
         }
 #ifdef BMOE_TRACE
         issue_ns += (long long)globaltimer_ns() - tw1;
+        if (threadIdx.x == 0) FSTRACE(1, issued);
 #endif
         ++issued;
         r.next();
@@ -260,6 +277,7 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
 #ifdef BMOE_TRACE
         const long long tw1 = (long long)globaltimer_ns();
         wait_ns += tw1 - tw0;
+        if (w == 0 && lane == 0) FSTRACE(2, job);
 #else
         (void)wait_ns;
         (void)issue_ns;
@@ -293,6 +311,7 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
             tc_commit_w(&p.empty[r.stage]);
 #ifdef BMOE_TRACE
             issue_ns += (long long)globaltimer_ns() - tw1;
+            if (w == 0 && lane == 0) FSTRACE(3, job);
 #endif
         }
         __syncwarp();
@@ -614,9 +633,21 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 long long ew1 = 0, ew2 = 0;  // empty-stage wait ns in GEMM1 / GEMM2 units (tracing builds)
                 long long pi1 = 0, pi2 = 0;  // issue ns
                 fence_proxy_async_all();  // phase-0 rows and scale atoms are read through the async proxy
+                FCursor pcur;             // one unit ahead: the next unit's first weight box is prefetched to L2
                 for (int ui = 0; ui < my_units && ok; ++ui) {
                     const FUnit fu = fused_unit(blockIdx.x + ui * gridDim.x, U1, cur, pl, mt1, mt2);
                     const UnitInfo& cu = fu.u;
+                    if (kUnitPrefetch && ui + 1 < my_units) {
+                        // a unit's first loads start in weight rows no CTA has touched yet; fetching its first
+                        // box one unit early takes that latency off the stage ring
+                        const FUnit nu = fused_unit(blockIdx.x + (ui + 1) * gridDim.x, U1, pcur, pl, mt1, mt2);
+                        if (!nu.g2)
+                            tma_prefetch_4d_w(&tm_w13p, 0, nu.u.m * 128, 0, nu.u.e);
+                        else if (f.kc2 == 2)
+                            tma_prefetch_3d_w(&tm_w2, 0, nu.u.e * H + nu.u.m * 128, 0);
+                        else
+                            tma_prefetch_2d_w(&tm_w2, 0, nu.u.e * H + nu.u.m * 128);
+                    }
                     if (!fu.g2) {
                         ok = produce_unit<false, 1>(p, ring, issued, &tm_w13p, &tm_aq, cu.m * 128, cu.e, cu.row0,
                                                     ws.as + (size_t)cu.g * kt1 * 512, kt1, pol_w, pol_b, ew1, pi1);
@@ -743,6 +774,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             uint4 cur[2][4], nxt[2][4];
             int clen = load_group(cur);
             Ring ring;
+            long sjob = 0;
             bool ok = true;
             while (clen > 0 && ok) {
                 const int nlen = load_group(nxt);
@@ -753,6 +785,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                                        kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs)) {
                             ok = false;
                         } else {
+                            if (lane == 0) FSTRACE(4, sjob);
                             uint4* dst = reinterpret_cast<uint4*>(sSFA + (ring.stage * 2) * 512) + lane;
                             dst[0] = make_uint4(word(cur[0][0], j), word(cur[0][1], j), word(cur[0][2], j),
                                                 word(cur[0][3], j));
@@ -760,6 +793,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                                                  word(cur[1][3], j));
                             fence_proxy_async_smem();
                             mbar_arrive(&full[ring.stage]);
+                            if (lane == 0) FSTRACE(5, sjob);
+                            ++sjob;
                             ring.next();
                         }
                     }
@@ -948,5 +983,9 @@ cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaun
 #ifdef BMOE_TRACE
 extern "C" int bmoe_fused_trace_copy(void* dst, size_t bytes) {
     return static_cast<int>(cudaMemcpyFromSymbol(dst, g_fused_trace, bytes < sizeof(g_fused_trace) ? bytes : sizeof(g_fused_trace)));
+}
+extern "C" int bmoe_fused_stage_trace_copy(void* dst, size_t bytes) {
+    return static_cast<int>(cudaMemcpyFromSymbol(
+        dst, g_fused_stage_trace, bytes < sizeof(g_fused_stage_trace) ? bytes : sizeof(g_fused_stage_trace)));
 }
 #endif

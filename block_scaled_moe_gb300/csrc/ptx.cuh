@@ -160,6 +160,22 @@ __device__ __forceinline__ void bulk_load_w(void* dst, const void* src, uint32_t
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
+// L2 prefetch of one tensor box (no shared memory, no barrier), warp-level like the loads.
+__device__ __forceinline__ void tma_prefetch_2d_w(const CUtensorMap* map, int c0, int c1) {
+    asm volatile(BMOE_ELECT_ISSUE("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}]")
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_3d_w(const CUtensorMap* map, int c0, int c1, int c2) {
+    asm volatile(BMOE_ELECT_ISSUE("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}]")
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_4d_w(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+    asm volatile(BMOE_ELECT_ISSUE("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}]")
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -82,6 +82,39 @@ def fused_trace(lib, n_sms: int) -> np.ndarray:
     return buf.reshape(1024, 32)[:n_sms]
 
 
+FUSED_STAGES = 4096
+
+
+def fused_stage_trace(lib) -> np.ndarray:
+    """[2 CTAs][6][4096] clock64 per K stage: 0 producer got a free stage, 1 issued it, 2 MMA chain 0 saw it
+    full, 3 chain 0 issued, 4 weight-scale warp got it, 5 that warp filled it."""
+    buf = np.zeros(2 * 6 * FUSED_STAGES, np.int64)
+    lib.bmoe_fused_stage_trace_copy.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    rc = lib.bmoe_fused_stage_trace_copy(buf.ctypes.data, buf.nbytes)
+    if rc:
+        raise RuntimeError(f"bmoe_fused_stage_trace_copy failed ({rc})")
+    return buf.reshape(2, 6, FUSED_STAGES)
+
+
+def summarize_fused_stages(st: np.ndarray, n_g1: int) -> list:
+    """Per-stage medians of CTA 0, GEMM1 stages [0, n_g1) and GEMM2 stages after them (cycles)."""
+    lines = []
+    s = st[0].astype(np.float64)
+    n = int((s[3] > 0).sum())
+    for name, lo, hi in (("GEMM1", 1, min(n_g1, n)), ("GEMM2", n_g1 + 1, n)):
+        if hi - lo < 4:
+            continue
+        sl = slice(lo, hi)
+        P0, P1, M0, M1, S0, S1 = (s[i] for i in range(6))
+        lines.append(f"  CTA 0 {name} stages {lo}..{hi} (cycles, median): producer wait for a free stage "
+                     f"{np.median(P0[sl] - P1[lo - 1:hi - 1]):.0f}, load latency issue->full "
+                     f"{np.median(M0[sl] - P1[sl]):.0f}, scale warp fills {np.median(S1[sl] - P1[sl]):.0f} after the "
+                     f"issue, MMA chain 0 wait {np.median(M0[sl] - M1[lo - 1:hi - 1]):.0f}, issue "
+                     f"{np.median(M1[sl] - M0[sl]):.0f}, stage period {np.median(np.diff(M0[lo - 1:hi])):.0f} "
+                     f"(mean {np.mean(np.diff(M0[lo - 1:hi])):.0f})")
+    return lines
+
+
 def summarize_fused(t: np.ndarray) -> list:
     t = t.astype(np.float64)
     base = t[:, 0].min()
@@ -100,6 +133,7 @@ def main(argv=None) -> int:
     p = argparse.ArgumentParser()
     p.add_argument("workload")
     p.add_argument("--path", default="auto", choices=["auto", "fused", "multi"])
+    p.add_argument("--save", default="", help="also write the raw stamps to this .npz file")
     args = p.parse_args(argv)
     if os.environ.get("BMOE_LIB_VARIANT") != "trace":
         print("run with BMOE_LIB_VARIANT=trace (the tracing build)", file=sys.stderr)
@@ -131,10 +165,16 @@ def main(argv=None) -> int:
     n_sms = torch.cuda.get_device_properties(0).multi_processor_count
     print(f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} top-{w.K} nvr={w.nvr}, path {L.last_path}, status {status:#x}")
     if L.last_path == "fused":
-        lines = summarize_fused(fused_trace(lib, n_sms))
+        ft = fused_trace(lib, n_sms)
+        fs = fused_stage_trace(lib)
+        lines = summarize_fused(ft) + summarize_fused_stages(fs, int(ft[0, 11]) * (w.H // 128))
+        raw = {"fused_phases": ft, "fused_stages": fs}
     else:
         t = gemm_trace(lib, n_sms)
         lines = summarize_gemm("GEMM1", t["gemm1"]) + summarize_gemm("GEMM2", t["gemm2"])
+        raw = {f"{g}_{k}": v for g, d in t.items() for k, v in d.items()}
+    if args.save:
+        np.savez(args.save, **raw)
     print("\n".join(lines))
     L.close()
     return 0 if status == 0 else 1
