@@ -92,3 +92,24 @@ def test_dispatch_fuzz(seed):
                 assert np.array_equal(L.debug_array("occ").reshape(E, -1), df["occ"]), tag
                 assert np.array_equal(L.debug_array("route_slot").reshape(T, K), df["route_slot"]), tag
             del L
+
+
+@pytest.mark.parametrize("E", [3072, 4096])
+def test_compact_dispatch_many_experts(E):
+    """The largest expert counts a handle accepts: the compact dispatch's count kernel keeps 4E+2 int32 in
+    shared memory (above the default 48 KB from E = 3072); counts, offsets, packed order and slot map
+    equal the oracle's, and the forward is within tolerance (H = I = 128)."""
+    T, K = 700, 8
+    w = synth.micro(T, 128, 128, E, K, nvr=650, invalid_frac=0.05, seed=E % 97, dispatch="compact")
+    c = Case(w)
+    L = c.layer(dispatch="compact", debug=True)
+    got = torch_bf16_bits(c.run(L))
+    torch.cuda.synchronize()
+    d = oracle.dispatch_compact(c.ids, E, w.nvr)
+    assert np.array_equal(L.debug_array("counts"), d["counts"])
+    assert np.array_equal(L.debug_array("offsets"), d["offsets"])
+    R = int(d["offsets"][-1])
+    assert np.array_equal(L.debug_array("perm")[:R], d["perm"])
+    assert np.array_equal(L.debug_array("route_row").reshape(T, K), d["route_row"])
+    assert_close(got, c.oracle(), f"E={E}")
+    assert L.read_status() == 0
