@@ -467,10 +467,12 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
         fl.T = T;
         mark(1);
         mark(2);
-        // 256-wide GEMM2 K stages (I % 256 == 0) read W2 and h through the two-chunk views
-        const bool k2 = g.I % 256 == 0;
-        e = bmoe::launch_fused(g, ws, fl, &wb.tm_w13p, &h->tm_aq, k2 ? &wb.tm_w2k2 : &wb.tm_w2,
-                               k2 ? &h->tm_hqk2 : &h->tm_hq, h->num_sms, s);
+        // GEMM2 takes W2 tiles in pairs (H % 256 == 0: the 256-row W2 boxes, 128-wide K stages); else
+        // 256-wide K stages (I % 256 == 0) read W2 and h through the two-chunk views
+        const bool w2w = g.H % 256 == 0, k2 = !w2w && g.I % 256 == 0;
+        e = bmoe::launch_fused(g, ws, fl, &wb.tm_w13p, &h->tm_aq,
+                               w2w ? &wb.tm_w2w : (k2 ? &wb.tm_w2k2 : &wb.tm_w2), k2 ? &h->tm_hqk2 : &h->tm_hq,
+                               h->num_sms, s);
         if (e == cudaErrorCooperativeLaunchTooLarge && h->opt_path != MOE_PATH_FUSED) {
             // the driver could not make the grid co-resident (fewer SMs available to this context than
             // the device reports): nothing was enqueued; take the multi-kernel path from now on
@@ -550,8 +552,8 @@ int moe_forward(moe_handle h, const void* x, const int32_t* topk_ids, const floa
     h->launches += 1;
     mark(3);
     // GEMM2: W2 x h rows, K = I
-    // prefill route tiles take W2 tiles in pairs (one 256-row box, two accumulator chains)
-    const bool w2_pairs = g.NT >= 128 && g.H % 256 == 0;
+    // W2 tiles go in pairs when H allows it (one 256-row box, alternate accumulator chains per tile)
+    const bool w2_pairs = g.H % 256 == 0;
     a.w_sf = wb.w2s;
     a.w_rows = g.H;
     a.ld_sf = g.I / 32;

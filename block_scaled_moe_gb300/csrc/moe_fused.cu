@@ -93,7 +93,8 @@ struct FusedArgs {
     const uint8_t* w2s;
     int I;
     int w13_rs, w13_up;    // W13 scale rows: gate j at j * w13_rs, up j at j * w13_rs + w13_up
-    int kc2;               // K chunks per GEMM2 stage (2 when I % 256 == 0)
+    int kc2;               // K chunks per GEMM2 stage of single W2 tiles (2 when I % 256 == 0)
+    int w2w;               // GEMM2 units take W2 tiles in pairs (H % 256 == 0): one 256-row box per 128-wide K stage
     uint8_t* y8;           // GEMM2 rows as MXFP8 codes / scales (nullptr: BF16 rows in ws.y)
     uint8_t* ys;
     int nchunks;           // compact dispatch chunks
@@ -205,8 +206,10 @@ struct Ring {
 // TMA producer, one unit of kt K stages.  GEMM1 (G2 false): the gate and up chunks of weight
 // tile m of expert e (one box of the W13 pair view, coordinates (k, m*128, 0, e)), one row
 // chunk and its scale atom per stage; GEMM2: KC (W2 chunk, h chunk) pairs and KC h-scale
-// atoms per stage (W2 rows from wrow).  The row-scale atoms of the unit start at bsf.
-template <bool G2, int KC>
+// atoms per stage (W2 rows from wrow), or, for paired W2 tiles (PAIR2), one 256-row W2 box
+// (both tiles, back to back like GEMM1's gate and up chunks), one h chunk and its atom per
+// stage.  The row-scale atoms of the unit start at bsf.
+template <bool G2, int KC, bool PAIR2 = false>
 __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued, const CUtensorMap* tw,
                                              const CUtensorMap* tb, int wrow, int e, int row0,
                                              const uint8_t* bsf, int kt, uint64_t pol_w, uint64_t pol_b,
@@ -233,6 +236,11 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
         if constexpr (!G2) {
             mbar_arrive_expect_tx_w(fb, 2 * F_A_TX + F_B_BYTES + 512);
             tma_load_4d_w(a0, tw, fb, kk * 128, wrow, 0, e, pol_w);
+            tma_load_2d_w(b0, tb, fb, kk * 128, row0, pol_b);
+            bulk_load_w(p.sSFB + (r.stage * 2) * 512, bsf + static_cast<size_t>(kk) * 512, 512, fb);
+        } else if constexpr (PAIR2) {
+            mbar_arrive_expect_tx_w(fb, 2 * F_A_TX + F_B_BYTES + 512);
+            tma_load_2d_w(a0, tw, fb, kk * 128, wrow, pol_w);
             tma_load_2d_w(b0, tb, fb, kk * 128, row0, pol_b);
             bulk_load_w(p.sSFB + (r.stage * 2) * 512, bsf + static_cast<size_t>(kk) * 512, 512, fb);
         } else {
@@ -326,13 +334,17 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
 // bits.  GEMM1: gate/up -> optional clamp -> SwiGLU -> MXFP8 per 32 features (OCP MX rule)
 // into the h rows and their scale atom, then this warp's share of tile g is released to the
 // GEMM2 units; GEMM2: BF16 rows of y.  The accumulator is handed back before the stores.
-template <bool G2>
+// GEMM2 with paired W2 tiles (PAIR2): chains 0 / 2 hold the first tile, 1 / 3 the second (like GEMM1's
+// gate and up), summed in the same order; the unit's rows are features m*256 + f and m*256 + 128 + f.
+// These are stored as each 16-column slice is read (the pair's 64 values per lane do not fit the
+// register budget), so the accumulator goes back after the stores are issued.
+template <bool G2, bool PAIR2 = false>
 __device__ __forceinline__ void epilogue_unit(const P1& p, uint64_t* acce_b, const Workspace& ws, const UnitInfo& cu,
                                               int acc, int qd, int lane, int I, int H, float L, uint8_t* y8,
                                               uint8_t* ys) {
     const uint32_t tb = p.tmem + (static_cast<uint32_t>(32 * qd) << 16) + static_cast<uint32_t>(acc * F_ACC_COLS);
-    const int feat = cu.m * 128 + 32 * qd + lane;
-    float v[F_NT];
+    const int feat = cu.m * (PAIR2 ? 256 : 128) + 32 * qd + lane;
+    float v[PAIR2 ? 1 : F_NT];
 #pragma unroll
     for (int j = 0; j < F_NT / 16; ++j) {
         const int c0 = 16 * j;
@@ -346,7 +358,7 @@ __device__ __forceinline__ void epilogue_unit(const P1& p, uint64_t* acce_b, con
                 float ga = 0.f, ub = 0.f;
 #pragma unroll
                 for (int w = 0; w < F_MW; ++w) {
-                    if (!G2 && (w & 1))
+                    if ((!G2 || PAIR2) && (w & 1))
                         ub += __uint_as_float(r[w][i]);
                     else
                         ga += __uint_as_float(r[w][i]);
@@ -362,6 +374,20 @@ __device__ __forceinline__ void epilogue_unit(const P1& p, uint64_t* acce_b, con
                         ub = fminf(fmaxf(ub, -L), L);
                     }
                     v[c0 + i] = __fdividef(ga, 1.0f + __expf(-ga)) * ub;  // SwiGLU, fast exp / divide intrinsics
+                } else if constexpr (PAIR2) {
+                    if (c0 + i < cu.n) {
+                        const size_t prow = static_cast<size_t>(cu.row0 + c0 + i);
+                        if (y8) {  // MXFP8 GEMM2 rows: this warp's 32 features of each tile are one 1x32 block
+                            uint8_t sc;
+                            y8[prow * H + feat] = rows::quant_block_warp(ga, &sc);
+                            if (lane == 0) ys[prow * (H >> 5) + (feat >> 5)] = sc;
+                            y8[prow * H + feat + 128] = rows::quant_block_warp(ub, &sc);
+                            if (lane == 0) ys[prow * (H >> 5) + ((feat + 128) >> 5)] = sc;
+                        } else {
+                            ws.y[prow * H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(ga));
+                            ws.y[prow * H + feat + 128] = __bfloat16_as_ushort(__float2bfloat16_rn(ub));
+                        }
+                    }
                 } else {
                     v[c0 + i] = ga;
                 }
@@ -370,6 +396,7 @@ __device__ __forceinline__ void epilogue_unit(const P1& p, uint64_t* acce_b, con
     }
     tc_fence_before();
     mbar_arrive(acce_b);
+    if constexpr (PAIR2) return;
     if (G2 && y8) {  // MXFP8 GEMM2 rows: this warp's 32 features are one 1x32 block
 #pragma unroll
         for (int c = 0; c < F_NT; ++c) {
@@ -569,7 +596,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     // ------------------------------------------------------------------ phase 1: GEMM1 + GEMM2
     {
         const int ntiles = t_tile[E];
-        const int mt1 = I / 128, mt2 = H / 128;
+        const int mt1 = I / 128, mt2 = H / (f.w2w ? 256 : 128);
         const int U1 = ntiles * mt1, U = U1 + ntiles * mt2;
 #ifdef MOE_DEBUG_BOUNDS
         const int all_units =
@@ -578,7 +605,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
 #endif
             static_cast<int>(blockIdx.x) < U ? (U - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
                                              : 0;
-        const int kt1 = H / 128, kt2 = I / (128 * f.kc2), ktot2 = I / 128;
+        const int kt1 = H / 128, kt2 = f.w2w ? I / 128 : I / (128 * f.kc2), ktot2 = I / 128;
         const Plan pl{t_tile, t_row, t_cnt};
 #ifdef MOE_DEBUG_BOUNDS
         FCursor chk_cur;
@@ -643,6 +670,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                         const FUnit nu = fused_unit(blockIdx.x + (ui + 1) * gridDim.x, U1, pcur, pl, mt1, mt2);
                         if (!nu.g2)
                             tma_prefetch_4d_w(&tm_w13p, 0, nu.u.m * 128, 0, nu.u.e);
+                        else if (f.w2w)
+                            tma_prefetch_2d_w(&tm_w2, 0, nu.u.e * H + nu.u.m * 256);
                         else if (f.kc2 == 2)
                             tma_prefetch_3d_w(&tm_w2, 0, nu.u.e * H + nu.u.m * 128, 0);
                         else
@@ -679,12 +708,14 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                     }
 #endif
                     fence_proxy_async_all();
-                    const int wrow = cu.e * H + cu.m * 128;
+                    const int wrow = cu.e * H + cu.m * (f.w2w ? 256 : 128);
                     const uint8_t* bsf = ws.hs + (size_t)cu.g * ktot2 * 512;
-                    ok = f.kc2 == 2 ? produce_unit<true, 2>(p, ring, issued, &tm_w2, &tm_hq, wrow, 0, cu.row0, bsf,
-                                                            kt2, pol_w, pol_b, ew2, pi2)
-                                    : produce_unit<true, 1>(p, ring, issued, &tm_w2, &tm_hq, wrow, 0, cu.row0, bsf,
-                                                            kt2, pol_w, pol_b, ew2, pi2);
+                    ok = f.w2w ? produce_unit<true, 1, true>(p, ring, issued, &tm_w2, &tm_hq, wrow, 0, cu.row0, bsf,
+                                                             kt2, pol_w, pol_b, ew2, pi2)
+                         : f.kc2 == 2 ? produce_unit<true, 2>(p, ring, issued, &tm_w2, &tm_hq, wrow, 0, cu.row0, bsf,
+                                                              kt2, pol_w, pol_b, ew2, pi2)
+                                      : produce_unit<true, 1>(p, ring, issued, &tm_w2, &tm_hq, wrow, 0, cu.row0, bsf,
+                                                              kt2, pol_w, pol_b, ew2, pi2);
                 }
 #ifdef BMOE_TRACE
                 FTRACE(4, wait_ns);
@@ -699,15 +730,17 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         } else if (warp == 1) {
             // -------------------------------------------------------- weight-scale producer (32 lanes)
             // Lane l writes, per stage, line l of two 128x4 scale atoms (GEMM1: gate and up rows;
-            // GEMM2: two K chunks): the 4 K-block bytes of rows l, l+32, l+64, l+96.  Stages are
+            // GEMM2: the two W2 tiles of a pair, or two K chunks of one tile): the 4 K-block bytes
+            // of rows l, l+32, l+64, l+96.  Stages are
             // handled in groups of up to 4 of one unit, loaded one group ahead into registers
             // (component j of each uint4 = stage j).  GEMM1 rows whose scale stride is a multiple
             // of 16 bytes take one 16-byte load per row and group: the weight-scale lines then need
             // not stay in L1, which this kernel's shared-memory footprint leaves small.
             const bool g1_vec = (H % 512) == 0;
-            const bool g2_pair = f.kc2 == 2 && (I / 32) % 8 == 0;  // 8-byte aligned scale rows
-            int q_ui = 0, q_kk = 0, q_kt = 0, q_ld = 0, q_rs = 1;
-            bool q_g2 = false;
+            const bool g2w_vec = f.w2w && (I % 512) == 0;           // paired W2 tiles: 16-byte scale vectors
+            const bool g2_pair = !f.w2w && f.kc2 == 2 && (I / 32) % 8 == 0;  // 8-byte aligned scale rows
+            int q_ui = 0, q_kk = 0, q_kt = 0, q_ld = 0, q_rs = 1, q_up = 0;
+            bool q_g2 = false, q_two = false, q_vec = false;  // q_two: the two atoms are two tiles' rows
             const uint8_t* q_base = nullptr;
             FCursor qcur;
             auto load_group = [&](uint4(&g)[2][4]) -> int {
@@ -718,18 +751,21 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                     q_kt = fu.g2 ? kt2 : kt1;
                     q_ld = fu.g2 ? I / 32 : H / 32;
                     q_rs = fu.g2 ? 1 : f.w13_rs;
-                    const int rrow = fu.g2 ? fu.u.e * H + fu.u.m * 128 + lane
+                    q_two = !fu.g2 || f.w2w;
+                    q_up = fu.g2 ? 128 : f.w13_up;
+                    q_vec = fu.g2 ? g2w_vec : g1_vec;
+                    const int rrow = fu.g2 ? fu.u.e * H + fu.u.m * (f.w2w ? 256 : 128) + lane
                                            : fu.u.e * 2 * I + (fu.u.m * 128 + lane) * f.w13_rs;
                     q_base = (fu.g2 ? f.w2s : f.w13s) + static_cast<size_t>(rrow) * q_ld;
                 }
                 const int len = min(4, q_kt - q_kk);
-                if (!q_g2 && g1_vec) {
+                if (q_two && q_vec) {
 #pragma unroll
                     for (int a4 = 0; a4 < 2; ++a4)
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             g[a4][i] = __ldg(reinterpret_cast<const uint4*>(
-                                q_base + static_cast<size_t>(a4 * f.w13_up + 32 * i * q_rs) * q_ld + q_kk * 4));
+                                q_base + static_cast<size_t>(a4 * q_up + 32 * i * q_rs) * q_ld + q_kk * 4));
                 } else if (q_g2 && g2_pair) {
                     // 256-wide GEMM2 stages: the two K chunks' words of a row are one 8-byte pair
 #pragma unroll
@@ -746,15 +782,15 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 } else {
 #pragma unroll
                     for (int a4 = 0; a4 < 2; ++a4) {
-                        const bool use = !q_g2 || a4 < f.kc2;
+                        const bool use = q_two || a4 < f.kc2;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             uint32_t w4[4];
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const int kk = q_kk + j;
-                                const uint8_t* src = q_g2 ? q_base + (kk * f.kc2 + a4) * 4
-                                                          : q_base + static_cast<size_t>(a4 * f.w13_up) * q_ld + kk * 4;
+                                const uint8_t* src = !q_two ? q_base + (kk * f.kc2 + a4) * 4
+                                                            : q_base + static_cast<size_t>(a4 * q_up) * q_ld + kk * 4;
                                 w4[j] = (use && j < len) ? __ldg(reinterpret_cast<const uint32_t*>(
                                                                src + static_cast<size_t>(32 * i * q_rs) * q_ld))
                                                          : 0u;
@@ -832,7 +868,9 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 (fu.g2 ? aw2 : aw1) += (long long)globaltimer_ns() - ta0;
 #endif
                 tc_fence_after();
+                // paired W2 tiles issue like GEMM1's gate / up pair: chain w takes tile w & 1
                 const bool ok = !fu.g2       ? mma_unit<false, 1>(p, ring, job, w, lane, d_tmem, N, kt1, fw1, mi1)
+                                : f.w2w      ? mma_unit<false, 1>(p, ring, job, w, lane, d_tmem, N, kt2, fw2, mi2)
                                 : f.kc2 == 2 ? mma_unit<true, 2>(p, ring, job, w, lane, d_tmem, N, kt2, fw2, mi2)
                                              : mma_unit<true, 1>(p, ring, job, w, lane, d_tmem, N, kt2, fw2, mi2);
                 if (!ok) break;
@@ -877,6 +915,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
 #endif
                 if (!fu.g2)
                     epilogue_unit<false>(p, &acce[acc], ws, fu.u, acc, qd, lane, I, H, L, f.y8, f.ys);
+                else if (f.w2w)
+                    epilogue_unit<true, true>(p, &acce[acc], ws, fu.u, acc, qd, lane, I, H, L, f.y8, f.ys);
                 else
                     epilogue_unit<true>(p, &acce[acc], ws, fu.u, acc, qd, lane, I, H, L, f.y8, f.ys);
                 acc ^= 1;
@@ -962,6 +1002,7 @@ cudaError_t launch_fused(const Geometry& g, const Workspace& ws, const FusedLaun
     f.y8 = fl.y8;
     f.ys = fl.ys;
     f.kc2 = g.I % 256 == 0 ? 2 : 1;
+    f.w2w = g.H % 256 == 0 ? 1 : 0;
     f.nchunks = (fl.T * g.K + kChunk - 1) / kChunk;
     f.tiles_cap = static_cast<int>(g.tiles_cap);
     f.swiglu_limit = fl.swiglu_limit;

@@ -95,7 +95,7 @@ struct Cfg {
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(4 % KS == 0, "K-steps per stage must split evenly");
     static_assert(!G1 || KC == 1, "GEMM1 stages hold one K chunk (the W13 pair box)");
-    static_assert(!WIDE || (!G1 && NT >= 128 && KC == 1), "wide units: GEMM2, prefill route tiles");
+    static_assert(!WIDE || (!G1 && KC == 1), "wide units: GEMM2 with one K chunk per stage");
     static_assert(!ROT3 || (MW == 2 && NI == 2 && 3 * NT <= SF_BASE), "three rotating slots");
     static_assert(MW <= 4, "barrier slots");
     static_assert(CW % 8 == 0, "epilogue column split");
@@ -549,6 +549,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
             const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
             const int feat = cu.m * 128 + 32 * q + lane;
             float v[CW];  // GEMM1: h = SwiGLU(gate, up); GEMM2: y
+            float v2[WIDE && !C::ROT3 ? CW : 1];  // GEMM2 wide units without rotating slots: the second tile's y
             if constexpr (C::ROT3) {
                 // chain by chain from its rotating slot; each slot is freed as soon as it is drained
                 bool ok = true;
@@ -641,7 +642,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                             float ga = 0.f, ub = 0.f;
 #pragma unroll
                             for (int w = 0; w < MW; ++w) {
-                                if (G1 && (w & 1))
+                                if (PAIR && (w & 1))
                                     ub += __uint_as_float(r[w][i]);
                                 else
                                     ga += __uint_as_float(r[w][i]);
@@ -663,7 +664,10 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                             for (int i = 0; i < LDC; ++i) v[LDC * j + i] = swiglu(gav[i], ubv[i], clamp, L);
                         } else {
 #pragma unroll
-                            for (int i = 0; i < LDC; ++i) v[LDC * j + i] = gav[i];
+                            for (int i = 0; i < LDC; ++i) {
+                                v[LDC * j + i] = gav[i];
+                                if constexpr (WIDE) v2[LDC * j + i] = ubv[i];  // the pair's second W2 tile
+                            }
                         }
                     }
                 }
@@ -676,6 +680,27 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
                 } else {
                     acc_phase ^= 1u;
                 }
+            }
+            if constexpr (WIDE && !C::ROT3) {  // two W2 tiles: rows of features m*256 + f and m*256 + 128 + f
+                const int featw = cu.m * a.m_rows + 32 * q + lane;
+                if (a.y8) {
+#pragma unroll
+                    for (int j = 0; j < CW; ++j) {
+                        const int c = cbase + j;
+                        if (c < cu.n) {
+                            const size_t prow = static_cast<size_t>(cu.row0 + c);
+                            uint8_t sc;
+                            a.y8[prow * a.H + featw] = rows::quant_block_warp(v[j], &sc);
+                            if (lane == 0) a.ys[prow * (a.H >> 5) + (featw >> 5)] = sc;
+                            a.y8[prow * a.H + featw + 128] = rows::quant_block_warp(v2[j], &sc);
+                            if (lane == 0) a.ys[prow * (a.H >> 5) + ((featw + 128) >> 5)] = sc;
+                        }
+                    }
+                } else {
+                    store_rows_bf16<CW>(a.y, v, cu.row0 + cbase, cu.n - cbase, a.H, featw);
+                    store_rows_bf16<CW>(a.y, v2, cu.row0 + cbase, cu.n - cbase, a.H, featw + 128);
+                }
+                continue;
             }
             if (!G1 && a.y8) {  // MXFP8 GEMM2 rows: this warp's 32 features are one 1x32 block
 #pragma unroll
@@ -772,6 +797,7 @@ cudaError_t gemm_set_attributes() {
     if ((e = set_attr<true, 32, 1, false>()) != cudaSuccess) return e;
     if ((e = set_attr<false, 128, 1, false>()) != cudaSuccess) return e;
     if ((e = set_attr<false, 32, 1, false>()) != cudaSuccess) return e;
+    if ((e = set_attr<false, 32, 1, true>()) != cudaSuccess) return e;
     if ((e = set_attr<false, 128, 1, true>()) != cudaSuccess) return e;
     return set_attr<false, 32, 2, false>();
 }
@@ -786,10 +812,14 @@ cudaError_t launch_gemm1(const GemmArgs& a, const CUtensorMap* tm_w, const CUten
 cudaError_t launch_gemm2(const GemmArgs& a, const CUtensorMap* tm_w, const CUtensorMap* tm_w_wide,
                          const CUtensorMap* tm_w_k2, const CUtensorMap* tm_h, const CUtensorMap* tm_h_k2, int NT,
                          int grid, cudaStream_t s) {
-    // decode tiles stream W2 in 256-wide K stages when I allows it (halves the per-stage cost per byte),
-    // each operand's two K chunks in one box of its two-chunk view
-    if (NT == 32) return a.ktiles % 2 == 0 ? launch<false, 32, 2, false>(a, tm_w_k2, tm_h_k2, grid, s)
-                                           : launch<false, 32, 1, false>(a, tm_w, tm_h, grid, s);
+    // decode tiles: pairs of W2 tiles (a.m_rows == 256) when H allows it, else 256-wide K stages when I
+    // allows it (halves the per-stage cost per byte), each operand's two K chunks in one box of its
+    // two-chunk view
+    if (NT == 32) {
+        if (a.m_rows == 256) return launch<false, 32, 1, true>(a, tm_w_wide, tm_h, grid, s);
+        return a.ktiles % 2 == 0 ? launch<false, 32, 2, false>(a, tm_w_k2, tm_h_k2, grid, s)
+                                 : launch<false, 32, 1, false>(a, tm_w, tm_h, grid, s);
+    }
     // prefill route tiles: pairs of W2 tiles (a.m_rows == 256) when H allows it
     if (NT == 128)
         return a.m_rows == 256 ? launch<false, 128, 1, true>(a, tm_w_wide, tm_h, grid, s)
