@@ -53,20 +53,66 @@ struct Plan {
 // major and route tile j minor, so CTAs running consecutive units share a
 // weight tile (L2 reuse when an expert has several route tiles).  `ecur` only
 // moves forward because every role walks its units in increasing order.
-__device__ __forceinline__ UnitInfo decode_unit(int u, int& ecur, const Plan& pl, int mtiles, int NT) {
-    const int q = u / mtiles;
-    while (pl.tile_base[ecur + 1] <= q) ++ecur;
-    const int tb = pl.tile_base[ecur];
-    const int nt = pl.tile_base[ecur + 1] - tb;
+// Unit u of expert e (tile_base[e] <= u / mtiles < tile_base[e + 1]).
+__device__ __forceinline__ UnitInfo unit_of_expert(int u, int e, const Plan& pl, int mtiles, int NT) {
+    const int tb = pl.tile_base[e];
+    const int nt = pl.tile_base[e + 1] - tb;
     const int ul = u - tb * mtiles;
     UnitInfo r;
-    r.e = ecur;
+    r.e = e;
     r.m = ul / nt;
     const int j = ul - r.m * nt;
     r.g = tb + j;
-    r.row0 = pl.rowbase[ecur] + j * NT;
-    r.n = min(NT, pl.counts[ecur] - j * NT);
+    r.row0 = pl.rowbase[e] + j * NT;
+    r.n = min(NT, pl.counts[e] - j * NT);
     return r;
+}
+
+__device__ __forceinline__ UnitInfo decode_unit(int u, int& ecur, const Plan& pl, int mtiles, int NT) {
+    const int q = u / mtiles;
+    while (pl.tile_base[ecur + 1] <= q) ++ecur;
+    return unit_of_expert(u, ecur, pl, mtiles, NT);
+}
+
+// The expert of unit u by bisection of tile_base[0..E] (no cursor), for decoding a CTA's units once
+// up front: the cursor walk costs a dependent shared-memory load per expert passed, which under a
+// full stage ring adds up to a few thousand cycles per unit.
+__device__ __forceinline__ int expert_of_unit(int u, const Plan& pl, int mtiles, int E) {
+    const int q = u / mtiles;
+    int lo = 0, hi = E;  // tile_base[lo] <= q < tile_base[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pl.tile_base[mid] <= q)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Units of a CTA decoded once into shared memory before the pipeline starts (16 bytes each, up to
+// kUnitTab of them, fewer where the stage ring leaves less room); later units, if any, are decoded
+// with the role's cursor.
+constexpr int kUnitTab = 512;
+
+// A decoded unit in one 16-byte shared-memory word: {e, m | n << 16, g, row0}.
+__device__ __forceinline__ int4 pack_unit(const UnitInfo& r) { return make_int4(r.e, r.m | (r.n << 16), r.g, r.row0); }
+__device__ __forceinline__ UnitInfo unpack_unit(int4 v) {
+    UnitInfo r;
+    r.e = v.x;
+    r.m = v.y & 0xffff;
+    r.n = v.y >> 16;
+    r.g = v.z;
+    r.row0 = v.w;
+    return r;
+}
+
+// The CTA's unit number ui of a single unit list (GEMM units strided over the grid); the table
+// holds the first `ntab` units.
+__device__ __forceinline__ UnitInfo unit_ref(int ui, const int4* utab, int ntab, int& ecur, const Plan& pl, int mtiles,
+                                             int NT) {
+    if (ui < ntab) return unpack_unit(utab[ui]);
+    return decode_unit(static_cast<int>(blockIdx.x) + ui * static_cast<int>(gridDim.x), ecur, pl, mtiles, NT);
 }
 
 #ifdef MOE_DEBUG_BOUNDS

@@ -31,13 +31,18 @@
 #ifdef BMOE_TRACE
 // Phase trace (tracing builds only): per CTA 32 int64 slots of globaltimer ns
 // stamps and counters, read back with bmoe_fused_trace_copy; and per K stage of
-// CTAs 0 and 1, clock64 stamps [2 CTAs][6 events][4096 stages]: 0 producer got
+// CTAs 0 and 1, clock64 stamps [2 CTAs][16 events][4096 stages]: 0 producer got
 // a free stage, 1 producer issued it, 2 MMA chain 0 saw it full, 3 chain 0
-// issued, 4 weight-scale warp got it, 5 that warp filled it
-// (bmoe_fused_stage_trace_copy).
+// issued, 4 weight-scale warp got it, 5 that warp filled it, 6 producer began
+// waiting for it, 7 / 8 / 9 chains 1 / 2 / 3 issued, 10 chain 0 began waiting for
+// it, 11 chain 3 saw it full; per unit (index = the CTA's unit number): 12 producer
+// entered the unit, 13 producer decoded it, 14 producer issued its prefetch, 15 chain 0
+// decoded it (stamps 13 and 15 take an index that depends on the decoded unit, so that
+// they follow the decode) (bmoe_fused_stage_trace_copy).
 __device__ long long g_fused_trace[1024 * 32];
 constexpr int kFusedTraceStages = 4096;
-__device__ long long g_fused_stage_trace[2 * 6 * kFusedTraceStages];
+constexpr int kFusedStageEvents = 16;
+__device__ long long g_fused_stage_trace[2 * kFusedStageEvents * kFusedTraceStages];
 #define FTRACE(ev, val)                                              \
     do {                                                             \
         if (blockIdx.x < 1024) g_fused_trace[blockIdx.x * 32 + (ev)] = (val); \
@@ -45,7 +50,7 @@ __device__ long long g_fused_stage_trace[2 * 6 * kFusedTraceStages];
 #define FSTRACE(ev, idx)                                                                         \
     do {                                                                                         \
         if (blockIdx.x < 2 && (idx) < kFusedTraceStages)                                          \
-            g_fused_stage_trace[(blockIdx.x * 6 + (ev)) * kFusedTraceStages + (idx)] = clock64(); \
+            g_fused_stage_trace[(blockIdx.x * kFusedStageEvents + (ev)) * kFusedTraceStages + (idx)] = clock64(); \
     } while (0)
 #else
 #define FTRACE(ev, val) \
@@ -79,7 +84,9 @@ constexpr int F_SF_BASE = 512 - F_MW * 2 * F_SF_SLOT;       // two slots per cha
 constexpr int F_NUM_ACC = 2;
 constexpr bool kUnitPrefetch = true;  // L2 prefetch of each unit's first weight box one unit ahead
 constexpr int F_BAR_BYTES = (2 * F_STAGES + 2 * 2 + 1) * 8 + 16;
-constexpr int F_SMEM = 1024 + F_STAGES * F_STAGE_BYTES + F_TAB_BYTES + F_BAR_BYTES;
+constexpr int F_UTAB = kUnitTab;                            // a CTA's first units, decoded once (16 bytes each)
+constexpr int F_UTAB_OFF = (F_STAGES * F_STAGE_BYTES + F_TAB_BYTES + F_BAR_BYTES + 15) & ~15;
+constexpr int F_SMEM = 1024 + F_UTAB_OFF + F_UTAB * 16;
 static_assert(4 * F_SCR_INTS <= F_STAGES * F_STAGE_BYTES, "phase-0 scratch");
 static_assert(F_NUM_ACC * F_ACC_COLS <= F_SF_BASE, "TMEM columns");
 static_assert(F_SMEM <= 232448, "shared memory");
@@ -179,6 +186,18 @@ __device__ __forceinline__ FUnit fused_unit(int u, int U1, FCursor& c, const Pla
     return r;
 }
 
+// The CTA's unit number ui: from the table decoded before phase 1 (the first F_UTAB units), else
+// decoded here with the role's cursor.
+__device__ __forceinline__ FUnit unit_at(int ui, const int4* utab, int U1, FCursor& c, const Plan& pl, int mt1,
+                                         int mt2) {
+    const int u = static_cast<int>(blockIdx.x) + ui * static_cast<int>(gridDim.x);
+    if (ui >= F_UTAB) return fused_unit(u, U1, c, pl, mt1, mt2);
+    FUnit r;
+    r.g2 = u >= U1;
+    r.u = unpack_unit(utab[ui]);
+    return r;
+}
+
 // Phase-1 pipeline: the stage ring in shared memory and the TMEM base.
 struct P1 {
     uint8_t* sA;     // [stage][2] weight chunks
@@ -217,6 +236,7 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
     for (int kk = 0; kk < kt; ++kk) {
 #ifdef BMOE_TRACE
         const long long tw0 = (long long)globaltimer_ns();
+        if (threadIdx.x == 0) FSTRACE(6, issued);
 #endif
         const bool got = mbar_wait(&p.empty[r.stage], r.phase ^ 1u, p.abort_flag, p.status,
                                    kStTimeout | (1u << (kSiteShift + 0)), kWaitLimitNs);
@@ -278,6 +298,7 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
     for (int kk = 0; kk < kt; ++kk) {
 #ifdef BMOE_TRACE
         const long long tw0 = (long long)globaltimer_ns();
+        if (w == 0 && lane == 0) FSTRACE(10, job);
 #endif
         const bool got = mbar_wait(&p.full[r.stage], r.phase, p.abort_flag, p.status,
                                    kStTimeout | (1u << (kSiteShift + 3)), kWaitLimitNs);
@@ -286,6 +307,7 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
         const long long tw1 = (long long)globaltimer_ns();
         wait_ns += tw1 - tw0;
         if (w == 0 && lane == 0) FSTRACE(2, job);
+        if (w == 3 && lane == 0) FSTRACE(11, job);
 #else
         (void)wait_ns;
         (void)issue_ns;
@@ -319,7 +341,7 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
             tc_commit_w(&p.empty[r.stage]);
 #ifdef BMOE_TRACE
             issue_ns += (long long)globaltimer_ns() - tw1;
-            if (w == 0 && lane == 0) FSTRACE(3, job);
+            if (lane == 0) FSTRACE(w == 0 ? 3 : 6 + w, job);
 #endif
         }
         __syncwarp();
@@ -459,6 +481,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     uint64_t* drain = acce + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int4* utab = reinterpret_cast<int4*>(sm + F_UTAB_OFF);  // [F_UTAB] decoded units of this CTA
 
     const rows::QuantArgs& q = f.q;
     const Workspace& ws = q.ws;
@@ -613,6 +636,12 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             all_units, [&](int i) { return fused_unit(blockIdx.x + i * gridDim.x, U1, chk_cur, pl, mt1, mt2).u; },
             F_NT, ws.lim_rows, ws.lim_tiles, ws.status, ws.ticket);
 #endif
+        for (int i = threadIdx.x; i < min(my_units, F_UTAB); i += blockDim.x) {
+            const int u = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+            const bool g2 = u >= U1;
+            const int uu = g2 ? u - U1 : u, mt = g2 ? mt2 : mt1;
+            utab[i] = pack_unit(unit_of_expert(uu, expert_of_unit(uu, pl, mt, E), pl, mt, F_NT));
+        }
         if (threadIdx.x == 0) {
             for (int s = 0; s < F_STAGES; ++s) {
                 mbar_init(&full[s], 1 + 32);  // the producer's arrive.expect_tx + the scale warp's lanes
@@ -662,12 +691,14 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 fence_proxy_async_all();  // phase-0 rows and scale atoms are read through the async proxy
                 FCursor pcur;             // one unit ahead: the next unit's first weight box is prefetched to L2
                 for (int ui = 0; ui < my_units && ok; ++ui) {
-                    const FUnit fu = fused_unit(blockIdx.x + ui * gridDim.x, U1, cur, pl, mt1, mt2);
+                    if (threadIdx.x == 0) FSTRACE(12, ui);
+                    const FUnit fu = unit_at(ui, utab, U1, cur, pl, mt1, mt2);
                     const UnitInfo& cu = fu.u;
+                    if (threadIdx.x == 0) FSTRACE(13, ui + (cu.n > 1000 ? 1 : 0));
                     if (kUnitPrefetch && ui + 1 < my_units) {
                         // a unit's first loads start in weight rows no CTA has touched yet; fetching its first
                         // box one unit early takes that latency off the stage ring
-                        const FUnit nu = fused_unit(blockIdx.x + (ui + 1) * gridDim.x, U1, pcur, pl, mt1, mt2);
+                        const FUnit nu = unit_at(ui + 1, utab, U1, pcur, pl, mt1, mt2);
                         if (!nu.g2)
                             tma_prefetch_4d_w(&tm_w13p, 0, nu.u.m * 128, 0, nu.u.e);
                         else if (f.w2w)
@@ -677,6 +708,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                         else
                             tma_prefetch_2d_w(&tm_w2, 0, nu.u.e * H + nu.u.m * 128);
                     }
+                    if (threadIdx.x == 0) FSTRACE(14, ui);
                     if (!fu.g2) {
                         ok = produce_unit<false, 1>(p, ring, issued, &tm_w13p, &tm_aq, cu.m * 128, cu.e, cu.row0,
                                                     ws.as + (size_t)cu.g * kt1 * 512, kt1, pol_w, pol_b, ew1, pi1);
@@ -746,7 +778,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             auto load_group = [&](uint4(&g)[2][4]) -> int {
                 if (q_ui >= my_units) return 0;
                 if (q_kk == 0) {
-                    const FUnit fu = fused_unit(blockIdx.x + q_ui * gridDim.x, U1, qcur, pl, mt1, mt2);
+                    const FUnit fu = unit_at(q_ui, utab, U1, qcur, pl, mt1, mt2);
                     q_g2 = fu.g2;
                     q_kt = fu.g2 ? kt2 : kt1;
                     q_ld = fu.g2 ? I / 32 : H / 32;
@@ -855,8 +887,9 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             long long aw1 = 0, aw2 = 0;  // accumulator wait ns
 #endif
             for (int ui = 0; ui < my_units; ++ui) {
-                const FUnit fu = fused_unit(blockIdx.x + ui * gridDim.x, U1, cur, pl, mt1, mt2);
+                const FUnit fu = unit_at(ui, utab, U1, cur, pl, mt1, mt2);
                 const int N = (fu.u.n + 15) & ~15;
+                if (w == 0 && lane == 0) FSTRACE(15, ui + (N > 1000 ? 1 : 0));
 #ifdef BMOE_TRACE
                 const long long ta0 = (long long)globaltimer_ns();
 #endif
@@ -904,7 +937,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             bool fused_g2_prev = false;
 #endif
             for (int ui = 0; ui < my_units; ++ui) {
-                const FUnit fu = fused_unit(blockIdx.x + ui * gridDim.x, U1, cur, pl, mt1, mt2);
+                const FUnit fu = unit_at(ui, utab, U1, cur, pl, mt1, mt2);
                 if (!mbar_wait(&accf[acc], acc_phase, abort_flag, ws.status, kStTimeout | (1u << (kSiteShift + 5)),
                                kWaitLimitNs))
                     break;

@@ -62,10 +62,10 @@ struct Cfg {
     static constexpr int B_BYTES = NT * 128;               // one row chunk in smem
     static constexpr int NB = (NT + 127) / 128;            // 128-row scale atoms per row chunk
     static constexpr int STAGE_BYTES = KC * (NA * A_BYTES + B_BYTES + (NA + NB) * 512);
-    static constexpr int TAB_E = 512;                      // experts whose plan fits the smem tables
-    static constexpr int TAB_BYTES = 4 * (3 * TAB_E + 4);
-    static constexpr int STAGES = (220 * 1024 - TAB_BYTES) / STAGE_BYTES > 12 ? 12
-                                                                             : (220 * 1024 - TAB_BYTES) / STAGE_BYTES;
+    static constexpr int UTAB = 384;                       // the CTA's first units, decoded once (16 bytes each)
+    static constexpr int UTAB_BYTES = 16 * UTAB;
+    static constexpr int STAGES = (220 * 1024 - UTAB_BYTES) / STAGE_BYTES > 12 ? 12
+                                                                              : (220 * 1024 - UTAB_BYTES) / STAGE_BYTES;
     // MMA issuers and their accumulator chains: 4 for the decode tile width (issue
     // bound); for 128-wide tiles GEMM1 keeps its gate/up pair and GEMM2 one chain,
     // so that GEMM2's accumulator can be double-buffered in TMEM.
@@ -90,7 +90,11 @@ struct Cfg {
     static constexpr int EPI_WARP0 = 2 + NI;
     static constexpr int THREADS = 32 * (2 + NI + EW);
     static constexpr int BAR_BYTES = (2 * STAGES + 4 + 4 + 1) * 8 + 16;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + TAB_BYTES + BAR_BYTES;
+    static constexpr int UTAB_OFF = (STAGES * STAGE_BYTES + BAR_BYTES + 15) & ~15;
+    static constexpr int SMEM = 1024 + UTAB_OFF + UTAB_BYTES;
+    // the plan's three tables are staged in the stage ring (idle until the pipeline starts) while
+    // the units are decoded
+    static_assert(STAGES * STAGE_BYTES >= 4 * 3 * (kMaxExperts + 1), "plan staging");
     static_assert(NUM_ACC * ACC_COLS <= SF_BASE, "TMEM columns");
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(4 % KS == 0, "K-steps per stage must split evenly");
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
     uint64_t* drain = acce + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int32_t* tab = reinterpret_cast<int32_t*>(sSFB + STAGES * KC * NB * 512 + C::BAR_BYTES);
+    int4* utab = reinterpret_cast<int4*>(sm + C::UTAB_OFF);  // [UTAB] decoded units of this CTA
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) trace_cta(a, 0);
@@ -181,14 +185,28 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
         (n_units - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1;
     const int KT = a.ktiles / KC;  // K stages per unit
 
-    Plan pl{a.tile_base, a.rowbase, a.counts};
-    if (a.E <= C::TAB_E) {
-        for (int i = threadIdx.x; i <= a.E; i += blockDim.x) {
-            tab[i] = __ldg(a.tile_base + i);
-            tab[C::TAB_E + 1 + i] = __ldg(a.rowbase + i);
-            if (i < a.E) tab[2 * C::TAB_E + 2 + i] = __ldg(a.counts + i);
+    // The CTA's units are decoded once (bisection per unit, one thread each) from a copy of the plan
+    // staged in the idle stage ring; units past the table, and the bounds check, read the global plan.
+    const Plan pl{a.tile_base, a.rowbase, a.counts};
+    {
+        int32_t* ptab = reinterpret_cast<int32_t*>(sA);
+        const int E = a.E;
+        for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+            ptab[i] = __ldg(a.tile_base + i);
+            ptab[E + 1 + i] = __ldg(a.rowbase + i);
+            if (i < E) ptab[2 * E + 2 + i] = __ldg(a.counts + i);
         }
-        pl = Plan{tab, tab + C::TAB_E + 1, tab + 2 * C::TAB_E + 2};
+        __syncthreads();
+        const Plan sp{ptab, ptab + E + 1, ptab + 2 * E + 2};
+#ifdef MOE_DEBUG_BOUNDS
+        const int n_tab = min(all_units, C::UTAB);
+#else
+        const int n_tab = min(my_units, C::UTAB);
+#endif
+        for (int i = threadIdx.x; i < n_tab; i += blockDim.x) {
+            const int u = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+            utab[i] = pack_unit(unit_of_expert(u, expert_of_unit(u, sp, a.mtiles, E), sp, a.mtiles, NT));
+        }
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -234,7 +252,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
             long issued = 0;
             bool ok = true;
             for (int ui = 0; ui < my_units && ok; ++ui) {
-                const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
+                const UnitInfo cu = unit_ref(ui, utab, C::UTAB, ecur, pl, a.mtiles, NT);
                 const int wrow = cu.e * a.w_rows + cu.m * a.m_rows;  // GEMM2 (GEMM1 reads the W13 pair view)
                 const uint8_t* b_sf = a.b_sf + static_cast<size_t>(cu.g) * a.ktiles * NB * 512;
                 for (int kk = 0; kk < KT; ++kk) {
@@ -309,7 +327,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
             auto gload = [&](V(&dst)[NV]) {
                 if (q_ui >= my_units) return;
                 if (q_g == 0) {
-                    const UnitInfo pu = decode_unit(blockIdx.x + q_ui * gridDim.x, q_ecur, pl, a.mtiles, NT);
+                    const UnitInfo pu = unit_ref(q_ui, utab, C::UTAB, q_ecur, pl, a.mtiles, NT);
                     q_src = a.w_sf +
                             (static_cast<size_t>(pu.e) * a.w_rows + (pu.m * a.m_rows + lane) * a.w_rs) * a.ld_sf;
                 }
@@ -381,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
             auto load_next = [&](uint32_t(&dst)[NW]) {
                 if (p_ui >= my_units) return;
                 if (p_kk == 0) {
-                    const UnitInfo pu = decode_unit(blockIdx.x + p_ui * gridDim.x, p_ecur, pl, a.mtiles, NT);
+                    const UnitInfo pu = unit_ref(p_ui, utab, C::UTAB, p_ecur, pl, a.mtiles, NT);
                     p_src = a.w_sf + (static_cast<size_t>(pu.e) * a.w_rows + (pu.m * a.m_rows + lane) * a.w_rs) * a.ld_sf;
                 }
     #pragma unroll
@@ -441,7 +459,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
         long job = 0;
         bool ok = true;
         for (int ui = 0; ui < my_units && ok; ++ui) {
-            const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
+            const UnitInfo cu = unit_ref(ui, utab, C::UTAB, ecur, pl, a.mtiles, NT);
             const int N = (cu.n + 15) & ~15;
             // ROT3: this warp's one chain (w = wi) uses slot (2 ui + wi) % 3, its (2 ui + wi) / 3-th use
             const int rq = 2 * ui + wi, rslot = rq % 3;
@@ -546,7 +564,7 @@ __global__ void __launch_bounds__(Cfg<G1, NT, KC, WIDE>::THREADS, 1)
         const bool clamp = L > 0.f;
         const bool tracer = warp == C::EPI_WARP0 && lane == 0;
         for (int ui = 0; ui < my_units; ++ui) {
-            const UnitInfo cu = decode_unit(blockIdx.x + ui * gridDim.x, ecur, pl, a.mtiles, NT);
+            const UnitInfo cu = unit_ref(ui, utab, C::UTAB, ecur, pl, a.mtiles, NT);
             const int feat = cu.m * 128 + 32 * q + lane;
             float v[CW];  // GEMM1: h = SwiGLU(gate, up); GEMM2: y
             float v2[WIDE && !C::ROT3 ? CW : 1];  // GEMM2 wide units without rotating slots: the second tile's y
