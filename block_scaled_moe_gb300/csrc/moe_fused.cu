@@ -17,8 +17,9 @@
 // arriving (equality, so the 32-bit word may wrap) and are bounded: on expiry
 // the CTA sets MOE_ST_TIMEOUT with a site bit and skips the remaining phases.
 //
-// GEMM tiles are the decode width (N <= 32 routed rows, 4 MMA-issuing warps
-// each owning an accumulator chain); a stage holds up to two 128x128 weight
+// GEMM tiles are the decode width (N <= 32 routed rows, 2 MMA-issuing warps
+// each owning an accumulator chain: GEMM1 gate / up, GEMM2 one W2 tile of a pair
+// or half of a stage's K-steps); a stage holds up to two 128x128 weight
 // chunks (GEMM1: gate and up; GEMM2: two 128-wide K chunks) and two row chunks.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -34,8 +35,8 @@
 // CTAs 0 and 1, clock64 stamps [2 CTAs][16 events][4096 stages]: 0 producer got
 // a free stage, 1 producer issued it, 2 MMA chain 0 saw it full, 3 chain 0
 // issued, 4 weight-scale warp got it, 5 that warp filled it, 6 producer began
-// waiting for it, 7 / 8 / 9 chains 1 / 2 / 3 issued, 10 chain 0 began waiting for
-// it, 11 chain 3 saw it full; per unit (index = the CTA's unit number): 12 producer
+// waiting for it, 7 / 8 / 9 chains 1 / 2 / 3 (those there are) issued, 10 chain 0 began
+// waiting for it, 11 the last chain saw it full; per unit (index = the CTA's unit number): 12 producer
 // entered the unit, 13 producer decoded it, 14 producer issued its prefetch, 15 chain 0
 // decoded it (stamps 13 and 15 take an index that depends on the decoded unit, so that
 // they follow the decode) (bmoe_fused_stage_trace_copy).
@@ -66,7 +67,7 @@ namespace bmoe {
 namespace {
 
 constexpr int F_NT = 32;                                    // route tile width
-constexpr int F_MW = 4;                                     // accumulator chains = MMA-issuing warps
+constexpr int F_MW = 2;                                     // accumulator chains = MMA-issuing warps
 constexpr int F_EW = 4;                                     // epilogue warps (one per TMEM lane quadrant)
 constexpr int F_MMA_WARP0 = 2, F_EPI_WARP0 = 2 + F_MW;
 constexpr int F_THREADS = 32 * (2 + F_MW + F_EW);
@@ -292,9 +293,12 @@ __device__ __forceinline__ bool produce_unit(const P1& p, Ring& r, long& issued,
 template <bool G2, int KC>
 __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w, int lane, uint32_t d_tmem, int N,
                                          int kt, long long& wait_ns, long long& issue_ns) {
-    static_assert(F_MW == 4 && (KC == 1 || KC == 2), "each chain's K-steps lie in one chunk");
-    const int ach = G2 ? (w * KC) >> 2 : (w & 1);  // weight chunk (GEMM1: operand) of this chain
-    const int bch = G2 ? (w * KC) >> 2 : 0;        // row chunk of this chain
+    constexpr int SPC = 4 * KC / F_MW;   // GEMM2: consecutive K-steps of a chain per stage
+    constexpr int KSPLIT = F_MW / 2;     // GEMM1: chains per operand (K-steps split by k % KSPLIT)
+    static_assert((F_MW == 2 || F_MW == 4) && (KC == 1 || KC == 2) && SPC >= 1 && SPC <= 4,
+                  "each chain's K-steps lie in one chunk");
+    const int ach = G2 ? (w * SPC) >> 2 : (w & 1);  // weight chunk (GEMM1: operand) of this chain
+    const int bch = G2 ? (w * SPC) >> 2 : 0;        // row chunk of this chain
     for (int kk = 0; kk < kt; ++kk) {
 #ifdef BMOE_TRACE
         const long long tw0 = (long long)globaltimer_ns();
@@ -307,7 +311,7 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
         const long long tw1 = (long long)globaltimer_ns();
         wait_ns += tw1 - tw0;
         if (w == 0 && lane == 0) FSTRACE(2, job);
-        if (w == 3 && lane == 0) FSTRACE(11, job);
+        if (w == F_MW - 1 && lane == 0) FSTRACE(11, job);
 #else
         (void)wait_ns;
         (void)issue_ns;
@@ -324,15 +328,15 @@ __device__ __forceinline__ bool mma_unit(const P1& p, Ring& r, long& job, int w,
                 const int kq = w >> 1;
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4) {
-                    if ((k4 & 1) != kq) continue;
+                    if (k4 % KSPLIT != kq) continue;
                     tc_mma_mx_w(d_tmem, da0 + static_cast<uint64_t>((k4 * 32) >> 4),
                                 db0 + static_cast<uint64_t>((k4 * 32) >> 4), idesc_mx(128, N, 5, 0, k4, k4), sfa, sfb,
                                 (kk > 0 || k4 != kq) ? 1u : 0u);
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < KC; ++j) {
-                    const int k4 = (w * KC + j) & 3;
+                for (int j = 0; j < SPC; ++j) {
+                    const int k4 = (w * SPC + j) & 3;
                     tc_mma_mx_w(d_tmem, da0 + static_cast<uint64_t>((k4 * 32) >> 4),
                                 db0 + static_cast<uint64_t>((k4 * 32) >> 4), idesc_mx(128, N, 5, 0, k4, k4), sfa, sfb,
                                 (kk > 0 || j > 0) ? 1u : 0u);

@@ -69,7 +69,7 @@ struct Cfg {
     // MMA issuers and their accumulator chains: 4 for the decode tile width (issue
     // bound); for 128-wide tiles GEMM1 keeps its gate/up pair and GEMM2 one chain,
     // so that GEMM2's accumulator can be double-buffered in TMEM.
-    static constexpr int MW = NT <= 64 ? 4 : (PAIR ? 2 : 1);
+    static constexpr int MW = NT <= 64 ? 2 : (PAIR ? 2 : 1);
     static constexpr int NI = MW;                          // MMA-issuing warps (chain w is issued by warp w % NI)
     static constexpr int KS = PAIR ? MW / 2 : MW;          // K-steps of a stage split over KS chains per operand
     static constexpr int EW = NT <= 64 ? 4 : 8;            // epilogue warps (EW/4 per TMEM lane quadrant)

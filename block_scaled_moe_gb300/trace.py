@@ -91,7 +91,8 @@ FUSED_STAGE_EVENTS = 16
 def fused_stage_trace(lib) -> np.ndarray:
     """[2 CTAs][16][4096] clock64 per K stage: 0 producer got a free stage, 1 issued it, 2 MMA chain 0 saw it
     full, 3 chain 0 issued, 4 weight-scale warp got it, 5 that warp filled it, 6 producer began waiting for
-    it, 7 / 8 / 9 chains 1 / 2 / 3 issued, 10 chain 0 began waiting for it, 11 chain 3 saw it full; per unit
+    it, 7 / 8 / 9 chains 1 / 2 / 3 (those there are) issued, 10 chain 0 began waiting for it, 11 the last
+    chain saw it full; per unit
     of the CTA: 12 producer entered it, 13 decoded it, 14 issued its prefetch, 15 chain 0 decoded it."""
     buf = np.zeros(2 * FUSED_STAGE_EVENTS * FUSED_STAGES, np.int64)
     lib.bmoe_fused_stage_trace_copy.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
