@@ -133,13 +133,22 @@ int make_map(moe_ctx* h, CUtensorMap* m, CUtensorMapDataType dt, const void* bas
     return MOE_OK;
 }
 
+// L2 promotion of a weight map: a box reads 64 bytes of each weight row per K stage, and 256-byte
+// promotion fetches four stages of a row at once.  Where the row pitch is not a multiple of 256
+// bytes (e.g. W2 rows of I/2 = 1152 bytes), a row's last promoted block is shared with the next
+// row and measured ~3% extra DRAM reads on the single-launch decode (the streamed lines are
+// evict-first); such maps promote 128 bytes.
+CUtensorMapL2promotion weight_promotion(uint64_t row_bytes) {
+    return row_bytes % 256 == 0 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
+}
+
 // W13 as a 4D view (K, output feature j, half: gate / up, expert) so that one box
 // {128, 128, 2, 1} brings the gate tile and the matching up tile of a unit's K
 // chunk: a GEMM1 stage is one TMA.  Concatenated halves: feature stride one row,
 // half stride I rows; interleaved rows (gate j at 2j, up j at 2j + 1): feature
 // stride two rows, half stride one row.
 int make_map_w13_pair(moe_ctx* h, CUtensorMap* m, const void* base, uint64_t H, uint64_t I, uint64_t E,
-                      bool interleaved) {
+                      bool interleaved, CUtensorMapL2promotion l2) {
     auto fn = encode_fn();
     if (!fn) return fail(h, MOE_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const uint64_t row = H / 2;
@@ -148,8 +157,7 @@ int make_map_w13_pair(moe_ctx* h, CUtensorMap* m, const void* base, uint64_t H, 
     cuuint32_t box[4] = {128, 128, 2, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(h, MOE_ECUDA, "cuTensorMapEncodeTiled failed (%d) for the W13 pair view", (int)r);
     return MOE_OK;
 }
@@ -352,16 +360,17 @@ int prepare_binding(moe_handle h, Binding* b, const void* w13_fp4, const void* w
     if ((rc = check_device_ptr(h, w2_sf, "w2_sf", 16))) return rc;
     const Geometry& g = h->geo;
     const bool inter = h->opt_w13_layout == MOE_W13_INTERLEAVED;
-    if ((rc = make_map_w13_pair(h, &b->tm_w13p, w13_fp4, g.H, g.I, g.E, inter))) return rc;
+    if ((rc = make_map_w13_pair(h, &b->tm_w13p, w13_fp4, g.H, g.I, g.E, inter, weight_promotion(g.H / 2)))) return rc;
+    const CUtensorMapL2promotion w2p = weight_promotion(g.I / 2);
     if ((rc = make_map(h, &b->tm_w2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2_fp4, g.I, (uint64_t)g.E * g.H, g.I / 2,
-                       128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
+                       128, w2p)))
         return rc;
     if ((rc = make_map(h, &b->tm_w2w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2_fp4, g.I, (uint64_t)g.E * g.H, g.I / 2,
-                       256, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
+                       256, w2p)))
         return rc;
     if (g.I % 256 == 0 &&
         (rc = make_map_k2(h, &b->tm_w2k2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2_fp4, g.I, (uint64_t)g.E * g.H,
-                          g.I / 2, 64, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
+                          g.I / 2, 64, 128, w2p)))
         return rc;
     b->w13_layout = h->opt_w13_layout;
     b->w13 = static_cast<const uint8_t*>(w13_fp4);
