@@ -143,9 +143,9 @@ def workload_bytes_flops(w, ids):
 
 
 # source files of each kernel whose ncu traffic figure is committed under profiles/
-KERNEL_SOURCES = {
-    "gemm1": ("moe_gemm.cu", "gemm_common.cuh", "ptx.cuh"),
-    "fused": ("moe_fused.cu", "gemm_common.cuh", "layer_rows.cuh", "ptx.cuh"),
+KERNEL_SOURCES = {  # the kernels' sources and the launcher that builds their tensor maps
+    "gemm1": ("moe_gemm.cu", "gemm_common.cuh", "ptx.cuh", "moe_api.cu"),
+    "fused": ("moe_fused.cu", "gemm_common.cuh", "layer_rows.cuh", "ptx.cuh", "moe_api.cu"),
 }
 
 
