@@ -133,14 +133,13 @@ int make_map(moe_ctx* h, CUtensorMap* m, CUtensorMapDataType dt, const void* bas
     return MOE_OK;
 }
 
-// L2 promotion of a weight map: a box reads 64 bytes of each weight row per K stage, and 256-byte
-// promotion fetches four stages of a row at once.  Where the row pitch is not a multiple of 256
-// bytes (e.g. W2 rows of I/2 = 1152 bytes), a row's last promoted block is shared with the next
-// row and measured ~3% extra DRAM reads on the single-launch decode (the streamed lines are
-// evict-first); such maps promote 128 bytes.
-CUtensorMapL2promotion weight_promotion(uint64_t row_bytes) {
-    return row_bytes % 256 == 0 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
-}
+// L2 promotion of the weight maps: a box reads 64 bytes of each weight row per K stage.  With
+// 256-byte promotion one stage in four fetched four stages of every row from DRAM and the ring
+// waited on it, and where the row pitch is not a multiple of 256 bytes (W2 rows of I/2 = 1152
+// bytes) a row's last promoted block, shared with the next row, was read twice (~3% extra DRAM
+// bytes on the single-launch decode).  128-byte promotion measured faster on every workload
+// (decode -1.1%, small-M -0.7%, 8192-row prefill -1.3 to -1.7%, skewed prefill +-0.3%).
+CUtensorMapL2promotion weight_promotion(uint64_t /*row_bytes*/) { return CU_TENSOR_MAP_L2_PROMOTION_L2_128B; }
 
 // W13 as a 4D view (K, output feature j, half: gate / up, expert) so that one box
 // {128, 128, 2, 1} brings the gate tile and the matching up tile of a unit's K
