@@ -121,6 +121,36 @@ def summarize_fused_stages(st: np.ndarray, n_g1: int) -> list:
     return lines
 
 
+def transition_costs(st: np.ndarray, cta: int, n1: int, n_units: int, kt1: int, kt2: int) -> dict:
+    """Unit transitions of one traced CTA (cycles, medians over its units after the first), per GEMM:
+    the producer from its last issue of a unit to entering the next (`enter`), decoding it (`decode`),
+    issuing the prefetch of the unit after it (`prefetch`), and from there to starting the wait for the
+    new unit's first stage (`to_wait`, which holds the GEMM2 readiness wait); the MMA warp from its last
+    issue to having decoded the next unit (`mma_decode`) and then to starting its first wait
+    (`mma_to_wait`); and the period of chain 0 at the unit's first stage against the median period
+    (`first_period`, `period`).  Unit u of the CTA starts at stage sum(kt of units < u); its first n1
+    units are GEMM1 units of kt1 stages, the rest GEMM2 units of kt2."""
+    s = st[cta].astype(np.int64)
+    P1, M0, M1, PW, MW0 = s[1], s[2], s[3], s[6], s[10]
+    U0, U1, U2, UM = s[12], s[13], s[14], s[15]
+    starts = np.cumsum([0] + [kt1 if u < n1 else kt2 for u in range(n_units - 1)])
+    n_stages = int((M1 > 0).sum())
+    out = {}
+    for name, units in (("GEMM1", np.arange(1, n1)), ("GEMM2", np.arange(n1 + 1, n_units))):
+        units = units[starts[units] < n_stages]
+        if len(units) == 0:
+            continue
+        b = starts[units]
+        med = lambda a: float(np.median(a))
+        periods = np.diff(M0[:n_stages])
+        out[name] = {"units": int(len(units)), "enter": med(U0[units] - P1[b - 1]),
+                     "decode": med(U1[units] - U0[units]), "prefetch": med(U2[units] - U1[units]),
+                     "to_wait": med(PW[b] - U2[units]), "mma_decode": med(UM[units] - M1[b - 1]),
+                     "mma_to_wait": med(MW0[b] - UM[units]), "first_period": med(M0[b] - M0[b - 1]),
+                     "period": med(periods)}
+    return out
+
+
 def summarize_fused(t: np.ndarray) -> list:
     t = t.astype(np.float64)
     base = t[:, 0].min()
@@ -173,7 +203,15 @@ def main(argv=None) -> int:
     if L.last_path == "fused":
         ft = fused_trace(lib, n_sms)
         fs = fused_stage_trace(lib)
-        lines = summarize_fused(ft) + summarize_fused_stages(fs, int(ft[0, 11]) * (w.H // 128))
+        n1 = int(ft[0, 11])
+        lines = summarize_fused(ft) + summarize_fused_stages(fs, n1 * (w.H // 128))
+        kt2 = w.I // 128 if w.H % 256 == 0 else w.I // (256 if w.I % 256 == 0 else 128)
+        for name, c in transition_costs(fs, 0, n1, n1 + int(ft[0, 12]), w.H // 128, kt2).items():
+            lines.append(f"  CTA 0 {name} unit transitions (cycles, median over {c['units']} units): producer "
+                         f"enter {c['enter']:.0f}, decode {c['decode']:.0f}, prefetch {c['prefetch']:.0f}, to the "
+                         f"first wait {c['to_wait']:.0f}; MMA decode {c['mma_decode']:.0f}, to the first wait "
+                         f"{c['mma_to_wait']:.0f}; first-stage period {c['first_period']:.0f} against "
+                         f"{c['period']:.0f}")
         raw = {"fused_phases": ft, "fused_stages": fs}
     else:
         t = gemm_trace(lib, n_sms)
