@@ -13,10 +13,13 @@
 //     I+[128m,128m+128) of W13[e], K = H.  Epilogue: SwiGLU (optional clamp,
 //     ROCm/aiter PR #6154 "clamp-10 SwiGLU") and MXFP8 1x32 re-quantisation of
 //     h along I ("FP8 intermediate quantization", aiter #6154 Summary).
-//   GEMM2 unit = (route tile, tile m): rows [128m,128m+128) of W2[e], K = I.
-//     Epilogue: BF16 rows y (aiter #6881: GEMM2 rows go to the combine as BF16).
+//   GEMM2 unit = (route tile, tile m): rows [128m,128m+128) of W2[e], K = I; or,
+//     when H % 256 == 0, (route tile, pair m): rows [256m,256m+256), one 256-row
+//     box per K stage.  Epilogue: BF16 rows y (aiter #6881: GEMM2 rows go to the
+//     combine as BF16).
 //
-// Pipeline per CTA (persistent, one CTA per SM, units strided over the grid):
+// Pipeline per CTA (persistent, one CTA per SM, units strided over the grid; the
+// CTA's units are decoded once into a shared-memory table before the roles start):
 //   warp 0      TMA producer (one thread): TMA of the FP4 weight tile
 //               (16U4_ALIGN16B expands each 16 codes to 16 bytes in shared
 //               memory, the layout kind::mxf8f6f4 reads), TMA of the FP8 row
@@ -66,9 +69,11 @@ struct Cfg {
     static constexpr int UTAB_BYTES = 16 * UTAB;
     static constexpr int STAGES = (220 * 1024 - UTAB_BYTES) / STAGE_BYTES > 12 ? 12
                                                                               : (220 * 1024 - UTAB_BYTES) / STAGE_BYTES;
-    // MMA issuers and their accumulator chains: 4 for the decode tile width (issue
-    // bound); for 128-wide tiles GEMM1 keeps its gate/up pair and GEMM2 one chain,
-    // so that GEMM2's accumulator can be double-buffered in TMEM.
+    // MMA issuers and their accumulator chains: two for decode tiles (gate / up, the two
+    // tiles of a W2 pair, or the halves of a stage's K-steps: each chain copies its own
+    // scale atoms per stage, so more chains cost more copies than they save in issue) and
+    // for the prefill pairs; one for unpaired 128-wide GEMM2 tiles, so that GEMM2's
+    // accumulator can be double-buffered in TMEM.
     static constexpr int MW = NT <= 64 ? 2 : (PAIR ? 2 : 1);
     static constexpr int NI = MW;                          // MMA-issuing warps (chain w is issued by warp w % NI)
     static constexpr int KS = PAIR ? MW / 2 : MW;          // K-steps of a stage split over KS chains per operand
